@@ -1,0 +1,533 @@
+// C ABI of the fz library: argument checks, context-owned device memory and
+// the launch sequence of one batch (host side).
+//
+// EXTEND batch:  inspector (register window) -> inspector (wide band, only the
+// extensions that outgrew the window) -> classify + bin scatter + scans ->
+// [one read-back: bin counts, arena sizes] -> executor (both paths, chunked
+// when the direction-code arena would exceed its cap) -> CIGAR emission.
+// LOCAL batch:  local fill -> result records.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "fz_dev.cuh"
+#include "fz_kernels.h"
+
+using namespace fz;
+
+namespace {
+
+struct DevBuf {
+  void* p = nullptr;
+  size_t bytes = 0;
+  cudaError_t ensure(size_t need) {
+    if (need <= bytes) return cudaSuccess;
+    if (p) { cudaFree(p); p = nullptr; bytes = 0; }
+    size_t b = need + need / 4 + 256;
+    cudaError_t e = cudaMalloc(&p, b);
+    if (e != cudaSuccess) { p = nullptr; (void)cudaGetLastError(); return e; }
+    bytes = b;
+    return cudaSuccess;
+  }
+  void release() { if (p) cudaFree(p); p = nullptr; bytes = 0; }
+  template <class T> T* as() const { return static_cast<T*>(p); }
+};
+
+struct Counters {
+  unsigned long long live_total;
+  unsigned long long exec_total;
+  uint64_t trace_total;
+  uint64_t cig_total;
+  uint32_t work[4];
+  uint32_t wide_count;
+  uint32_t err;
+  uint32_t bin_count[8];
+  uint32_t bin_cursor[8];
+};
+
+constexpr uint64_t TRACE_CAP_DEFAULT = 8ull << 30;   // executor arena cap before chunking
+
+}  // namespace
+
+struct fz_ctx {
+  int device = 0;
+  int sms = 0;
+  fz_mode mode = FZ_EXTEND;
+  Params p{};
+  bool fast_ok = false;
+  uint32_t mcol[4] = {0, 0, 0, 0};
+  std::string err;
+  DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, counters;
+  DevBuf cigar, trace, scratch, spill;
+  DevBuf in_t, in_q, in_seeds, out_res;
+  Counters* h_cnt = nullptr;         // pinned
+  cudaStream_t last_stream = nullptr;
+  fz_stats stats{};
+  bool have_batch = false;
+  uint64_t trace_cap = TRACE_CAP_DEFAULT;
+  int grid_fast = 0, grid_fast_trace = 0, grid_wide = 0, grid_local = 0;
+  size_t local_smem = 0;
+  bool local_use_smem = true;
+  uint32_t launches = 0;
+  bool profiling = false;
+  cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool ev_set[6] = {false, false, false, false, false, false};
+};
+
+namespace {
+
+fz_status fail(fz_ctx* c, fz_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf;
+  return s;
+}
+
+#define CU(call)                                                                          \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess) {                                                              \
+      (void)cudaGetLastError();                                                           \
+      return fail(ctx, e_ == cudaErrorMemoryAllocation ? FZ_ERR_OOM : FZ_ERR_CUDA,        \
+                  "%s: %s", #call, cudaGetErrorString(e_));                               \
+    }                                                                                     \
+  } while (0)
+
+bool fault_injected(const char* what) {
+  const char* f = getenv("FZ_FAULT");
+  return f && strcmp(f, what) == 0;
+}
+
+fz_status ensure_batch_buffers(fz_ctx* ctx, uint32_t n_ext) {
+  const size_t n = std::max<uint32_t>(n_ext, 1);
+  if (fault_injected("alloc")) return fail(ctx, FZ_ERR_OOM, "allocation failure injected by FZ_FAULT=alloc");
+  CU(ctx->rec.ensure(n * sizeof(ExtRec)));
+  CU(ctx->ext_bin.ensure(n * 4));
+  CU(ctx->exec_list.ensure(n * 4));
+  CU(ctx->exec_pos.ensure(n * 4));
+  CU(ctx->trace_sz.ensure(n * 8));
+  CU(ctx->cig_cap.ensure(n * 8));
+  CU(ctx->scan_tmp.ensure((size_t)scan_tmp_elems((uint32_t)n) * 8));
+  CU(ctx->wide_list.ensure(n * 4));
+  CU(ctx->counters.ensure(sizeof(Counters)));
+  if (ctx->mode == FZ_EXTEND) {
+    const uint64_t per = wide_scratch_elems(ctx->p.max_len) * 4;
+    CU(ctx->scratch.ensure((size_t)ctx->grid_wide * wide_warps_per_block() * per));
+  } else if (!ctx->local_use_smem) {
+    const uint64_t per = 2ull * (ctx->p.max_len + 1) * 4;
+    CU(ctx->spill.ensure((size_t)ctx->grid_local * local_warps_per_block() * per));
+  }
+  return FZ_OK;
+}
+
+// Phase boundary k (0 = batch start, 1 inspector, 2 wide inspector, 3 bins and
+// scans, 4 executor, 5 emission) when profiling is on.
+void mark(fz_ctx* ctx, int k, cudaStream_t st) {
+  if (!ctx->profiling) return;
+  if (cudaEventRecord(ctx->ev[k], st) == cudaSuccess) ctx->ev_set[k] = true;
+}
+
+fz_status check_device_error(fz_ctx* ctx) {
+  if (ctx->h_cnt->err) return fail(ctx, FZ_ERR_DEVICE, "device check failed (code 0x%x)", ctx->h_cnt->err);
+  return FZ_OK;
+}
+
+fz_status run_local(fz_ctx* ctx, const fz_seed* d_seeds, uint32_t n_seeds, fz_result* d_out, cudaStream_t st) {
+  const uint32_t n_ext = 2 * n_seeds;
+  Counters* dc = ctx->counters.as<Counters>();
+  LocalArgs la{};
+  la.n_work = n_ext;
+  la.counter = &dc->work[0];
+  la.rec = ctx->rec.as<ExtRec>();
+  la.live_total = &dc->live_total;
+  la.spill = ctx->spill.as<int32_t>();
+  la.spill_stride = 2ull * (ctx->p.max_len + 1);
+  la.use_smem = ctx->local_use_smem ? 1 : 0;
+  memcpy(la.mcol, ctx->mcol, sizeof(la.mcol));
+  mark(ctx, 0, st);
+  CU(launch_local(ctx->p, la, ctx->grid_local, st));
+  ctx->launches += 1;
+  mark(ctx, 1, st);
+  EmitArgs ea{};
+  ea.rec = ctx->rec.as<ExtRec>();
+  ea.n_ext = n_ext;
+  ea.out = d_out;
+  ea.err = &dc->err;
+  ea.local = 1;
+  CU(launch_emit_direct(ea, st));
+  ctx->launches += 1;
+  mark(ctx, 5, st);
+  (void)d_seeds;
+  return FZ_OK;
+}
+
+fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream_t st) {
+  const uint32_t n_ext = 2 * n_seeds;
+  Counters* dc = ctx->counters.as<Counters>();
+  WorkArgs wa{};
+  wa.rec = ctx->rec.as<ExtRec>();
+  wa.wide_list = ctx->wide_list.as<uint32_t>();
+  wa.wide_count = &dc->wide_count;
+  wa.live_total = &dc->live_total;
+  wa.exec_total = &dc->exec_total;
+  wa.err = &dc->err;
+  wa.scratch = ctx->scratch.as<int32_t>();
+  wa.scratch_stride = wide_scratch_elems(ctx->p.max_len);
+
+  // 1. inspector
+  mark(ctx, 0, st);
+  if (ctx->fast_ok) {
+    wa.list = nullptr;
+    wa.n_work = n_ext;
+    wa.counter = &dc->work[0];
+    CU(launch_inspect_fast(ctx->p, wa, ctx->grid_fast, st));
+    mark(ctx, 1, st);
+    wa.list = ctx->wide_list.as<uint32_t>();
+    wa.counter = &dc->work[1];
+    CU(launch_inspect_wide(ctx->p, wa, ctx->grid_wide, st));
+    ctx->launches += 2;
+  } else {
+    // every extension takes the general path (scores outside the byte range)
+    std::vector<uint32_t> ids(n_ext);
+    for (uint32_t k = 0; k < n_ext; ++k) ids[k] = k;
+    CU(cudaMemcpyAsync(ctx->wide_list.p, ids.data(), (size_t)n_ext * 4, cudaMemcpyHostToDevice, st));
+    CU(cudaMemcpyAsync(&dc->wide_count, &n_ext, 4, cudaMemcpyHostToDevice, st));
+    CU(cudaStreamSynchronize(st));
+    mark(ctx, 1, st);
+    wa.list = ctx->wide_list.as<uint32_t>();
+    wa.counter = &dc->work[1];
+    CU(launch_inspect_wide(ctx->p, wa, ctx->grid_wide, st));
+    ctx->launches += 1;
+  }
+  mark(ctx, 2, st);
+
+  // 2. bins, executor work list, arena offsets
+  PipeArgs pa{};
+  pa.rec = ctx->rec.as<ExtRec>();
+  pa.n_ext = n_ext;
+  pa.ext_bin = ctx->ext_bin.as<uint32_t>();
+  pa.bin_count = dc->bin_count;
+  pa.bin_cursor = dc->bin_cursor;
+  pa.exec_list = ctx->exec_list.as<uint32_t>();
+  pa.exec_pos = ctx->exec_pos.as<uint32_t>();
+  pa.trace_sz = ctx->trace_sz.as<uint64_t>();
+  pa.cig_cap = ctx->cig_cap.as<uint64_t>();
+  pa.err = &dc->err;
+  pa.local = 0;
+  CU(cudaMemsetAsync(ctx->trace_sz.p, 0, (size_t)n_ext * 8, st));
+  CU(launch_classify(pa, st));
+  CU(launch_scatter(pa, st));
+  CU(launch_scan_u64(pa.cig_cap, n_ext, ctx->scan_tmp.as<uint64_t>(), &dc->cig_total, st));
+  CU(launch_scan_u64(pa.trace_sz, n_ext, ctx->scan_tmp.as<uint64_t>(), &dc->trace_total, st));
+  ctx->launches += 3 + 6;
+  mark(ctx, 3, st);
+  CU(cudaMemcpyAsync(ctx->h_cnt, dc, sizeof(Counters), cudaMemcpyDeviceToHost, st));
+  CU(cudaStreamSynchronize(st));
+  fz_status s = check_device_error(ctx);
+  if (s != FZ_OK) return s;
+  const Counters& hc = *ctx->h_cnt;
+  uint32_t n_exec = 0;
+  for (int k = 1; k <= 5; ++k) n_exec += hc.bin_count[k];
+  if (hc.cig_total >= (1ull << 32)) return fail(ctx, FZ_ERR_ARG, "CIGAR arena would exceed 2^32 runs; split the batch");
+  CU(ctx->cigar.ensure(std::max<uint64_t>(hc.cig_total, 1) * 4));
+  ctx->stats.trace_bytes = hc.trace_total;
+  ctx->stats.cigar_runs = hc.cig_total;
+
+  // 3. executor + traceback, chunked by the arena cap
+  std::vector<std::pair<uint32_t, uint32_t>> chunks;
+  std::vector<uint64_t> toff;
+  if (n_exec) {
+    if (hc.trace_total <= ctx->trace_cap) {
+      chunks.push_back({0u, n_exec});
+      CU(ctx->trace.ensure(std::max<uint64_t>(hc.trace_total, 16)));
+    } else {
+      toff.resize(n_exec + 1);
+      CU(cudaMemcpy(toff.data(), ctx->trace_sz.p, (size_t)n_exec * 8, cudaMemcpyDeviceToHost));
+      toff[n_exec] = hc.trace_total;
+      uint32_t a = 0;
+      while (a < n_exec) {
+        uint32_t b = a + 1;
+        while (b < n_exec && toff[b + 1] - toff[a] <= ctx->trace_cap) ++b;
+        if (toff[b] - toff[a] > ctx->trace_cap && b - a == 1) {
+          // a single extension larger than the cap: grow for it
+        }
+        chunks.push_back({a, b});
+        a = b;
+      }
+      uint64_t biggest = 16;
+      for (auto& c : chunks) biggest = std::max<uint64_t>(biggest, toff[c.second] - toff[c.first]);
+      CU(ctx->trace.ensure(biggest));
+    }
+  }
+  EmitArgs ea{};
+  ea.rec = ctx->rec.as<ExtRec>();
+  ea.n_ext = n_ext;
+  ea.cig_off = ctx->cig_cap.as<uint64_t>();
+  ea.cigar = ctx->cigar.as<uint32_t>();
+  ea.out = d_out;
+  ea.exec_list = ctx->exec_list.as<uint32_t>();
+  ea.trace_off = ctx->trace_sz.as<uint64_t>();
+  ea.trace = ctx->trace.as<uint8_t>();
+  ea.err = &dc->err;
+  ea.local = 0;
+  int slot = 2;
+  for (auto& c : chunks) {
+    const uint64_t sub = toff.empty() ? 0 : toff[c.first];
+    WorkArgs we = wa;
+    we.list = ctx->exec_list.as<uint32_t>() + c.first;
+    we.n_work = c.second - c.first;
+    we.trace = ctx->trace.as<uint8_t>();
+    we.trace_off = ctx->trace_sz.as<uint64_t>() + c.first;
+    we.trace_sub = sub;
+    if (slot + 1 >= 4) {
+      CU(cudaMemsetAsync(&dc->work[2], 0, 8, st));
+      slot = 2;
+    }
+    we.counter = &dc->work[slot];
+    if (ctx->fast_ok) {
+      CU(launch_execute_fast(ctx->p, we, ctx->grid_fast_trace, st));
+      ctx->launches += 1;
+    }
+    we.counter = &dc->work[slot + 1];
+    CU(launch_execute_wide(ctx->p, we, ctx->grid_wide, st));
+    ctx->launches += 1;
+    slot += 2;
+    if (chunks.size() > 1) {
+      EmitArgs ex = ea;
+      ex.exec_begin = c.first;
+      ex.exec_end = c.second;
+      ex.trace_sub = sub;
+      CU(launch_emit_exec(ex, st));
+      ctx->launches += 1;
+    }
+  }
+  mark(ctx, 4, st);
+  CU(launch_emit_direct(ea, st));
+  ctx->launches += 1;
+  if (chunks.size() == 1) {
+    EmitArgs ex = ea;
+    ex.exec_begin = 0;
+    ex.exec_end = n_exec;
+    ex.trace_sub = 0;
+    CU(launch_emit_exec(ex, st));
+    ctx->launches += 1;
+  }
+  mark(ctx, 5, st);
+  ctx->stats.eager = hc.bin_count[0];
+  for (int k = 0; k < 5; ++k) ctx->stats.bin[k] = hc.bin_count[k + 1];
+  ctx->stats.wide = hc.wide_count;
+  ctx->stats.extensions = hc.bin_count[7];
+  return FZ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32_t gap_extend, int32_t ydrop,
+                    int32_t max_len, fz_mode mode) {
+  fz_ctx* ctx = nullptr;
+  if (!out) return FZ_ERR_ARG;
+  *out = nullptr;
+  if (!sub || gap_open < 0 || gap_extend < 1 || (ydrop < 0 && ydrop != FZ_YDROP_INF) || max_len < 1 ||
+      max_len > FZ_MAX_LEN_LIMIT || (mode != FZ_EXTEND && mode != FZ_LOCAL))
+    return FZ_ERR_ARG;
+  int64_t amax = (int64_t)gap_open + gap_extend;
+  bool bytes = true;
+  for (int k = 0; k < 16; ++k) {
+    amax = std::max<int64_t>(amax, std::llabs((long long)sub[k]));
+    if (sub[k] < -128 || sub[k] > 127) bytes = false;
+  }
+  if (amax * (2 * (int64_t)max_len + 1) >= (1ll << 28)) return FZ_ERR_ARG;
+  if (mode == FZ_LOCAL && !bytes) return FZ_ERR_ARG;
+  ctx = new (std::nothrow) fz_ctx();
+  if (!ctx) return FZ_ERR_OOM;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
+    (void)cudaGetLastError();
+    delete ctx;
+    return FZ_ERR_CUDA;
+  }
+  ctx->mode = mode;
+  Params& p = ctx->p;
+  p.o = gap_open;
+  p.e = gap_extend;
+  p.oe = gap_open + gap_extend;
+  p.ydrop = ydrop;
+  p.max_len = max_len;
+  for (int k = 0; k < 16; ++k) p.sub[k] = sub[k];
+  ctx->fast_ok = bytes;
+  for (int t = 0; t < 4; ++t) {
+    uint32_t row = 0, col = 0;
+    for (int q = 0; q < 4; ++q) {
+      row |= (uint32_t)((bytes ? sub[t * 4 + q] : 0) + 128) << (8 * q);
+      col |= (uint32_t)((bytes ? sub[q * 4 + t] : 0) + 128) << (8 * q);
+    }
+    p.mrow[t] = row;
+    ctx->mcol[t] = col;
+  }
+  ctx->grid_fast = ctx->sms * extend_fast_blocks_per_sm(false);
+  ctx->grid_fast_trace = ctx->sms * extend_fast_blocks_per_sm(true);
+  ctx->grid_wide = ctx->sms;
+  ctx->local_smem = local_smem_bytes(max_len);
+  ctx->local_use_smem = ctx->local_smem <= 200 * 1024;
+  ctx->grid_local = ctx->sms * local_blocks_per_sm(ctx->local_use_smem ? ctx->local_smem : 0);
+  if (cudaMallocHost(&ctx->h_cnt, sizeof(Counters)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    delete ctx;
+    return FZ_ERR_OOM;
+  }
+  memset(ctx->h_cnt, 0, sizeof(Counters));
+  if (cudaGetLastError() != cudaSuccess) {
+    cudaFreeHost(ctx->h_cnt);
+    delete ctx;
+    return FZ_ERR_CUDA;
+  }
+  const char* cap = getenv("FZ_TRACE_CAP");
+  if (cap) ctx->trace_cap = std::max<uint64_t>(strtoull(cap, nullptr, 10), 4096);
+  *out = ctx;
+  return FZ_OK;
+}
+
+fz_status fz_extend_batch(fz_ctx* ctx, const uint8_t* d_target2, uint64_t t_len, const uint8_t* d_query2,
+                          uint64_t q_len, const fz_seed* d_seeds, uint32_t n_seeds, fz_result* d_out,
+                          const uint32_t** d_cigar, void* cuda_stream) {
+  if (!ctx) return FZ_ERR_ARG;
+  ctx->err.clear();
+  if (n_seeds && (!d_seeds || !d_out)) return fail(ctx, FZ_ERR_ARG, "null seeds or output with n_seeds > 0");
+  if ((t_len && !d_target2) || (q_len && !d_query2)) return fail(ctx, FZ_ERR_ARG, "null sequence with nonzero length");
+  if (n_seeds > 0x7fffffffu) return fail(ctx, FZ_ERR_ARG, "n_seeds too large");
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  CU(cudaSetDevice(ctx->device));
+  ctx->last_stream = st;
+  ctx->stats = fz_stats{};
+  ctx->have_batch = false;
+  ctx->launches = 0;
+  for (bool& b : ctx->ev_set) b = false;
+  const uint32_t n_ext = 2 * n_seeds;
+  fz_status s = ensure_batch_buffers(ctx, n_ext);
+  if (s != FZ_OK) return s;
+  if (d_cigar) *d_cigar = ctx->cigar.as<uint32_t>();
+  CU(cudaMemsetAsync(ctx->counters.p, 0, sizeof(Counters), st));
+  Params& p = ctx->p;
+  p.t2 = d_target2;
+  p.q2 = d_query2;
+  p.t_len = t_len;
+  p.q_len = q_len;
+  p.seeds = d_seeds;
+  p.n_seeds = n_seeds;
+  if (n_seeds == 0) {
+    ctx->have_batch = true;
+    return FZ_OK;
+  }
+  s = ctx->mode == FZ_LOCAL ? run_local(ctx, d_seeds, n_seeds, d_out, st) : run_extend(ctx, n_seeds, d_out, st);
+  if (s != FZ_OK) return s;
+  if (d_cigar) *d_cigar = ctx->cigar.as<uint32_t>();
+  ctx->have_batch = true;
+  return FZ_OK;
+}
+
+fz_status fz_extend_batch_host(fz_ctx* ctx, const uint8_t* h_target2, uint64_t t_len, const uint8_t* h_query2,
+                               uint64_t q_len, const fz_seed* h_seeds, uint32_t n_seeds, fz_result* h_out,
+                               uint32_t* h_cigar, uint64_t cigar_cap, uint64_t* cigar_used, void* cuda_stream) {
+  if (!ctx) return FZ_ERR_ARG;
+  ctx->err.clear();
+  if ((n_seeds && (!h_seeds || !h_out)) || (cigar_cap && !h_cigar))
+    return fail(ctx, FZ_ERR_ARG, "null host buffer");
+  if ((t_len && !h_target2) || (q_len && !h_query2)) return fail(ctx, FZ_ERR_ARG, "null sequence with nonzero length");
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  CU(cudaSetDevice(ctx->device));
+  const size_t tb = (t_len + 3) / 4, qb = (q_len + 3) / 4;
+  CU(ctx->in_t.ensure(std::max<size_t>(tb, 16)));
+  CU(ctx->in_q.ensure(std::max<size_t>(qb, 16)));
+  CU(ctx->in_seeds.ensure(std::max<size_t>((size_t)n_seeds * sizeof(fz_seed), 16)));
+  CU(ctx->out_res.ensure(std::max<size_t>((size_t)n_seeds * 2 * sizeof(fz_result), 16)));
+  if (tb) CU(cudaMemcpyAsync(ctx->in_t.p, h_target2, tb, cudaMemcpyHostToDevice, st));
+  if (qb) CU(cudaMemcpyAsync(ctx->in_q.p, h_query2, qb, cudaMemcpyHostToDevice, st));
+  if (n_seeds) CU(cudaMemcpyAsync(ctx->in_seeds.p, h_seeds, (size_t)n_seeds * sizeof(fz_seed), cudaMemcpyHostToDevice, st));
+  const uint32_t* dc = nullptr;
+  fz_status s = fz_extend_batch(ctx, ctx->in_t.as<uint8_t>(), t_len, ctx->in_q.as<uint8_t>(), q_len,
+                                ctx->in_seeds.as<fz_seed>(), n_seeds, ctx->out_res.as<fz_result>(), &dc, cuda_stream);
+  if (s != FZ_OK) return s;
+  if (n_seeds) CU(cudaMemcpyAsync(h_out, ctx->out_res.p, (size_t)n_seeds * 2 * sizeof(fz_result), cudaMemcpyDeviceToHost, st));
+  const uint64_t used = ctx->mode == FZ_EXTEND ? ctx->stats.cigar_runs : 0;
+  if (cigar_used) *cigar_used = used;
+  if (used && used <= cigar_cap) CU(cudaMemcpyAsync(h_cigar, dc, used * 4, cudaMemcpyDeviceToHost, st));
+  CU(cudaStreamSynchronize(st));
+  if (used > cigar_cap) return fail(ctx, FZ_ERR_ARG, "CIGAR needs %llu runs, buffer holds %llu",
+                                    (unsigned long long)used, (unsigned long long)cigar_cap);
+  return FZ_OK;
+}
+
+fz_status fz_get_stats(fz_ctx* ctx, fz_stats* out) {
+  if (!ctx || !out) return FZ_ERR_ARG;
+  if (!ctx->have_batch) return fail(ctx, FZ_ERR_ARG, "no completed batch");
+  CU(cudaSetDevice(ctx->device));
+  CU(cudaStreamSynchronize(ctx->last_stream));
+  CU(cudaMemcpy(ctx->h_cnt, ctx->counters.p, sizeof(Counters), cudaMemcpyDeviceToHost));
+  fz_status s = check_device_error(ctx);
+  ctx->stats.live_cells = ctx->h_cnt->live_total;
+  ctx->stats.exec_cells = ctx->h_cnt->exec_total;
+  ctx->stats.launches = ctx->launches;
+  ctx->stats.profiled = 0;
+  for (float& f : ctx->stats.phase_ms) f = 0.f;
+  if (ctx->profiling && ctx->ev_set[0]) {
+    ctx->stats.profiled = 1;
+    int prev = 0;
+    for (int k = 1; k <= 5; ++k) {
+      if (!ctx->ev_set[k]) continue;
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ctx->ev[prev], ctx->ev[k]) == cudaSuccess) ctx->stats.phase_ms[k - 1] = ms;
+      prev = k;
+    }
+    float tot = 0.f;
+    if (cudaEventElapsedTime(&tot, ctx->ev[0], ctx->ev[prev]) == cudaSuccess) ctx->stats.phase_ms[5] = tot;
+    (void)cudaGetLastError();
+  }
+  if (ctx->mode == FZ_LOCAL) {
+    ctx->stats.extensions = 0;
+  }
+  *out = ctx->stats;
+  return s;
+}
+
+fz_status fz_set_profiling(fz_ctx* ctx, int on) {
+  if (!ctx) return FZ_ERR_ARG;
+  CU(cudaSetDevice(ctx->device));
+  if (on && !ctx->ev[0]) {
+    for (int k = 0; k < 6; ++k) CU(cudaEventCreate(&ctx->ev[k]));
+  }
+  ctx->profiling = on != 0;
+  return FZ_OK;
+}
+
+const char* fz_last_error(fz_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+void fz_destroy(fz_ctx* ctx) {
+  if (!ctx) return;
+  cudaSetDevice(ctx->device);
+  DevBuf* bufs[] = {&ctx->rec, &ctx->ext_bin, &ctx->exec_list, &ctx->exec_pos, &ctx->trace_sz, &ctx->cig_cap,
+                    &ctx->scan_tmp, &ctx->wide_list, &ctx->counters, &ctx->cigar, &ctx->trace, &ctx->scratch,
+                    &ctx->spill, &ctx->in_t, &ctx->in_q, &ctx->in_seeds, &ctx->out_res};
+  for (DevBuf* b : bufs) b->release();
+  if (ctx->h_cnt) cudaFreeHost(ctx->h_cnt);
+  for (cudaEvent_t& e : ctx->ev)
+    if (e) cudaEventDestroy(e);
+  delete ctx;
+}
+
+fz_status fz_bench_int_rates(double rates[4]) {
+  if (!rates) return FZ_ERR_ARG;
+  return bench_int_rates(rates) == cudaSuccess ? FZ_OK : FZ_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,434 @@
+// Register-window anti-diagonal sweep: inspector and executor (sm_103a).
+//
+// One warp owns one extension at a time.  Lane l holds K consecutive rows of
+// the current anti-diagonal, rows b + l*K .. b + l*K + K-1 (a 32*K-row window
+// with base b), with per row: h = S - o - e of the current anti-diagonal, h of
+// the previous one (diagonal source), I, D, the substitution row of its
+// target base and the query selector of its column.  Stepping d -> d+1 either
+// keeps the base (rows gain one query column; data of the row above comes
+// from lane l-1 by shuffle) or moves it up by one row once row b is dead (the
+// row above each row is then the same slot of the previous step; data of the
+// row below comes from lane l+1).  Only the window's edges exchange values,
+// three shuffles per step, so scores never leave registers (FastZ section
+// 3.2's use-and-discard ring, in the anti-diagonal layout of its section 2.2).
+//
+// Y-drop: a cell is live when S >= best - ydrop, best being the maximum over
+// completed anti-diagonals (kept in a warp-uniform register after a warp max
+// reduction per step).  Only S is cleared on a pruned cell: I and D of a dead
+// cell are below the threshold and can never make a later cell live, and no
+// traceback path goes through them, so scores, ends and paths are those of
+// the strict recurrence.
+//
+// The executor is the same sweep stopped at the inspector's best cell's
+// anti-diagonal; it replays every threshold and window decision and stores a
+// 4-bit direction code per cell (FastZ section 3.1.3 stores the S/I/D choices
+// in 2+1+1 bits).
+#include <cuda_runtime.h>
+
+#include "fz_dev.cuh"
+#include "fz_kernels.h"
+
+namespace fz {
+
+namespace {
+
+constexpr int WARPS = 4;
+
+struct Reservoir {          // warp-uniform stream of bases
+  uint64_t res;
+  uint32_t pend;
+  int32_t cnt;
+  int64_t next;
+};
+
+__device__ __forceinline__ void res_init(Reservoir& r, const uint8_t* s, uint64_t len, int64_t g0, int dir,
+                                         int64_t first) {
+  r.res = fetch16(s, len, g0, dir, first);
+  r.pend = fetch16(s, len, g0, dir, first + 16);
+  r.cnt = 16;
+  r.next = first + 32;
+}
+
+__device__ __forceinline__ uint32_t res_take(Reservoir& r, const uint8_t* s, uint64_t len, int64_t g0, int dir) {
+  const uint32_t b = (uint32_t)r.res & 3u;
+  r.res >>= 2;
+  if (--r.cnt < 16) {
+    r.res |= (uint64_t)r.pend << (2 * r.cnt);
+    r.cnt += 16;
+    r.pend = fetch16(s, len, g0, dir, r.next);
+    r.next += 16;
+  }
+  return b;
+}
+
+__device__ __forceinline__ int32_t hi_row(uint32_t mask, int32_t base, int K) {
+  return mask ? base + (32 - __clz(mask)) * K - 1 : -0x7fffffff;
+}
+__device__ __forceinline__ int32_t lo_row(uint32_t mask, int32_t base, int K) {
+  return mask ? base + (__ffs(mask) - 1) * K : 0x7fffffff;
+}
+
+// Eager traceback inside the 16x16 corner (FastZ section 3.1.2): recompute
+// cells (i, j), i, j <= 16, with the sweep's thresholds, lane = row, then walk
+// back from (bi, bj).  Returns the walk as 2-bit ops, first op = last column.
+__device__ void eager_corner(const Params& p, const Window& w, int lane, const int32_t* sT,
+                             uint8_t* tile, const int32_t* s_sub, int32_t bi, int32_t bj,
+                             uint64_t& path, uint32_t& npath, uint32_t* err) {
+  const int32_t dstar = bi + bj;
+  const int i = lane;
+  const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, 1);
+  const uint32_t qw = fetch16(p.q2, p.q_len, w.qg0, w.dir, 1);
+  const int tb = i >= 1 ? (int)((tw >> (2 * ((i - 1) & 15))) & 3u) : 0;
+  const int32_t oe = p.oe, e = p.e;
+  int32_t Sp = i == 0 ? 0 : NEG, Ip = NEG, Dp = NEG, Spp = NEG;
+  for (int d = 1; d <= dstar; ++d) {
+    const int j = d - i;
+    int32_t su = __shfl_up_sync(FULL, Sp, 1);
+    int32_t du = __shfl_up_sync(FULL, Dp, 1);
+    int32_t sd = __shfl_up_sync(FULL, Spp, 1);
+    if (lane == 0) { su = NEG; du = NEG; sd = NEG; }
+    const int32_t Ic = j >= 1 ? imax(Ip - e, Sp - oe) : NEG;
+    const int32_t Dc = i >= 1 ? imax(du - e, su - oe) : NEG;
+    int32_t G = NEG;
+    if (i >= 1 && j >= 1 && j <= EAGER_N) G = sd + s_sub[tb * 4 + (int)((qw >> (2 * (j - 1))) & 3u)];
+    const int32_t S = imax(G, imax(Ic, Dc));
+    const bool valid = j >= 0 && j <= w.n && i <= w.m && i <= EAGER_N && j <= EAGER_N;
+    const bool alive = valid && S >= sT[d];
+    if (valid) {
+      const uint32_t sc = G == S ? 0u : (Ic == S ? 1u : 2u);
+      const uint32_t io = (j >= 1 && Ic == Sp - oe) ? 4u : 0u;
+      const uint32_t dop = (i >= 1 && Dc == su - oe) ? 8u : 0u;
+      tile[i * (EAGER_N + 1) + j] = (uint8_t)(sc | io | dop);
+    }
+    Spp = Sp;
+    Sp = alive ? S : NEG;
+    Ip = alive ? Ic : NEG;
+    Dp = alive ? Dc : NEG;
+  }
+  __syncwarp();
+  uint64_t code = 0;
+  uint32_t k = 0;
+  if (lane == 0) {
+    int ci = bi, cj = bj, st = 0;
+    int guard = 4 * EAGER_N + 4;
+    while ((ci > 0 || cj > 0) && k < 2 * EAGER_N && --guard > 0) {
+      const uint32_t c = tile[ci * (EAGER_N + 1) + cj];
+      if (st == 0) {
+        const uint32_t sc = c & 3u;
+        if (sc == 0 && ci > 0 && cj > 0) { ++k; --ci; --cj; }   // op M = 0
+        else if (sc == 1 && cj > 0) st = 1;
+        else if (sc == 2 && ci > 0) st = 2;
+        else { atomicOr(err, 8u); break; }
+      } else if (st == 1) {
+        if (cj <= 0) { atomicOr(err, 8u); break; }
+        code |= 1ull << (2 * k); ++k;
+        st = (c & 4u) ? 0 : 1;
+        --cj;
+      } else {
+        if (ci <= 0) { atomicOr(err, 8u); break; }
+        code |= 2ull << (2 * k); ++k;
+        st = (c & 8u) ? 0 : 2;
+        --ci;
+      }
+    }
+  }
+  path = __shfl_sync(FULL, code, 0);
+  npath = __shfl_sync(FULL, k, 0);
+  __syncwarp();
+}
+
+// Register state of one lane: K consecutive rows of the window.
+template <int K>
+struct LaneState {
+  int32_t H[K], HP[K], I[K], D[K];
+  uint32_t MR[K];
+  uint32_t QP[K / 2];
+};
+
+struct StepIn {
+  int32_t Th;          // threshold on h = S - o - e for the new anti-diagonal
+  int32_t vhi, vlo;    // edge mode: slot r is inside the window iff vlo <= r <= vhi
+  int32_t oe, ne, c1;
+  uint32_t qb;         // NOSHIFT: query base entering lane 0
+  uint32_t mr_new;     // SHIFT: substitution row entering lane 31
+};
+
+// One anti-diagonal step.  Returns the lane max of the pruned h; cnt counts
+// live cells; packed receives the direction codes in TRACE mode.
+template <int K, bool TRACE, bool SHIFT, bool EDGE>
+__device__ __forceinline__ int32_t step(LaneState<K>& L, const StepIn& in, int lane, uint32_t& cnt,
+                                        uint64_t& packed) {
+  constexpr int KH = K / 2;
+  int32_t lm = NEG;
+  if (!SHIFT) {
+    const int32_t dtop = __viaddmax_s32(L.D[K - 1], in.ne, L.H[K - 1]);
+    int32_t dc_top = __shfl_up_sync(FULL, dtop, 1);
+    int32_t hp_top = __shfl_up_sync(FULL, L.HP[K - 1], 1);
+    uint32_t qs_top = __shfl_up_sync(FULL, L.QP[KH - 1] >> 16, 1);
+    int32_t hu_top = 0;
+    if (TRACE) hu_top = __shfl_up_sync(FULL, L.H[K - 1], 1);
+    if (lane == 0) { dc_top = NEG; hp_top = NEG; qs_top = 0x4440u | in.qb; hu_top = NEG; }
+#pragma unroll
+    for (int k = KH - 1; k >= 1; --k) L.QP[k] = __funnelshift_l(L.QP[k - 1], L.QP[k], 16);
+    L.QP[0] = (L.QP[0] << 16) | qs_top;
+#pragma unroll
+    for (int r = K - 1; r >= 0; --r) {
+      const int32_t hl = L.H[r];
+      const int32_t Ic = __viaddmax_s32(L.I[r], in.ne, hl);
+      const int32_t Dc = r ? __viaddmax_s32(L.D[r - 1], in.ne, L.H[r - 1]) : dc_top;
+      const int32_t hp = r ? L.HP[r - 1] : hp_top;
+      const uint32_t sel = (r & 1) ? (L.QP[r >> 1] >> 16) : L.QP[r >> 1];
+      const int32_t G = hp + (int32_t)prmt(L.MR[r], 0u, sel) + in.c1;
+      const int32_t S = __vimax3_s32(G, Ic, Dc);
+      const int32_t hn = S - in.oe;
+      bool alive = hn >= in.Th;
+      if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
+      if (TRACE) {
+        const int32_t hu = r ? L.H[r - 1] : hu_top;
+        const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
+        packed |= (uint64_t)code << (4 * r);
+      }
+      L.HP[r] = hl;
+      L.H[r] = alive ? hn : NEG;
+      L.I[r] = Ic;
+      L.D[r] = Dc;
+      lm = imax(lm, L.H[r]);
+      cnt += alive ? 1u : 0u;
+    }
+  } else {
+    const int32_t itop = __viaddmax_s32(L.I[0], in.ne, L.H[0]);
+    int32_t ic_top = __shfl_down_sync(FULL, itop, 1);
+    int32_t h_top = __shfl_down_sync(FULL, L.H[0], 1);
+    uint32_t mr_top = __shfl_down_sync(FULL, L.MR[0], 1);
+    if (lane == 31) { ic_top = NEG; h_top = NEG; mr_top = in.mr_new; }
+#pragma unroll
+    for (int r = 0; r < K - 1; ++r) L.MR[r] = L.MR[r + 1];
+    L.MR[K - 1] = mr_top;
+#pragma unroll
+    for (int r = 0; r < K; ++r) {
+      const int32_t hl = r < K - 1 ? L.H[r + 1] : h_top;
+      const int32_t Ic = r < K - 1 ? __viaddmax_s32(L.I[r + 1], in.ne, L.H[r + 1]) : ic_top;
+      const int32_t hu = L.H[r];
+      const int32_t Dc = __viaddmax_s32(L.D[r], in.ne, hu);
+      const int32_t hp = L.HP[r];
+      const uint32_t sel = (r & 1) ? (L.QP[r >> 1] >> 16) : L.QP[r >> 1];
+      const int32_t G = hp + (int32_t)prmt(L.MR[r], 0u, sel) + in.c1;
+      const int32_t S = __vimax3_s32(G, Ic, Dc);
+      const int32_t hn = S - in.oe;
+      bool alive = hn >= in.Th;
+      if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
+      if (TRACE) {
+        const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
+        packed |= (uint64_t)code << (4 * r);
+      }
+      L.HP[r] = hl;
+      L.H[r] = alive ? hn : NEG;
+      L.I[r] = Ic;
+      L.D[r] = Dc;
+      lm = imax(lm, L.H[r]);
+      cnt += alive ? 1u : 0u;
+    }
+  }
+  return lm;
+}
+
+template <int K, bool TRACE>
+__device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint32_t idx, int lane,
+                        int32_t* sT, uint8_t* tile, const uint32_t* s_mrow, const int32_t* s_sub) {
+  static_assert(K == 16, "one 16-base fetch per lane");
+  constexpr int KH = K / 2;
+  constexpr int32_t WIN = 32 * K;
+  const Window w = make_window(p, ext);
+  ExtRec* R = wa.rec + ext;
+  if (!w.requested) {
+    if (!TRACE && lane == 0) {
+      ExtRec z = {};
+      *R = z;
+    }
+    return;
+  }
+  const int32_t m = w.m, n = w.n, oe = p.oe;
+  int32_t d_stop = 0x7fffffff;
+  uint8_t* tbase = nullptr;
+  int32_t* lo_arr = nullptr;
+  if (TRACE) {
+    d_stop = R->i_end + R->j_end;
+    tbase = wa.trace + (wa.trace_off[idx] - wa.trace_sub);
+    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(WIN, d_stop));
+    if (lane == 0) lo_arr[0] = 0;
+  }
+
+  LaneState<K> L;
+  {
+    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * K);
+#pragma unroll
+    for (int r = 0; r < K; ++r) {
+      L.MR[r] = s_mrow[(tw >> (2 * r)) & 3u];
+      L.H[r] = NEG; L.HP[r] = NEG; L.I[r] = NEG; L.D[r] = NEG;
+    }
+#pragma unroll
+    for (int k = 0; k < KH; ++k) L.QP[k] = 0x44404440u;
+    if (lane == 0) L.H[0] = -oe;                       // origin: S(0,0) = 0
+  }
+  Reservoir qr, tr;
+  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);        // query columns 1, 2, ...
+  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);      // target rows WIN, WIN+1, ...
+
+  StepIn in;
+  in.oe = oe;
+  in.ne = -p.e;
+  in.c1 = oe - 128;
+  int32_t b = 0, b_prev = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
+  uint32_t lmask = 1u, lmask_prev = 0u;
+  bool live = true, live_prev = false, rowb_alive = true;
+  uint32_t cnt = lane == 0 ? 1u : 0u;
+  bool overflow = false;
+
+  for (;;) {
+    const int32_t dn = d + 1;
+    if (dn > m + n || d >= d_stop) break;
+    const bool shift = !rowb_alive;
+    const int32_t bn = b + (shift ? 1 : 0);
+    if (!TRACE && !shift && (((lmask >> 31) & 1u) || (b_prev == b && ((lmask_prev >> 31) & 1u)))) {
+      overflow = true;   // the live band may grow past the window top
+      break;
+    }
+    const int32_t T = threshold(best, p.ydrop);
+    in.Th = T - oe;
+    const bool edge = (bn + WIN - 1 > m && (hi_row(lmask, b, K) >= m || hi_row(lmask_prev, b_prev, K) >= m)) ||
+                      lo_row(lmask, b, K) <= d - n || lo_row(lmask_prev, b_prev, K) <= d - 1 - n;
+    const int32_t rowbase = bn + lane * K;
+    in.vhi = m - rowbase;
+    in.vlo = dn - n - rowbase;
+    uint64_t packed = 0;
+    int32_t lm;
+    if (!shift) {
+      in.qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
+      lm = edge ? step<K, TRACE, false, true>(L, in, lane, cnt, packed)
+                : step<K, TRACE, false, false>(L, in, lane, cnt, packed);
+    } else {
+      in.mr_new = s_mrow[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+      lm = edge ? step<K, TRACE, true, true>(L, in, lane, cnt, packed)
+                : step<K, TRACE, true, false>(L, in, lane, cnt, packed);
+    }
+
+    const int32_t wm = __reduce_max_sync(FULL, lm);
+    const uint32_t mask = __ballot_sync(FULL, lm >= in.Th);
+    const uint32_t rb = __ballot_sync(FULL, L.H[0] >= in.Th) & 1u;
+    const bool any = mask != 0u;
+    if (any) {
+      d_last = dn;
+      const int32_t sbest = wm + oe;
+      if (sbest > best) {
+        int rf = K;
+#pragma unroll
+        for (int r = K - 1; r >= 0; --r) rf = (L.H[r] == wm) ? r : rf;
+        const uint32_t fm = __ballot_sync(FULL, rf < K);
+        const int Ln = __ffs(fm) - 1;
+        const int rr = __shfl_sync(FULL, rf, Ln);
+        bi = bn + Ln * K + rr;
+        bj = dn - bi;
+        best = sbest;
+      }
+    }
+    if (!TRACE && dn <= 2 * EAGER_N && lane == 0) sT[dn] = T;
+    if (TRACE) {
+      *reinterpret_cast<uint64_t*>(tbase + (uint64_t)dn * (WIN / 2) + lane * (K / 2)) = packed;
+      if (lane == 0) lo_arr[dn] = bn;
+    }
+    lmask_prev = lmask; lmask = mask;
+    b_prev = b; b = bn;
+    live_prev = live; live = any;
+    rowb_alive = rb != 0u;
+    d = dn;
+    if (!live && !live_prev) break;
+  }
+
+  // live-cell count of this sweep
+  uint64_t tot = cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+
+  if (TRACE) {
+    if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)tot);
+    return;
+  }
+  if (overflow) {
+    if (lane == 0) {
+      ExtRec z = {};
+      z.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE;
+      z.m = m;
+      z.n = n;
+      *R = z;
+      const uint32_t slot = atomicAdd(wa.wide_count, 1u);
+      wa.wide_list[slot] = ext;
+    }
+    return;
+  }
+  uint64_t path = 0;
+  uint32_t npath = 0;
+  uint32_t flags = FZ_FLAG_DONE;
+  uint32_t width = WIN;
+  if (bi <= EAGER_N && bj <= EAGER_N) {
+    flags |= FZ_FLAG_EAGER;
+    width = 0;
+    if (bi + bj > 0) eager_corner(p, w, lane, sT, tile, s_sub, bi, bj, path, npath, wa.err);
+  }
+  if (lane == 0) {
+    ExtRec o;
+    o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
+    o.live = tot; o.path = path; o.flags = flags; o.npath = npath;
+    o.m = m; o.n = n; o.width = width; o.pad = 0;
+    *R = o;
+    atomicAdd(wa.live_total, (unsigned long long)tot);
+  }
+}
+
+template <int K, bool TRACE>
+__global__ void __launch_bounds__(WARPS * 32) k_extend(Params p, WorkArgs wa) {
+  __shared__ int32_t s_T[WARPS][2 * EAGER_N + 1];
+  __shared__ uint8_t s_tile[WARPS][(EAGER_N + 1) * (EAGER_N + 1)];
+  __shared__ uint32_t s_mrow[4];
+  __shared__ int32_t s_sub[16];
+  if (threadIdx.x < 4) s_mrow[threadIdx.x] = p.mrow[threadIdx.x];
+  if (threadIdx.x < 16) s_sub[threadIdx.x] = p.sub[threadIdx.x];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (;;) {
+    uint32_t idx = 0;
+    if (lane == 0) idx = atomicAdd(wa.counter, 1u);
+    idx = __shfl_sync(FULL, idx, 0);
+    if (idx >= wa.n_work) break;
+    uint32_t ext = wa.list ? wa.list[idx] : idx;
+    if (TRACE) {
+      // executor: this kernel takes the register-window extensions only
+      if (wa.rec[ext].flags & FZ_FLAG_WIDE) continue;
+    }
+    run_ext<K, TRACE>(p, wa, ext, idx, lane, s_T[warp], s_tile[warp], s_mrow, s_sub);
+  }
+}
+
+}  // namespace
+
+int fast_window_rows() { return 32 * 16; }
+
+cudaError_t launch_inspect_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
+  k_extend<16, false><<<grid, WARPS * 32, 0, st>>>(p, wa);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_execute_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
+  k_extend<16, true><<<grid, WARPS * 32, 0, st>>>(p, wa);
+  return cudaGetLastError();
+}
+
+int extend_fast_blocks_per_sm(bool trace) {
+  int nb = 0;
+  if (trace)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<16, true>, WARPS * 32, 0);
+  else
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<16, false>, WARPS * 32, 0);
+  return nb > 0 ? nb : 1;
+}
+
+}  // namespace fz

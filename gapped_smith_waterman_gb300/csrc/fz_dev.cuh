@@ -1,0 +1,123 @@
+// Device-side definitions shared by the fz kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+
+#include "fz.h"
+
+namespace fz {
+
+constexpr int32_t NEG = -(1 << 30);       // dead / missing score
+constexpr int32_t TFLOOR = -(1 << 29);    // lowest threshold: every reachable cell is above it
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int EAGER_N = 16;               // eager traceback corner: i*, j* <= 16
+
+// Per-extension record written by the inspector, read by binning, the
+// executor and the traceback.
+struct ExtRec {
+  int32_t score, i_end, j_end, d_last;    // best S, its cell, last anti-diagonal with a live cell
+  uint64_t live;                          // live cells of the sweep
+  uint64_t path;                          // eager traceback: ops walking back, 2 bits each
+  uint32_t flags;                         // FZ_FLAG_*
+  uint32_t npath;                         // ops in path
+  int32_t m, n;                           // window sizes
+  uint32_t width;                         // executor trace row width (cells), 0 = no executor
+  uint32_t pad;
+};
+static_assert(sizeof(ExtRec) == 56, "ExtRec layout");
+
+struct Params {
+  const uint8_t* t2;
+  const uint8_t* q2;
+  uint64_t t_len, q_len;
+  const fz_seed* seeds;
+  uint32_t n_seeds;
+  int32_t o, e, oe;
+  int32_t ydrop;          // >= 0, or FZ_YDROP_INF
+  int32_t max_len;
+  uint32_t mrow[4];       // fast path: byte q of mrow[t] = sub[t][q] + 128
+  int32_t sub[16];
+};
+
+// Where one-sided extension `ext` (= 2 * seed + side, side 0 right, 1 left)
+// reads its bases: window index w (1-based) sits at genomic position
+// g0 + dir * w in each sequence.
+struct Window {
+  int64_t tg0, qg0;
+  int dir;
+  int32_t m, n;
+  bool requested;
+};
+
+__device__ __forceinline__ Window make_window(const Params& p, uint32_t ext) {
+  Window w;
+  const fz_seed s = p.seeds[ext >> 1];
+  const bool left = ext & 1u;
+  w.requested = (s.side & (left ? FZ_SIDE_LEFT : FZ_SIDE_RIGHT)) != 0;
+  const uint64_t tp = s.t_pos < p.t_len ? s.t_pos : p.t_len;
+  const uint64_t qp = s.q_pos < p.q_len ? s.q_pos : p.q_len;
+  const uint64_t ta = left ? tp : p.t_len - tp;
+  const uint64_t qa = left ? qp : p.q_len - qp;
+  w.m = (int32_t)(ta < (uint64_t)p.max_len ? ta : (uint64_t)p.max_len);
+  w.n = (int32_t)(qa < (uint64_t)p.max_len ? qa : (uint64_t)p.max_len);
+  w.dir = left ? -1 : 1;
+  w.tg0 = left ? (int64_t)tp : (int64_t)tp - 1;
+  w.qg0 = left ? (int64_t)qp : (int64_t)qp - 1;
+  if (!w.requested) { w.m = 0; w.n = 0; }
+  return w;
+}
+
+// 16 bases of a window starting at window index w: base w+k at bits 2k.
+// Positions outside the sequence read as 0 (callers never score them).
+__device__ __forceinline__ uint32_t fetch16(const uint8_t* __restrict__ s, uint64_t len, int64_t g0,
+                                            int dir, int64_t w) {
+  const int64_t lo = dir > 0 ? g0 + w : g0 - w - 15;   // lowest genomic position covered
+  const int64_t b0 = lo >> 2;                           // floor division
+  const int sh = (int)(lo & 3) * 2;
+  const int64_t nbytes = (int64_t)((len + 3) >> 2);
+  uint64_t v = 0;
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int64_t bi = b0 + k;
+    const uint32_t byte = (bi >= 0 && bi < nbytes) ? (uint32_t)__ldg(s + bi) : 0u;
+    v |= (uint64_t)byte << (8 * k);
+  }
+  const uint32_t fw = (uint32_t)(v >> sh);              // genomic lo .. lo+15, forward
+  if (dir > 0) return fw;
+  const uint32_t r = __brev(fw);                        // reverse the order of the 2-bit fields
+  return ((r >> 1) & 0x55555555u) | ((r & 0x55555555u) << 1);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ int32_t imax(int32_t a, int32_t b) { return a > b ? a : b; }
+__device__ __forceinline__ int32_t imin(int32_t a, int32_t b) { return a < b ? a : b; }
+
+// Prune threshold for an anti-diagonal from the best score of the completed
+// ones.  ydrop = INF (or huge) clamps to TFLOOR, below every reachable score.
+__device__ __forceinline__ int32_t threshold(int32_t best, int32_t ydrop) {
+  if (ydrop < 0) return TFLOOR;
+  const int64_t t = (int64_t)best - (int64_t)ydrop;
+  return t < (int64_t)TFLOOR ? TFLOOR : (int32_t)t;
+}
+
+// Trace arena layout of one executor extension: (d_end + 1) rows of `width`
+// 4-bit cells (row d covers rows lo[d] .. lo[d] + width - 1 of anti-diagonal
+// d), then (d_end + 1) int32 row origins.  Cell code: bits 0-1 S choice
+// (0 diag, 1 I, 2 D), bit 2 I opens here, bit 3 D opens here.
+// Every size is a multiple of 16 bytes, so each extension's base (a prefix sum
+// of sizes) stays 16-byte aligned for the executor's 8-byte stores.
+__host__ __device__ __forceinline__ uint64_t trace_lo_offset(uint32_t width, int32_t d_end) {
+  const uint64_t rows = (uint64_t)d_end + 1;
+  return (rows * (uint64_t)(width / 2) + 15) & ~uint64_t(15);
+}
+__host__ __device__ __forceinline__ uint64_t trace_bytes(uint32_t width, int32_t d_end) {
+  const uint64_t rows = (uint64_t)d_end + 1;
+  return trace_lo_offset(width, d_end) + ((rows * 4 + 15) & ~uint64_t(15));
+}
+
+}  // namespace fz

@@ -1,0 +1,96 @@
+// Kernel launchers of the fz library (host-side declarations).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "fz_dev.cuh"
+
+namespace fz {
+
+struct WorkArgs {
+  const uint32_t* list;        // extension ids, or nullptr for 0 .. n_work-1
+  uint32_t n_work;
+  uint32_t* counter;           // dynamic work counter, zeroed before the launch
+  ExtRec* rec;
+  uint32_t* wide_list;         // inspector: extensions whose band outgrew the register window
+  uint32_t* wide_count;
+  uint8_t* trace;              // executor: direction-code arena
+  const uint64_t* trace_off;   // executor: byte offset per work item
+  uint64_t trace_sub;          // executor: subtracted from trace_off (chunked runs)
+  unsigned long long* live_total;
+  unsigned long long* exec_total;
+  uint32_t* err;               // device error word (0 = fine)
+  int32_t* scratch;            // wide path: per-warp anti-diagonal buffers
+  uint64_t scratch_stride;     // int32 elements per warp
+};
+
+// register-window sweep (extend_fast.cu)
+int fast_window_rows();
+cudaError_t launch_inspect_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+cudaError_t launch_execute_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+int extend_fast_blocks_per_sm(bool trace);
+
+// general band sweep (extend_wide.cu)
+uint64_t wide_scratch_elems(int32_t max_len);   // per warp
+int wide_warps_per_block();
+cudaError_t launch_inspect_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+cudaError_t launch_execute_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+
+// local fill (local.cu)
+struct LocalArgs {
+  uint32_t n_work;
+  uint32_t* counter;
+  ExtRec* rec;
+  unsigned long long* live_total;
+  int32_t* spill;              // global spill rows when not in shared memory
+  uint64_t spill_stride;       // int32 elements per warp
+  int use_smem;
+  uint32_t mcol[4];            // byte t of mcol[q] = sub[t][q] + 128
+};
+int local_warps_per_block();
+size_t local_smem_bytes(int32_t max_len);
+cudaError_t launch_local(const Params& p, const LocalArgs& la, int grid, cudaStream_t st);
+int local_blocks_per_sm(size_t smem);
+
+// binning, scans and CIGAR emission (pipeline.cu)
+struct PipeArgs {
+  ExtRec* rec;
+  uint32_t n_ext;
+  uint32_t* ext_bin;           // per extension: 0 none / eager, 1..5 executor bin
+  uint32_t* bin_count;         // [8]: 0 eager, 1..5 bins, 6 unused, 7 requested
+  uint32_t* bin_cursor;        // [8]
+  uint32_t* exec_list;         // executor order: bins 5, 4, .., 1
+  uint32_t* exec_pos;          // per extension: index in exec_list
+  uint64_t* trace_sz;          // per exec item
+  uint64_t* cig_cap;           // per extension
+  uint32_t* err;
+  int local;
+};
+cudaError_t launch_classify(const PipeArgs& a, cudaStream_t st);
+cudaError_t launch_scatter(const PipeArgs& a, cudaStream_t st);
+// exclusive scan of n uint64 values in place; total written to *total
+cudaError_t launch_scan_u64(uint64_t* data, uint32_t n, uint64_t* block_tmp, uint64_t* total, cudaStream_t st);
+uint32_t scan_tmp_elems(uint32_t n);
+
+struct EmitArgs {
+  const ExtRec* rec;
+  const Params* dummy;
+  uint32_t n_ext;
+  const uint64_t* cig_off;     // per extension
+  uint32_t* cigar;             // arena
+  fz_result* out;
+  const uint32_t* exec_list;
+  const uint64_t* trace_off;   // per exec item
+  const uint8_t* trace;
+  uint64_t trace_sub;
+  uint32_t exec_begin, exec_end;
+  uint32_t* err;
+  int local;
+};
+cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st);   // eager, empty, local, not requested
+cudaError_t launch_emit_exec(const EmitArgs& a, cudaStream_t st);     // executor items [exec_begin, exec_end)
+
+// integer pipe microbenchmark (microbench.cu)
+cudaError_t bench_int_rates(double rates[4]);
+
+}  // namespace fz

@@ -1,0 +1,196 @@
+// Unpruned local fill, score and end cell only (sm_103a).
+//
+// Recurrence with a zero floor (the local cell of the DPX intrinsics article,
+// section 1.1, with affine gaps):
+//   E(i,j) = max(E(i,j-1) - e, H(i,j-1) - o - e)
+//   F(i,j) = max(F(i-1,j) - e, H(i-1,j) - o - e)
+//   H(i,j) = max(0, H(i-1,j-1) + M[t_i][q_j], E(i,j), F(i,j))
+// H = 0 and E = F = NEG on row and column 0.  Result: max H, earliest cell by
+// (i + j, then i).
+//
+// One warp per pair.  The query is cut into strips of 32 * KC columns; in a
+// strip lane l owns KC consecutive columns and works on row i = tau - l + 1 at
+// step tau (a wavefront across lanes), so each step needs only H and E of the
+// column left of its block, from lane l-1 by shuffle.  The column between two
+// strips is kept per row in a spill buffer (shared memory when it fits).  H
+// and F of a lane's columns stay in registers; the substitution score is one
+// byte permute of the column's 4-byte score profile by the row's target base.
+// The DPX 3-way max with ReLU does the zero floor for free.
+#include <cuda_runtime.h>
+
+#include "fz_dev.cuh"
+#include "fz_kernels.h"
+
+namespace fz {
+
+namespace {
+
+constexpr int WL = 4;          // warps per block
+constexpr int KC = 32;         // columns per lane
+constexpr int SW = 32 * KC;    // strip width
+
+struct Res {
+  uint64_t res;
+  uint32_t pend;
+  int32_t cnt;
+  int64_t next;
+};
+
+__device__ __forceinline__ void rinit(Res& r, const uint8_t* s, uint64_t len, int64_t g0, int dir, int64_t first) {
+  r.res = fetch16(s, len, g0, dir, first);
+  r.pend = fetch16(s, len, g0, dir, first + 16);
+  r.cnt = 16;
+  r.next = first + 32;
+}
+
+__device__ __forceinline__ uint32_t rtake(Res& r, const uint8_t* s, uint64_t len, int64_t g0, int dir) {
+  const uint32_t b = (uint32_t)r.res & 3u;
+  r.res >>= 2;
+  if (--r.cnt < 16) {
+    r.res |= (uint64_t)r.pend << (2 * r.cnt);
+    r.cnt += 16;
+    r.pend = fetch16(s, len, g0, dir, r.next);
+    r.next += 16;
+  }
+  return b;
+}
+
+template <bool PARTIAL>
+__device__ __forceinline__ void strip(const Params& p, const Window& w, int lane, int32_t s, int32_t nstrips,
+                                      const uint32_t* s_mcol, int32_t* spH, int32_t* spE, int32_t& bv,
+                                      int32_t& bd, int32_t& bi) {
+  const int32_t m = w.m, n = w.n, oe = p.oe, ne = -p.e;
+  const int32_t c0 = s * SW + lane * KC + 1;
+  const int32_t kv = imax(0, imin(KC, n - c0 + 1));
+  uint32_t QPF[KC];
+  int32_t Hc[KC], F[KC];
+  {
+    const uint32_t q0 = fetch16(p.q2, p.q_len, w.qg0, w.dir, c0);
+    const uint32_t q1 = fetch16(p.q2, p.q_len, w.qg0, w.dir, c0 + 16);
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      const uint32_t qb = ((k < 16 ? q0 : q1) >> (2 * (k & 15))) & 3u;
+      QPF[k] = s_mcol[qb];
+      Hc[k] = 0;
+      F[k] = NEG;
+    }
+  }
+  Res tr;
+  rinit(tr, p.t2, p.t_len, w.tg0, w.dir, 1);
+  int32_t h_out = 0, e_out = NEG, hh_prev = 0;
+  uint32_t t_cur = 0;
+  const bool first = s == 0, last = s == nstrips - 1;
+  for (int32_t tau = 0; tau < m + 31; ++tau) {
+    const int32_t i = tau - lane + 1;
+    int32_t hh = __shfl_up_sync(FULL, h_out, 1);
+    int32_t eh = __shfl_up_sync(FULL, e_out, 1);
+    uint32_t tb = __shfl_up_sync(FULL, t_cur, 1);
+    const uint32_t t0 = rtake(tr, p.t2, p.t_len, w.tg0, w.dir);
+    if (lane == 0) {
+      tb = t0;
+      if (first) { hh = 0; eh = NEG; }
+      else if (i <= m) { hh = spH[i]; eh = spE[i]; }
+    }
+    if (i >= 1 && i <= m) {
+      const uint32_t tsel = 0x4440u | tb;
+      int32_t E = eh, hl = hh, hd = hh_prev, rmax = 0;
+#pragma unroll
+      for (int k = 0; k < KC; ++k) {
+        E = __viaddmax_s32(E, ne, hl - oe);
+        F[k] = __viaddmax_s32(F[k], ne, Hc[k] - oe);
+        const int32_t G = hd + (int32_t)prmt(QPF[k], 0u, tsel) - 128;
+        int32_t H = __vimax3_s32_relu(G, E, F[k]);
+        if (PARTIAL) H = k < kv ? H : 0;
+        hd = Hc[k];
+        Hc[k] = H;
+        hl = H;
+        rmax = imax(rmax, H);
+      }
+      h_out = hl;
+      e_out = E;
+      if (rmax >= bv && rmax > 0) {
+        int kf = KC;
+#pragma unroll
+        for (int k = KC - 1; k >= 0; --k) kf = Hc[k] == rmax ? k : kf;
+        const int32_t c = c0 + kf, d = i + c;
+        if (rmax > bv || d < bd || (d == bd && i < bi)) { bv = rmax; bd = d; bi = i; }
+      }
+      if (lane == 31 && !last) { spH[i] = hl; spE[i] = E; }
+    }
+    hh_prev = hh;
+    t_cur = tb;
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(WL * 32) k_local(Params p, LocalArgs la) {
+  extern __shared__ int32_t smem[];
+  __shared__ uint32_t s_mcol[4];
+  if (threadIdx.x < 4) s_mcol[threadIdx.x] = la.mcol[threadIdx.x];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t cap = p.max_len + 1;
+  int32_t* sp = la.use_smem ? smem + (size_t)warp * 2 * cap
+                            : la.spill + ((uint64_t)blockIdx.x * WL + warp) * la.spill_stride;
+  int32_t* spH = sp;
+  int32_t* spE = sp + cap;
+  for (;;) {
+    uint32_t ext = 0;
+    if (lane == 0) ext = atomicAdd(la.counter, 1u);
+    ext = __shfl_sync(FULL, ext, 0);
+    if (ext >= la.n_work) break;
+    const Window w = make_window(p, ext);
+    ExtRec* R = la.rec + ext;
+    if (!w.requested) {
+      if (lane == 0) { ExtRec z = {}; *R = z; }
+      continue;
+    }
+    int32_t bv = 0, bd = 0, bi = 0;
+    const int32_t nstrips = (w.n + SW - 1) / SW;
+    if (w.m > 0) {
+      for (int32_t s = 0; s < nstrips; ++s) {
+        const bool partial = (s + 1) * SW > w.n;
+        if (partial) strip<true>(p, w, lane, s, nstrips, s_mcol, spH, spE, bv, bd, bi);
+        else strip<false>(p, w, lane, s, nstrips, s_mcol, spH, spE, bv, bd, bi);
+      }
+    }
+    const int32_t wm = __reduce_max_sync(FULL, bv);
+    const uint32_t dmin = __reduce_min_sync(FULL, bv == wm ? (uint32_t)bd : 0xffffffffu);
+    const uint32_t imn = __reduce_min_sync(FULL, (bv == wm && (uint32_t)bd == dmin) ? (uint32_t)bi : 0xffffffffu);
+    if (lane == 0) {
+      ExtRec o;
+      o.score = wm;
+      o.i_end = wm > 0 ? (int32_t)imn : 0;
+      o.j_end = wm > 0 ? (int32_t)dmin - (int32_t)imn : 0;
+      o.d_last = w.m + w.n;
+      o.live = (uint64_t)w.m * (uint64_t)w.n;
+      o.path = 0; o.flags = FZ_FLAG_DONE; o.npath = 0;
+      o.m = w.m; o.n = w.n; o.width = 0; o.pad = 0;
+      *R = o;
+      atomicAdd(la.live_total, (unsigned long long)o.live);
+    }
+  }
+}
+
+}  // namespace
+
+int local_warps_per_block() { return WL; }
+size_t local_smem_bytes(int32_t max_len) { return (size_t)WL * 2 * (size_t)(max_len + 1) * sizeof(int32_t); }
+
+int local_blocks_per_sm(size_t smem) {
+  int nb = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_local, WL * 32, smem);
+  return nb > 0 ? nb : 1;
+}
+
+cudaError_t launch_local(const Params& p, const LocalArgs& la, int grid, cudaStream_t st) {
+  const size_t smem = la.use_smem ? local_smem_bytes(p.max_len) : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_local<<<grid, WL * 32, smem, st>>>(p, la);
+  return cudaGetLastError();
+}
+
+}  // namespace fz

@@ -1,0 +1,173 @@
+/*
+ * fz -- batched gapped seed extension on one GB300 (sm_103a).  C ABI.
+ *
+ * The method is the gapped extension stage of seed-and-extend whole-genome
+ * alignment: from each seed anchor, a one-sided affine-gap (S/I/D) dynamic
+ * program with y-drop pruning, followed by a traceback of the best cell
+ * (FastZ: Accelerating Gapped Whole Genome Alignment on GPUs, sections 2.1,
+ * 2.2 and 3.1-3.4).  A second mode runs an unpruned, zero-floored local fill
+ * that returns the best score and its cell (the local recurrence of the DPX
+ * intrinsics article, section 1.1, with affine gaps).
+ *
+ * Recurrence, for window cells (i, j) (i indexes the target, j the query):
+ *   I(i,j) = max(I(i,j-1) - e, S(i,j-1) - o - e)
+ *   D(i,j) = max(D(i-1,j) - e, S(i-1,j) - o - e)
+ *   S(i,j) = max(S(i-1,j-1) + M[t_i][q_j], I(i,j), D(i,j))
+ * with S(0,0) = 0; a gap of k bases costs o + k*e.  Anti-diagonals d = i + j
+ * are swept in order; a cell on d is pruned when S < best - ydrop, best being
+ * the maximum S over live cells of anti-diagonals < d; a cell with no live
+ * predecessor is dead; the sweep ends when two consecutive anti-diagonals hold
+ * no live cell.  The result is the maximum live S (ties: smallest i + j, then
+ * smallest i) and the traceback from it (ties: diagonal > I > D; a gap opens
+ * rather than extends on a tie).
+ *
+ * All device pointers are caller-owned device memory unless stated; every
+ * call is asynchronous on the given CUDA stream except where a host read-back
+ * is documented.  No function throws; errors are status codes, and
+ * fz_last_error() gives a one-line message for the context.
+ */
+#ifndef FZ_H
+#define FZ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fz_ctx fz_ctx;
+
+typedef enum {
+    FZ_OK = 0,
+    FZ_ERR_ARG = 1,     /* invalid argument (null, out of range, capacity too small) */
+    FZ_ERR_OOM = 2,     /* device or host allocation failed; nothing leaked */
+    FZ_ERR_CUDA = 3,    /* a CUDA runtime call failed */
+    FZ_ERR_DEVICE = 4   /* a kernel reported an internal check failure */
+} fz_status;
+
+typedef enum {
+    FZ_EXTEND = 0,      /* one-sided y-drop extension with traceback */
+    FZ_LOCAL = 1        /* unpruned local fill, score and end cell only */
+} fz_mode;
+
+#define FZ_YDROP_INF (-1)   /* ydrop value meaning "never prune" */
+#define FZ_SIDE_RIGHT 1u
+#define FZ_SIDE_LEFT 2u
+#define FZ_SIDE_BOTH 3u
+#define FZ_MAX_LEN_LIMIT (1 << 20)
+
+/* result flags */
+#define FZ_FLAG_DONE 1u         /* extension was requested and computed */
+#define FZ_FLAG_EAGER 2u        /* end cell inside the 16x16 corner: traced in the inspector */
+#define FZ_FLAG_WIDE 4u         /* live band wider than the register window: general path */
+#define FZ_FLAG_BIN_SHIFT 4     /* bits 4..7: executor bin 1..5 (0 = none) */
+
+/* One seed anchor.  Right side: window t[t_pos ..], q[q_pos ..] (t[t_pos] is
+ * window index 1).  Left side: window read backwards from t[t_pos-1],
+ * q[q_pos-1].  Bases of the anchor itself are not scored. */
+typedef struct {
+    uint64_t t_pos, q_pos;
+    uint32_t side;          /* FZ_SIDE_RIGHT, FZ_SIDE_LEFT or FZ_SIDE_BOTH */
+} fz_seed;                  /* 24 bytes */
+
+/* One per seed and side: out[2k] = right, out[2k+1] = left of seed k. */
+typedef struct {
+    int32_t score;          /* best live S (>= 0); 0 if not requested */
+    int32_t t_end, q_end;   /* i*, j*: target / query bases consumed from the anchor */
+    uint32_t cigar_off;     /* first run in the CIGAR arena */
+    uint32_t cigar_len;     /* runs; each run is (len << 4) | op, op 0 = M, 1 = I, 2 = D,
+                               in forward genomic order (right: anchor outward;
+                               left: leftmost base first) */
+    uint32_t flags;         /* FZ_FLAG_* */
+} fz_result;                /* 24 bytes */
+
+typedef struct {
+    uint64_t live_cells;    /* live cells of all inspector sweeps (EXTEND) or m*n cells (LOCAL) */
+    uint64_t exec_cells;    /* cells the executor recomputed */
+    uint32_t eager;         /* extensions traced back inside the inspector */
+    uint32_t bin[5];        /* executor bins: max(i*, j*) <= 512, 2048, 8192, 32768, 131072 */
+    uint32_t extensions;    /* one-sided extensions computed */
+    uint32_t wide;          /* extensions that ran on the general (wide band) path */
+    uint64_t trace_bytes;   /* executor direction-bit arena used */
+    uint64_t cigar_runs;    /* CIGAR arena runs used */
+    uint32_t launches;      /* kernels launched by the last batch */
+    uint32_t profiled;      /* 1 if phase_ms holds device times (fz_set_profiling) */
+    float phase_ms[6];      /* device time per phase: 0 inspector (register window),
+                               1 inspector (wide band), 2 binning + scans, 3 executor,
+                               4 CIGAR emission, 5 whole batch */
+} fz_stats;
+
+/*
+ * Create a context.  sub: 4x4 substitution scores, row = target base, column =
+ * query base, order A, C, G, T (host memory, copied).  gap_open >= 0,
+ * gap_extend >= 1, ydrop >= 0 or FZ_YDROP_INF, 1 <= max_len <= FZ_MAX_LEN_LIMIT
+ * (window cap per side).  |score| bounds: max(|sub|, gap_open + gap_extend) *
+ * (2 * max_len + 1) must stay below 2^28 (int32 DP without wrap-around).
+ * The context owns its device scratch and arenas; the calling thread's current
+ * device is used.  Returns FZ_ERR_ARG on a bad parameter (*out = NULL).
+ */
+fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32_t gap_extend,
+                    int32_t ydrop, int32_t max_len, fz_mode mode);
+
+/*
+ * Extend every seed.  d_target2 / d_query2: 2-bit packed sequences (A=0, C=1,
+ * G=2, T=3; base k at bits 2*(k%4) of byte k/4), t_len / q_len bases.
+ * d_seeds: n_seeds anchors (t_pos <= t_len, q_pos <= q_len).  d_out: 2*n_seeds
+ * results.  *d_cigar receives the device address of the context-owned CIGAR
+ * arena (valid until the next call on this context or fz_destroy); LOCAL mode
+ * emits no CIGAR.
+ *
+ * Stream use: kernels run on cuda_stream (a cudaStream_t; NULL = legacy
+ * default stream).  EXTEND mode reads a few counters back to the host once per
+ * call (to size the executor and CIGAR arenas), so it returns after the
+ * inspector has finished; the executor and traceback are still asynchronous.
+ * The inputs must stay valid until the stream has passed this call's work.
+ */
+fz_status fz_extend_batch(fz_ctx* ctx, const uint8_t* d_target2, uint64_t t_len,
+                          const uint8_t* d_query2, uint64_t q_len, const fz_seed* d_seeds,
+                          uint32_t n_seeds, fz_result* d_out, const uint32_t** d_cigar,
+                          void* cuda_stream);
+
+/*
+ * Same computation from HOST buffers: copies the packed sequences and seeds to
+ * context-owned device memory, runs fz_extend_batch, copies the results to
+ * h_out (2*n_seeds) and the CIGAR runs to h_cigar, and synchronises the
+ * stream before returning.  h_cigar may be NULL when cigar_cap is 0.  If the
+ * CIGAR needs more than cigar_cap runs, the results are still written,
+ * *cigar_used holds the size needed and FZ_ERR_ARG is returned.  Host buffers
+ * may be pageable; page-locked buffers copy faster.
+ */
+fz_status fz_extend_batch_host(fz_ctx* ctx, const uint8_t* h_target2, uint64_t t_len,
+                               const uint8_t* h_query2, uint64_t q_len, const fz_seed* h_seeds,
+                               uint32_t n_seeds, fz_result* h_out, uint32_t* h_cigar,
+                               uint64_t cigar_cap, uint64_t* cigar_used, void* cuda_stream);
+
+/* Counters of the last completed batch (synchronises the context's last stream). */
+fz_status fz_get_stats(fz_ctx* ctx, fz_stats* out);
+
+/*
+ * Per-phase device timing: when on, each batch records CUDA events on its
+ * stream around its phases and fz_get_stats() fills phase_ms.  Off by default
+ * (events add a little host work per batch).
+ */
+fz_status fz_set_profiling(fz_ctx* ctx, int on);
+
+/* One-line description of the last error on this context ("" if none). */
+const char* fz_last_error(fz_ctx* ctx);
+
+/* Frees all device memory of the context.  NULL is ignored. */
+void fz_destroy(fz_ctx* ctx);
+
+/*
+ * Integer-pipe throughput microbenchmark (whole GPU, current device): op/s of
+ * DPX add-max (__viaddmax_s32), DPX 3-way max (__vimax3_s32), 32-bit add and
+ * 32-bit max, written to rates[0..3].  Independent dependency chains per
+ * thread, every SM busy; synchronises the device.  Used for the roofline.
+ */
+fz_status fz_bench_int_rates(double rates[4]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FZ_H */

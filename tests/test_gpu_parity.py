@@ -1,0 +1,308 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Scores, end cells, CIGARs and flags must be bit-exact (integer work).  Small
+workloads are compared on every extension; full-size workloads run in the
+benchmark's configuration and are compared on sampled extensions.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from gapped_smith_waterman_gb300 import workloads as W
+from tests import gpu_common as G
+from tests import refcheck as R
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from gapped_smith_waterman_gb300 import build
+    build.build()
+    import oracle
+    oracle.lib()
+
+
+def _one_pair_workload(t, q, sub=W.HOXD70, o=400, e=30, ydrop=9400, mode=W.MODE_EXTEND, side=W.SIDE_RIGHT):
+    t = np.asarray(t, np.uint8)
+    q = np.asarray(q, np.uint8)
+    seeds = np.zeros(1, W.SEED_DTYPE)
+    seeds["side"] = side
+    if side == W.SIDE_LEFT:
+        seeds["t_pos"] = t.size
+        seeds["q_pos"] = q.size
+        t, q = t[::-1].copy(), q[::-1].copy()
+    ml = max(1, t.size, q.size)
+    return W.Workload("pair", t, q, seeds, np.asarray(sub, np.int32), o, e, ydrop, ml, mode)
+
+
+def _batch_from_pairs(pairs, sub=W.HOXD70, o=400, e=30, ydrop=9400, mode=W.MODE_EXTEND):
+    """Pairs laid end to end; seed k anchors at the start of pair k; max_len
+    = the longest window, each pair padded so windows never overlap."""
+    ml = max(1, max(max(len(t), len(q)) for t, q in pairs))
+    T = np.zeros(len(pairs) * ml, np.uint8)          # padding A in the target ...
+    Q = np.ones(len(pairs) * ml, np.uint8)           # ... against C in the query: windows stop at pair ends
+    seeds = np.zeros(len(pairs), W.SEED_DTYPE)
+    tl = []
+    for k, (t, q) in enumerate(pairs):
+        T[k * ml:k * ml + len(t)] = t
+        Q[k * ml:k * ml + len(q)] = q
+        seeds[k]["t_pos"] = k * ml
+        seeds[k]["q_pos"] = k * ml
+        tl.append((len(t), len(q)))
+    seeds["side"] = W.SIDE_RIGHT
+    return W.Workload("pairs", T, Q, seeds, np.asarray(sub, np.int32), o, e, ydrop, ml, mode), tl
+
+
+def _check(w, seeds=None, label="", check_cigar=True):
+    gres, gcig, st = G.gpu_run(w, seeds)
+    ores, ocig, ooff = G.oracle_run(w, seeds)
+    G.compare(w, seeds, gres, gcig, ores, ocig, ooff, check_cigar=check_cigar, label=label)
+    return gres, gcig, st, ores
+
+
+def test_golden_closed_forms_gpu():
+    cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))["cases"]
+    code = {"A": 0, "C": 1, "G": 2, "T": 3}
+    for c in cases:
+        t = np.array([code[x] for x in c["target"]], np.uint8)
+        q = np.array([code[x] for x in c["query"]], np.uint8)
+        mode = W.MODE_LOCAL if c["mode"] == "local" else W.MODE_EXTEND
+        yd = c.get("ydrop", W.YDROP_INF)
+        w = _one_pair_workload(t, q, ydrop=yd, mode=mode)
+        gres, gcig, st = G.gpu_run(w)
+        ex = c["expect"]
+        g = gres[0]
+        assert (g["score"], g["t_end"], g["q_end"]) == (ex["score"], ex["i_end"], ex["j_end"]), c["name"]
+        if mode == W.MODE_EXTEND:
+            runs = gcig[g["cigar_off"]:g["cigar_off"] + g["cigar_len"]]
+            assert "".join(f"{int(r) >> 4}{'MID'[int(r) & 15]}" for r in runs) == ex["cigar"], c["name"]
+            if "live_cells" in ex:
+                assert st.live_cells == ex["live_cells"], c["name"]
+
+
+def test_cfg1_full():
+    w = G.workload(1)
+    gres, gcig, st, ores = _check(w, label="short-256bp")
+    assert st.live_cells == int(ores["live_cells"].sum())
+    assert st.extensions == len(w.seeds)
+    assert st.eager + sum(st.bin) == st.extensions
+
+
+def test_cfg2_subset_all_fields():
+    w = G.workload(2)
+    idx = np.arange(4000)
+    gres, gcig, st, ores = _check(w, w.seeds[idx], label="skewed-6kbp[:4000]")
+    assert st.live_cells == int(ores["live_cells"].sum())
+
+
+def test_cfg2_full_sampled():
+    w = G.workload(2)
+    gres, gcig, st = G.gpu_run(w)
+    idx = G.sample_seeds(w, 600, seed=2)
+    ores, ocig, ooff = G.oracle_run(w, w.seeds[idx])
+    xs = np.stack([2 * idx, 2 * idx + 1], 1).reshape(-1)
+    sub_res = gres[xs]
+    # CIGAR offsets refer to the full arena
+    G.compare(G.sub_workload(w, idx), None, sub_res, gcig, ores, ocig, ooff, label="skewed-6kbp sampled")
+    # every right extension: CIGAR re-scores to its score (independent scorer)
+    for k in G.sample_seeds(w, 3000, seed=5):
+        g = gres[2 * k]
+        runs = gcig[g["cigar_off"]:g["cigar_off"] + g["cigar_len"]]
+        t = W.window_bases(w.target, w.seeds["t_pos"][k], W.SIDE_RIGHT, w.max_len)
+        q = W.window_bases(w.query, w.seeds["q_pos"][k], W.SIDE_RIGHT, w.max_len)
+        assert R.rescore_cigar(runs, t, q, w.sub, w.gap_open, w.gap_extend) == (g["score"], g["t_end"], g["q_end"])
+    assert st.extensions == len(w.seeds)
+
+
+def test_cfg3_sampled():
+    w = G.workload(3)
+    gres, gcig, st = G.gpu_run(w)
+    idx = G.sample_seeds(w, 400, seed=3)
+    ores, ocig, ooff = G.oracle_run(w, w.seeds[idx])
+    xs = np.stack([2 * idx, 2 * idx + 1], 1).reshape(-1)
+    G.compare(G.sub_workload(w, idx), None, gres[xs], gcig, ores, ocig, ooff, label="chrom-50Mbp sampled")
+    assert st.extensions == 2 * len(w.seeds)
+
+
+def test_cfg4_sampled():
+    w = G.workload(4)
+    gres, gcig, st = G.gpu_run(w)
+    idx = G.sample_seeds(w, 8, seed=4)
+    ores, ocig, ooff = G.oracle_run(w, w.seeds[idx])
+    xs = np.stack([2 * idx, 2 * idx + 1], 1).reshape(-1)
+    G.compare(G.sub_workload(w, idx), None, gres[xs], gcig, ores, ocig, ooff, label="long-60kbp sampled")
+
+
+def test_cfg5_subset_and_sampled():
+    w = G.workload(5)
+    _check(w, w.seeds[:48], label="local-2048[:48]", check_cigar=False)
+    gres, gcig, st = G.gpu_run(w)
+    idx = G.sample_seeds(w, 24, seed=5)
+    ores, ocig, ooff = G.oracle_run(w, w.seeds[idx])
+    xs = np.stack([2 * idx, 2 * idx + 1], 1).reshape(-1)
+    G.compare(G.sub_workload(w, idx), None, gres[xs], gcig, ores, ocig, ooff, check_cigar=False,
+              label="local-2048 sampled")
+    assert st.live_cells == len(w.seeds) * 2048 * 2048
+
+
+def test_edge_cases():
+    rng = np.random.default_rng(42)
+    code = lambda s: np.array(["ACGT".index(c) for c in s], np.uint8)  # noqa: E731
+    x = rng.integers(0, 4, 200).astype(np.uint8)
+    pairs = [
+        (np.zeros(0, np.uint8), np.zeros(0, np.uint8)),          # empty windows
+        (code("A"), code("A")),                                   # window of 1
+        (code("A"), np.zeros(0, np.uint8)),
+        (np.zeros(0, np.uint8), code("ACGT")),
+        (np.zeros(30, np.uint8), np.ones(30, np.uint8)),         # all mismatch
+        (x, x),                                                   # identical
+        (x[:16], x[:16]),                                         # ends exactly at (16,16)
+        (x[:17], x[:16]),
+        (x[:16], x[:17]),
+        (np.concatenate([x[:17], code("AA")]), np.concatenate([x[:16], code("CC")])),
+        (np.concatenate([x[:80], np.zeros(60, np.uint8), x[80:]]), x),   # single long gap
+        (x[:100], np.concatenate([x[:50], x[60:100]])),
+    ]
+    # bin edges: identical prefixes ending at 512 and 513
+    for L in (511, 512, 513):
+        y = rng.integers(0, 4, L).astype(np.uint8)
+        pairs.append((np.concatenate([y, np.zeros(40, np.uint8)]), np.concatenate([y, np.ones(40, np.uint8)])))
+    w, _ = _batch_from_pairs(pairs)
+    _check(w, label="edge cases")
+    for yd in (0, 1, 429, 430, 5000, W.YDROP_INF):
+        w2 = W.Workload(w.name, w.target, w.query, w.seeds, w.sub, w.gap_open, w.gap_extend, yd, w.max_len, w.mode)
+        _check(w2, label=f"edge cases ydrop={yd}")
+
+
+def test_left_and_both_sides_and_sequence_ends():
+    rng = np.random.default_rng(7)
+    t = rng.integers(0, 4, 5000).astype(np.uint8)
+    q = W.mutate(rng, t, 0.08, 0.01, 2.0)
+    n = 300
+    seeds = np.zeros(n, W.SEED_DTYPE)
+    seeds["t_pos"] = rng.integers(0, t.size + 1, n)
+    seeds["q_pos"] = np.clip(seeds["t_pos"].astype(np.int64) + rng.integers(-3, 4, n), 0, q.size)
+    seeds["side"] = rng.integers(1, 4, n)
+    seeds[0]["t_pos"], seeds[0]["q_pos"], seeds[0]["side"] = 0, 0, 3
+    seeds[1]["t_pos"], seeds[1]["q_pos"], seeds[1]["side"] = t.size, q.size, 3
+    seeds[2]["t_pos"], seeds[2]["q_pos"], seeds[2]["side"] = t.size, 0, 3
+    w = W.Workload("sides", t, q, seeds, W.HOXD70.copy(), 400, 30, 9400, 700, W.MODE_EXTEND)
+    _check(w, label="sides")
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_fuzz_small_random_parameters(seed):
+    rng = np.random.default_rng(300 + seed)
+    for it in range(6):
+        sub = rng.integers(-120, 121, size=(4, 4)).astype(np.int32)
+        sub[np.arange(4), np.arange(4)] = rng.integers(20, 128, 4)
+        o = int(rng.integers(0, 600))
+        e = int(rng.integers(1, 60))
+        yd = int(rng.choice([0, 50, 300, 800, 2000, 9400, W.YDROP_INF]))
+        pairs = []
+        for _ in range(150):
+            m = int(rng.integers(0, 300))
+            t = rng.integers(0, 4, m).astype(np.uint8)
+            q = W.mutate(rng, t[:int(rng.integers(0, m + 1))], rng.uniform(0, 0.3), rng.uniform(0, 0.05), 2.0)
+            q = np.concatenate([q, rng.integers(0, 4, int(rng.integers(0, 60))).astype(np.uint8)])
+            pairs.append((t, q))
+        w, _ = _batch_from_pairs(pairs, sub=sub, o=o, e=e, ydrop=yd)
+        _check(w, label=f"fuzz seed={seed} it={it} o={o} e={e} ydrop={yd}")
+
+
+def test_local_fuzz():
+    rng = np.random.default_rng(77)
+    for it in range(4):
+        sub = rng.integers(-100, 101, size=(4, 4)).astype(np.int32)
+        sub[np.arange(4), np.arange(4)] = rng.integers(20, 128, 4)
+        pairs = []
+        for _ in range(60):
+            m = int(rng.integers(0, 1500))
+            t = rng.integers(0, 4, m).astype(np.uint8)
+            q = W.mutate(rng, t, 0.2, 0.02, 2.0) if rng.random() < 0.5 else rng.integers(0, 4, int(rng.integers(0, 2500))).astype(np.uint8)
+            pairs.append((t, q))
+        w, _ = _batch_from_pairs(pairs, sub=sub, o=int(rng.integers(0, 500)), e=int(rng.integers(1, 50)),
+                                 ydrop=W.YDROP_INF, mode=W.MODE_LOCAL)
+        _check(w, label=f"local fuzz {it}", check_cigar=False)
+
+
+def test_wide_band_path():
+    # ydrop far above the register window's reach: gaps of thousands stay live
+    rng = np.random.default_rng(8)
+    pairs = []
+    for _ in range(24):
+        t = rng.integers(0, 4, 1500).astype(np.uint8)
+        q = W.mutate(rng, t, 0.1, 0.02, 3.0)
+        pairs.append((t, q))
+    w, _ = _batch_from_pairs(pairs, ydrop=40000)
+    gres, gcig, st, ores = _check(w, label="wide band")
+    assert st.wide > 0
+
+
+def test_matrix_outside_byte_range_uses_general_path():
+    rng = np.random.default_rng(9)
+    sub = (W.HOXD70 * 3).astype(np.int32)          # entries beyond [-128, 127]
+    pairs = [(rng.integers(0, 4, 200).astype(np.uint8),) * 2 for _ in range(10)]
+    pairs += [(rng.integers(0, 4, 150).astype(np.uint8), rng.integers(0, 4, 170).astype(np.uint8)) for _ in range(10)]
+    w, _ = _batch_from_pairs(pairs, sub=sub, o=1200, e=90, ydrop=28200)
+    _check(w, label="x3 matrix")
+
+
+def test_host_entry_matches_device_entry():
+    w = G.workload(1)
+    a, acig, _ = G.gpu_run(w)
+    b, bcig, _ = G.gpu_run(w, host=True)
+    assert np.array_equal(a, b) and np.array_equal(acig, bcig)
+
+
+def test_chunked_executor(monkeypatch):
+    w = G.workload(1)
+    a, acig, sa = G.gpu_run(w)
+    monkeypatch.setenv("FZ_TRACE_CAP", str(1 << 20))
+    b, bcig, sb = G.gpu_run(w)
+    assert np.array_equal(a, b) and np.array_equal(acig, bcig)
+
+
+def test_context_reuse_and_growth():
+    from gapped_smith_waterman_gb300 import fz
+    w = G.workload(1)
+    ext = fz.Extender.for_workload(w)
+    try:
+        r1 = ext.extend_workload(w, w.seeds[:10])
+        r2 = ext.extend_workload(w, w.seeds)
+        r3 = ext.extend_workload(w, w.seeds[:10])
+        assert np.array_equal(r1[0], r3[0])
+        assert np.array_equal(r1[0], r2[0][:20])
+        r0 = ext.extend_workload(w, w.seeds[:0])
+        assert r0[0].size == 0
+    finally:
+        ext.close()
+
+
+def test_error_codes(monkeypatch):
+    from gapped_smith_waterman_gb300 import fz
+    with pytest.raises(fz.FzError) as ei:
+        fz.fz_create(W.HOXD70, 400, 0, 9400, 100)
+    assert ei.value.status == fz.FZ_ERR_ARG
+    with pytest.raises(fz.FzError):
+        fz.fz_create(W.HOXD70, 400, 30, -5, 100)
+    with pytest.raises(fz.FzError):
+        fz.fz_create(W.HOXD70 * 2, 400, 30, 9400, 100, fz.FZ_LOCAL)
+    w = G.workload(1)
+    ext = fz.Extender.for_workload(w)
+    try:
+        monkeypatch.setenv("FZ_FAULT", "alloc")
+        with pytest.raises(fz.FzError) as ei:
+            ext.extend_workload(w, w.seeds[:5])
+        assert ei.value.status == fz.FZ_ERR_OOM
+        monkeypatch.delenv("FZ_FAULT")
+        r = ext.extend_workload(w, w.seeds[:5])
+        assert r[0].size == 10
+    finally:
+        ext.close()
