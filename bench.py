@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bounded oracle sample for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seeds", type=int, default=0, help="use only the first N seeds (profiling captures)")
     return ap.parse_args()
 
 
@@ -196,7 +197,7 @@ def main():
         dist.barrier()
     w = W.make(args.config)
     t2, q2 = W.pack2(w.target), W.pack2(w.query)
-    seeds = np.ascontiguousarray(w.seeds)
+    seeds = np.ascontiguousarray(w.seeds[:args.seeds] if args.seeds else w.seeds)
     ext = fz.Extender.for_workload(w, device=dev)
     fz.fz_set_profiling(ext.ctx, True)
     d_t, d_q, d_s = ext.upload(t2, q2, seeds)
