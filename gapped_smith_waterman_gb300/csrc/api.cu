@@ -51,7 +51,7 @@ struct Counters {
   uint32_t bin_cursor[8];
 };
 
-constexpr uint64_t TRACE_CAP_DEFAULT = 8ull << 30;   // executor arena cap before chunking
+constexpr uint64_t TRACE_CAP_DEFAULT = 1ull << 30;   // smallest executor arena cap before chunking
 
 }  // namespace
 
@@ -61,6 +61,7 @@ struct fz_ctx {
   fz_mode mode = FZ_EXTEND;
   Params p{};
   bool fast_ok = false;
+  int32_t max_sub = 0;               // max(0, largest substitution score)
   uint32_t mcol[4] = {0, 0, 0, 0};
   std::string err;
   DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, counters;
@@ -223,6 +224,8 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   pa.cig_cap = ctx->cig_cap.as<uint64_t>();
   pa.err = &dc->err;
   pa.local = 0;
+  pa.oe = ctx->p.oe;
+  pa.max_sub = ctx->max_sub;
   CU(cudaMemsetAsync(ctx->trace_sz.p, 0, (size_t)n_ext * 8, st));
   CU(launch_classify(pa, st));
   CU(launch_scatter(pa, st));
@@ -279,6 +282,8 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   ea.trace = ctx->trace.as<uint8_t>();
   ea.err = &dc->err;
   ea.local = 0;
+  ea.oe = ctx->p.oe;
+  ea.max_sub = ctx->max_sub;
   int slot = 2;
   for (auto& c : chunks) {
     const uint64_t sub = toff.empty() ? 0 : toff[c.first];
@@ -364,7 +369,10 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
   p.oe = gap_open + gap_extend;
   p.ydrop = ydrop;
   p.max_len = max_len;
-  for (int k = 0; k < 16; ++k) p.sub[k] = sub[k];
+  for (int k = 0; k < 16; ++k) {
+    p.sub[k] = sub[k];
+    ctx->max_sub = std::max(ctx->max_sub, sub[k]);
+  }
   ctx->fast_ok = bytes;
   for (int t = 0; t < 4; ++t) {
     uint32_t row = 0, col = 0;
@@ -391,6 +399,13 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     cudaFreeHost(ctx->h_cnt);
     delete ctx;
     return FZ_ERR_CUDA;
+  }
+  {
+    // executor arena cap: 40% of the device memory free now (chunks beyond it)
+    size_t fr = 0, tot = 0;
+    if (cudaMemGetInfo(&fr, &tot) == cudaSuccess)
+      ctx->trace_cap = std::max<uint64_t>(TRACE_CAP_DEFAULT, (uint64_t)(fr * 0.4));
+    (void)cudaGetLastError();
   }
   const char* cap = getenv("FZ_TRACE_CAP");
   if (cap) ctx->trace_cap = std::max<uint64_t>(strtoull(cap, nullptr, 10), 4096);

@@ -65,6 +65,8 @@ struct PipeArgs {
   uint64_t* cig_cap;           // per extension
   uint32_t* err;
   int local;
+  int32_t oe;                  // gap open + extend
+  int32_t max_sub;             // max(0, largest substitution score)
 };
 cudaError_t launch_classify(const PipeArgs& a, cudaStream_t st);
 cudaError_t launch_scatter(const PipeArgs& a, cudaStream_t st);
@@ -86,6 +88,8 @@ struct EmitArgs {
   uint32_t exec_begin, exec_end;
   uint32_t* err;
   int local;
+  int32_t oe;
+  int32_t max_sub;
 };
 cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st);   // eager, empty, local, not requested
 cudaError_t launch_emit_exec(const EmitArgs& a, cudaStream_t st);     // executor items [exec_begin, exec_end)

@@ -22,6 +22,18 @@ __device__ __forceinline__ uint32_t bin_of(int32_t i, int32_t j) {
   return mx <= 512 ? 1u : mx <= 2048 ? 2u : mx <= 8192 ? 3u : mx <= 32768 ? 4u : 5u;
 }
 
+// Upper bound on the CIGAR runs of an alignment ending at (i, j).  The traced
+// alignment scores S* >= 0, so its g gap runs (each costing at least o + e)
+// are paid for by at most min(i, j) diagonal scores of at most max_sub each:
+// g <= max_sub * min(i, j) / (o + e); match runs number at most g + 1; and no
+// alignment has more runs than ops (i + j).
+__device__ __forceinline__ uint64_t cigar_cap(int32_t i, int32_t j, int32_t oe, int32_t max_sub) {
+  const uint64_t ops = (uint64_t)i + (uint64_t)j;
+  const uint64_t g = (uint64_t)max_sub * (uint64_t)imin(i, j) / (uint64_t)(oe > 0 ? oe : 1);
+  const uint64_t runs = 2 * g + 1;
+  return runs < ops ? runs : ops;
+}
+
 __global__ void k_classify(PipeArgs a) {
   __shared__ uint32_t h[8];
   if (threadIdx.x < 8) h[threadIdx.x] = 0;
@@ -34,7 +46,7 @@ __global__ void k_classify(PipeArgs a) {
     if (r.flags & FZ_FLAG_DONE) {
       atomicAdd(&h[7], 1u);
       if (!a.local) {
-        cap = (uint64_t)r.i_end + (uint64_t)r.j_end;
+        cap = cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub);
         if (r.flags & FZ_FLAG_EAGER) {
           atomicAdd(&h[0], 1u);
         } else {
@@ -157,11 +169,13 @@ struct RunWriter {
   uint64_t off, cap;
   bool backwards;
   uint32_t op, len, nruns;
+  bool overflow;
   __device__ void init(uint32_t* c, uint64_t o, uint64_t k, bool bw) {
-    dst = c; off = o; cap = k; backwards = bw; op = 0xffu; len = 0; nruns = 0;
+    dst = c; off = o; cap = k; backwards = bw; op = 0xffu; len = 0; nruns = 0; overflow = false;
   }
   __device__ void flush() {
     if (!len) return;
+    if (nruns >= cap) { overflow = true; return; }   // never write outside the slot
     const uint64_t at = backwards ? off + cap - 1 - nruns : off + nruns;
     dst[at] = (len << 4) | op;
     ++nruns;
@@ -198,11 +212,12 @@ __global__ void k_emit_direct(EmitArgs a) {
   if (a.local) { write_out(a.out + x, r, 0, 0, 0); return; }
   if (!(r.flags & FZ_FLAG_EAGER)) return;       // executor extension: k_emit_exec
   const uint64_t off = a.cig_off[x];
-  const uint64_t cap = (uint64_t)r.i_end + r.j_end;
+  const uint64_t cap = cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub);
   RunWriter wr;
   wr.init(a.cigar, off, cap, (x & 1u) == 0u);
   for (uint32_t k = 0; k < r.npath; ++k) wr.push((uint32_t)(r.path >> (2 * k)) & 3u);
   wr.flush();
+  if (wr.overflow) atomicOr(a.err, 16u);
   write_out(a.out + x, r, wr.nruns ? wr.first() : (uint32_t)off, wr.nruns, 0);
 }
 
@@ -217,7 +232,7 @@ __global__ void k_emit_exec(EmitArgs a) {
   const int32_t* lo = reinterpret_cast<const int32_t*>(base + trace_lo_offset(W, dend));
   const uint64_t off = a.cig_off[x];
   RunWriter wr;
-  wr.init(a.cigar, off, (uint64_t)dend, (x & 1u) == 0u);
+  wr.init(a.cigar, off, cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub), (x & 1u) == 0u);
   int32_t i = r.i_end, j = r.j_end, st = 0;
   int64_t guard = 2 * (int64_t)dend + 4;
   while ((i > 0 || j > 0) && --guard > 0) {
@@ -243,6 +258,7 @@ __global__ void k_emit_exec(EmitArgs a) {
   }
   if (guard <= 0) atomicOr(a.err, 4u);
   wr.flush();
+  if (wr.overflow) atomicOr(a.err, 16u);
   write_out(a.out + x, r, wr.nruns ? wr.first() : (uint32_t)off, wr.nruns, a.local ? 0u : bin_of(r.i_end, r.j_end));
 }
 
