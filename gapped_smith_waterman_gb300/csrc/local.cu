@@ -194,3 +194,147 @@ cudaError_t launch_local(const Params& p, const LocalArgs& la, int grid, cudaStr
 }
 
 }  // namespace fz
+
+// ---------------------------------------------------------------------------
+// Allocation-free local fill (fz_local_fill_noalloc in fz.h).
+//
+// For callers that cannot allocate device memory at run time (an allocator
+// that is already locked, an embedding runtime that forbids cudaMalloc on its
+// hot path).  Its scratch -- the work counter and the per-warp strip spill
+// rows -- lives in one file-scope device array instead of context memory; the
+// kernel always uses these global spill rows, never dynamic shared memory.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace fz {
+
+namespace {
+
+constexpr int32_t NA_MAX_LEN = 2048;                        // longest window per side
+constexpr int NA_MAX_BLOCKS = 152;                          // one block of WL warps per SM
+constexpr uint64_t NA_SPILL = 2ull * (NA_MAX_LEN + 1);      // int32 per warp
+constexpr uint64_t NA_HEAD = 64;                            // word 0: work counter
+constexpr uint64_t NA_WORDS = NA_HEAD + (uint64_t)NA_MAX_BLOCKS * WL * NA_SPILL;   // ~10 MB
+
+// Every GPU that loads this library holds this array until the process exits.
+static __device__ __align__(256) int32_t g_noalloc_scratch[NA_WORDS];
+
+__global__ void __launch_bounds__(WL * 32) k_local_noalloc(Params p, uint32_t n_work, int32_t* scratch,
+                                                           fz_result* out, uint4 mcol) {
+  __shared__ uint32_t s_mcol[4];
+  if (threadIdx.x == 0) {
+    s_mcol[0] = mcol.x; s_mcol[1] = mcol.y; s_mcol[2] = mcol.z; s_mcol[3] = mcol.w;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* counter = reinterpret_cast<uint32_t*>(scratch);
+  int32_t* sp = scratch + NA_HEAD + ((uint64_t)blockIdx.x * WL + warp) * NA_SPILL;
+  int32_t* spH = sp;
+  int32_t* spE = sp + (p.max_len + 1);
+  for (;;) {
+    uint32_t ext = 0;
+    if (lane == 0) ext = atomicAdd(counter, 1u);
+    ext = __shfl_sync(FULL, ext, 0);
+    if (ext >= n_work) break;
+    const Window w = make_window(p, ext);
+    if (!w.requested) {
+      if (lane == 0) { fz_result z = {0, 0, 0, 0, 0, 0}; out[ext] = z; }
+      continue;
+    }
+    int32_t bv = 0, bd = 0, bi = 0;
+    const int32_t nstrips = (w.n + SW - 1) / SW;
+    if (w.m > 0) {
+      for (int32_t s = 0; s < nstrips; ++s) {
+        if ((s + 1) * SW > w.n) strip<true>(p, w, lane, s, nstrips, s_mcol, spH, spE, bv, bd, bi);
+        else strip<false>(p, w, lane, s, nstrips, s_mcol, spH, spE, bv, bd, bi);
+      }
+    }
+    const int32_t wm = __reduce_max_sync(FULL, bv);
+    const uint32_t dmin = __reduce_min_sync(FULL, bv == wm ? (uint32_t)bd : 0xffffffffu);
+    const uint32_t imn = __reduce_min_sync(FULL, (bv == wm && (uint32_t)bd == dmin) ? (uint32_t)bi : 0xffffffffu);
+    if (lane == 0) {
+      fz_result o;
+      o.score = wm;
+      o.t_end = wm > 0 ? (int32_t)imn : 0;
+      o.q_end = wm > 0 ? (int32_t)dmin - (int32_t)imn : 0;
+      o.cigar_off = 0;
+      o.cigar_len = 0;
+      o.flags = FZ_FLAG_DONE;
+      out[ext] = o;
+    }
+  }
+}
+
+}  // namespace
+
+}  // namespace fz
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[256] = {};   // device address of g_noalloc_scratch, per device ordinal
+
+// Resolves the scratch array's device address for the current device (once
+// per device).  The name g_noalloc_scratch in host code is only a host-side
+// stand-in; kernels must be given this address instead.
+cudaError_t noalloc_scratch(int dev, int32_t** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, fz::g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = static_cast<int32_t*>(g_noalloc_ptr[dev]);
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_open, int32_t gap_extend,
+                                           int32_t max_len, const uint8_t* d_target2, uint64_t t_len,
+                                           const uint8_t* d_query2, uint64_t q_len, const fz_seed* d_seeds,
+                                           uint32_t n_seeds, fz_result* d_out, void* cuda_stream) {
+  using namespace fz;
+  if (!sub || gap_open < 0 || gap_extend < 1 || max_len < 1 || max_len > NA_MAX_LEN) return FZ_ERR_ARG;
+  if (n_seeds > 0x7fffffffu) return FZ_ERR_ARG;
+  if (n_seeds && (!d_seeds || !d_out)) return FZ_ERR_ARG;
+  if ((t_len && !d_target2) || (q_len && !d_query2)) return FZ_ERR_ARG;
+  int64_t amax = (int64_t)gap_open + gap_extend;
+  for (int k = 0; k < 16; ++k) {
+    if (sub[k] < -128 || sub[k] > 127) return FZ_ERR_ARG;
+    amax = amax > (sub[k] < 0 ? -(int64_t)sub[k] : sub[k]) ? amax : (sub[k] < 0 ? -(int64_t)sub[k] : sub[k]);
+  }
+  if (amax * (2 * (int64_t)max_len + 1) >= (1ll << 28)) return FZ_ERR_ARG;
+  if (n_seeds == 0) return FZ_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) { (void)cudaGetLastError(); return FZ_ERR_CUDA; }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FZ_ERR_CUDA;
+  }
+  int32_t* scratch = nullptr;
+  if (noalloc_scratch(dev, &scratch) != cudaSuccess) { (void)cudaGetLastError(); return FZ_ERR_CUDA; }
+  Params p{};
+  p.t2 = d_target2; p.q2 = d_query2; p.t_len = t_len; p.q_len = q_len;
+  p.seeds = d_seeds; p.n_seeds = n_seeds;
+  p.o = gap_open; p.e = gap_extend; p.oe = gap_open + gap_extend;
+  p.ydrop = FZ_YDROP_INF; p.max_len = max_len;
+  for (int k = 0; k < 16; ++k) p.sub[k] = sub[k];
+  uint32_t mc[4];
+  for (int t = 0; t < 4; ++t) {
+    uint32_t col = 0;
+    for (int q = 0; q < 4; ++q) col |= (uint32_t)(sub[q * 4 + t] + 128) << (8 * q);
+    mc[t] = col;
+  }
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // the work counter must start at zero; the spill rows need no clearing
+  if (cudaMemsetAsync(scratch, 0, NA_HEAD * sizeof(int32_t), st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FZ_ERR_CUDA;
+  }
+  const int grid = sms < NA_MAX_BLOCKS ? sms : NA_MAX_BLOCKS;
+  k_local_noalloc<<<grid, WL * 32, 0, st>>>(p, 2 * n_seeds, scratch, d_out, make_uint4(mc[0], mc[1], mc[2], mc[3]));
+  if (cudaGetLastError() != cudaSuccess) return FZ_ERR_CUDA;
+  return FZ_OK;
+}

@@ -21,7 +21,7 @@ FZ_FLAG_DONE, FZ_FLAG_EAGER, FZ_FLAG_WIDE = 1, 2, 4
 FZ_FLAG_BIN_SHIFT = 4
 
 SYMBOLS = ("fz_create", "fz_extend_batch", "fz_extend_batch_host", "fz_get_stats", "fz_set_profiling",
-           "fz_last_error", "fz_destroy", "fz_bench_int_rates")
+           "fz_last_error", "fz_destroy", "fz_bench_int_rates", "fz_local_fill_noalloc")
 
 RESULT_DTYPE = np.dtype([("score", "<i4"), ("t_end", "<i4"), ("q_end", "<i4"), ("cigar_off", "<u4"),
                          ("cigar_len", "<u4"), ("flags", "<u4")])
@@ -74,6 +74,9 @@ def load(path: str | None = None, build_if_missing: bool = False):
     L.fz_last_error.restype = ctypes.c_char_p
     L.fz_destroy.argtypes = [vp]
     L.fz_destroy.restype = None
+    L.fz_local_fill_noalloc.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, u8p, u64p, u8p, u64p, vp, ctypes.c_uint32, vp, vp]
+    L.fz_local_fill_noalloc.restype = ctypes.c_int
     L.fz_bench_int_rates.argtypes = [ctypes.POINTER(ctypes.c_double)]
     L.fz_bench_int_rates.restype = ctypes.c_int
     _lib = L
@@ -135,6 +138,14 @@ def fz_last_error(ctx) -> str:
 def fz_destroy(ctx) -> None:
     if ctx:
         load().fz_destroy(ctx)
+
+
+def fz_local_fill_noalloc(sub, gap_open: int, gap_extend: int, max_len: int, d_target2: int, t_len: int,
+                          d_query2: int, q_len: int, d_seeds: int, n_seeds: int, d_out: int, stream: int = 0) -> None:
+    """Allocation-free local fill (results only; see include/fz.h)."""
+    arr = (ctypes.c_int32 * 16)(*[int(x) for x in np.asarray(sub, np.int64).reshape(16)])
+    _check(None, load().fz_local_fill_noalloc(arr, gap_open, gap_extend, max_len, d_target2, t_len, d_query2,
+                                              q_len, d_seeds, n_seeds, d_out, stream))
 
 
 def fz_bench_int_rates():

@@ -159,6 +159,36 @@ const char* fz_last_error(fz_ctx* ctx);
 void fz_destroy(fz_ctx* ctx);
 
 /*
+ * Local fill without any allocation.  The papers this library follows have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory at run time -- for example code running under a caching
+ * allocator or a host framework that forbids cudaMalloc/cudaFree on its hot
+ * path, or a process that must not grow its footprint after start-up -- and so
+ * cannot create an fz_ctx (a context owns device buffers and pinned memory).
+ *
+ * Computes exactly what fz_extend_batch computes for a FZ_LOCAL context with
+ * the same sub / gap_open / gap_extend / max_len: one fz_result per seed and
+ * side (score, t_end, q_end, flags; no CIGAR, cigar_off = cigar_len = 0).
+ * The caller passes inputs and outputs in device memory, as for
+ * fz_extend_batch.  Limits: 1 <= max_len <= 2048, sub entries in [-128, 127];
+ * anything beyond returns FZ_ERR_ARG before touching the GPU.
+ *
+ * Scratch (the work counter and the per-warp strip spill rows, about 10 MB)
+ * is one file-scope device array of the library: every GPU that loads the
+ * library holds it until the process exits.  No cudaMalloc, cudaFree or other
+ * allocating call is made.  The first call on a device resolves that array's
+ * device address (cudaGetSymbolAddress) for the current device; make that
+ * first call before any stream capture.  Every call shares the one array and
+ * clears the counter at its start, so calls that overlap on the GPU (different
+ * streams, or host threads, on the same device) race and must be serialised
+ * by the caller.  Asynchronous on cuda_stream.
+ */
+fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_open, int32_t gap_extend,
+                                int32_t max_len, const uint8_t* d_target2, uint64_t t_len,
+                                const uint8_t* d_query2, uint64_t q_len, const fz_seed* d_seeds,
+                                uint32_t n_seeds, fz_result* d_out, void* cuda_stream);
+
+/*
  * Integer-pipe throughput microbenchmark (whole GPU, current device): op/s of
  * DPX add-max (__viaddmax_s32), DPX 3-way max (__vimax3_s32), 32-bit add and
  * 32-bit max, written to rates[0..3].  Independent dependency chains per

@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     assert {"fz_create", "fz_extend_batch", "fz_destroy", "fz_extend_batch_host", "fz_get_stats",
-            "fz_last_error", "fz_set_profiling", "fz_bench_int_rates"} <= set(names)
+            "fz_last_error", "fz_set_profiling", "fz_bench_int_rates", "fz_local_fill_noalloc"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
