@@ -44,7 +44,8 @@ struct Counters {
   unsigned long long exec_total;
   uint64_t trace_total;
   uint64_t cig_total;
-  uint32_t work[4];
+  uint32_t work[8];            // dynamic work counters: 0..2 inspectors, 3..5 executors
+  uint32_t retry_count;        // extensions retried with the 512-row window
   uint32_t wide_count;
   uint32_t err;
   uint32_t bin_count[8];
@@ -64,7 +65,7 @@ struct fz_ctx {
   int32_t max_sub = 0;               // max(0, largest substitution score)
   uint32_t mcol[4] = {0, 0, 0, 0};
   std::string err;
-  DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, counters;
+  DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, retry_list, counters;
   DevBuf cigar, trace, scratch, spill;
   DevBuf in_t, in_q, in_seeds, out_res;
   Counters* h_cnt = nullptr;         // pinned
@@ -72,7 +73,7 @@ struct fz_ctx {
   fz_stats stats{};
   bool have_batch = false;
   uint64_t trace_cap = TRACE_CAP_DEFAULT;
-  int grid_fast = 0, grid_fast_trace = 0, grid_wide = 0, grid_local = 0;
+  int grid_fast[2] = {0, 0}, grid_fast_trace[2] = {0, 0}, grid_wide = 0, grid_local = 0;
   size_t local_smem = 0;
   bool local_use_smem = true;
   uint32_t launches = 0;
@@ -119,6 +120,7 @@ fz_status ensure_batch_buffers(fz_ctx* ctx, uint32_t n_ext) {
   CU(ctx->cig_cap.ensure(n * 8));
   CU(ctx->scan_tmp.ensure((size_t)scan_tmp_elems((uint32_t)n) * 8));
   CU(ctx->wide_list.ensure(n * 4));
+  CU(ctx->retry_list.ensure(n * 4));
   CU(ctx->counters.ensure(sizeof(Counters)));
   if (ctx->mode == FZ_EXTEND) {
     const uint64_t per = wide_scratch_elems(ctx->p.max_len) * 4;
@@ -187,15 +189,27 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   // 1. inspector
   mark(ctx, 0, st);
   if (ctx->fast_ok) {
-    wa.list = nullptr;
-    wa.n_work = n_ext;
-    wa.counter = &dc->work[0];
-    CU(launch_inspect_fast(ctx->p, wa, ctx->grid_fast, st));
+    // 384-row window for every extension; retries with 512 rows; then the wide band
+    WorkArgs a = wa;
+    a.list = nullptr;
+    a.n_work = n_ext;
+    a.counter = &dc->work[0];
+    a.ovf_list = ctx->retry_list.as<uint32_t>();
+    a.ovf_count = &dc->retry_count;
+    CU(launch_inspect_fast(0, ctx->p, a, ctx->grid_fast[0], st));
+    WorkArgs b = wa;
+    b.list = ctx->retry_list.as<uint32_t>();
+    b.n_work = 0;
+    b.n_work_dev = &dc->retry_count;
+    b.counter = &dc->work[1];
+    b.ovf_list = ctx->wide_list.as<uint32_t>();
+    b.ovf_count = &dc->wide_count;
+    CU(launch_inspect_fast(1, ctx->p, b, ctx->grid_fast[1], st));
     mark(ctx, 1, st);
     wa.list = ctx->wide_list.as<uint32_t>();
-    wa.counter = &dc->work[1];
+    wa.counter = &dc->work[2];
     CU(launch_inspect_wide(ctx->p, wa, ctx->grid_wide, st));
-    ctx->launches += 2;
+    ctx->launches += 3;
   } else {
     // every extension takes the general path (scores outside the byte range)
     std::vector<uint32_t> ids(n_ext);
@@ -205,7 +219,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
     CU(cudaStreamSynchronize(st));
     mark(ctx, 1, st);
     wa.list = ctx->wide_list.as<uint32_t>();
-    wa.counter = &dc->work[1];
+    wa.counter = &dc->work[2];
     CU(launch_inspect_wide(ctx->p, wa, ctx->grid_wide, st));
     ctx->launches += 1;
   }
@@ -284,28 +298,28 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   ea.local = 0;
   ea.oe = ctx->p.oe;
   ea.max_sub = ctx->max_sub;
-  int slot = 2;
+  bool first_chunk = true;
   for (auto& c : chunks) {
     const uint64_t sub = toff.empty() ? 0 : toff[c.first];
     WorkArgs we = wa;
     we.list = ctx->exec_list.as<uint32_t>() + c.first;
     we.n_work = c.second - c.first;
+    we.n_work_dev = nullptr;
     we.trace = ctx->trace.as<uint8_t>();
     we.trace_off = ctx->trace_sz.as<uint64_t>() + c.first;
     we.trace_sub = sub;
-    if (slot + 1 >= 4) {
-      CU(cudaMemsetAsync(&dc->work[2], 0, 8, st));
-      slot = 2;
-    }
-    we.counter = &dc->work[slot];
+    if (!first_chunk) CU(cudaMemsetAsync(&dc->work[3], 0, 3 * sizeof(uint32_t), st));
+    first_chunk = false;
     if (ctx->fast_ok) {
-      CU(launch_execute_fast(ctx->p, we, ctx->grid_fast_trace, st));
-      ctx->launches += 1;
+      for (int tier = 0; tier < 2; ++tier) {
+        we.counter = &dc->work[3 + tier];
+        CU(launch_execute_fast(tier, ctx->p, we, ctx->grid_fast_trace[tier], st));
+        ctx->launches += 1;
+      }
     }
-    we.counter = &dc->work[slot + 1];
+    we.counter = &dc->work[5];
     CU(launch_execute_wide(ctx->p, we, ctx->grid_wide, st));
     ctx->launches += 1;
-    slot += 2;
     if (chunks.size() > 1) {
       EmitArgs ex = ea;
       ex.exec_begin = c.first;
@@ -383,8 +397,10 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     p.mrow[t] = row;
     ctx->mcol[t] = col;
   }
-  ctx->grid_fast = ctx->sms * extend_fast_blocks_per_sm(false);
-  ctx->grid_fast_trace = ctx->sms * extend_fast_blocks_per_sm(true);
+  for (int tier = 0; tier < 2; ++tier) {
+    ctx->grid_fast[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, false);
+    ctx->grid_fast_trace[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, true);
+  }
   ctx->grid_wide = ctx->sms;
   ctx->local_smem = local_smem_bytes(max_len);
   ctx->local_use_smem = ctx->local_smem <= 200 * 1024;
@@ -531,7 +547,7 @@ void fz_destroy(fz_ctx* ctx) {
   if (!ctx) return;
   cudaSetDevice(ctx->device);
   DevBuf* bufs[] = {&ctx->rec, &ctx->ext_bin, &ctx->exec_list, &ctx->exec_pos, &ctx->trace_sz, &ctx->cig_cap,
-                    &ctx->scan_tmp, &ctx->wide_list, &ctx->counters, &ctx->cigar, &ctx->trace, &ctx->scratch,
+                    &ctx->scan_tmp, &ctx->wide_list, &ctx->retry_list, &ctx->counters, &ctx->cigar, &ctx->trace, &ctx->scratch,
                     &ctx->spill, &ctx->in_t, &ctx->in_q, &ctx->in_seeds, &ctx->out_res};
   for (DevBuf* b : bufs) b->release();
   if (ctx->h_cnt) cudaFreeHost(ctx->h_cnt);

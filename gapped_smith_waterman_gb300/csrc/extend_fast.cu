@@ -71,7 +71,7 @@ __device__ __forceinline__ int32_t lo_row(uint32_t mask, int32_t base, int K) {
 // Eager traceback inside the 16x16 corner (FastZ section 3.1.2): recompute
 // cells (i, j), i, j <= 16, with the sweep's thresholds, lane = row, then walk
 // back from (bi, bj).  Returns the walk as 2-bit ops, first op = last column.
-__device__ void eager_corner(const Params& p, const Window& w, int lane, const int32_t* sT,
+__device__ __noinline__ void eager_corner(const Params& p, const Window& w, int lane, const int32_t* sT,
                              uint8_t* tile, const int32_t* s_sub, int32_t bi, int32_t bj,
                              uint64_t& path, uint32_t& npath, uint32_t* err) {
   const int32_t dstar = bi + bj;
@@ -235,7 +235,7 @@ __device__ __forceinline__ int32_t step(LaneState<K>& L, const StepIn& in, int l
 template <int K, bool TRACE>
 __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint32_t idx, int lane,
                         int32_t* sT, uint8_t* tile, const uint32_t* s_mrow, const int32_t* s_sub) {
-  static_assert(K == 16, "one 16-base fetch per lane");
+  static_assert(K % 4 == 0 && K <= 16, "one 16-base fetch per lane, whole bytes of codes");
   constexpr int KH = K / 2;
   constexpr int32_t WIN = 32 * K;
   const Window w = make_window(p, ext);
@@ -295,8 +295,12 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
     }
     const int32_t T = threshold(best, p.ydrop);
     in.Th = T - oe;
-    const bool edge = (bn + WIN - 1 > m && (hi_row(lmask, b, K) >= m || hi_row(lmask_prev, b_prev, K) >= m)) ||
-                      lo_row(lmask, b, K) <= d - n || lo_row(lmask_prev, b_prev, K) <= d - 1 - n;
+    // window bounds matter only near row m (window top past m) or column n
+    // (base at or below d - n); the lane-granular test runs only then
+    bool edge = false;
+    if (bn + WIN - 1 > m || b_prev <= d - n)
+      edge = (bn + WIN - 1 > m && (hi_row(lmask, b, K) >= m || hi_row(lmask_prev, b_prev, K) >= m)) ||
+             lo_row(lmask, b, K) <= d - n || lo_row(lmask_prev, b_prev, K) <= d - 1 - n;
     const int32_t rowbase = bn + lane * K;
     in.vhi = m - rowbase;
     in.vlo = dn - n - rowbase;
@@ -333,7 +337,13 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
     }
     if (!TRACE && dn <= 2 * EAGER_N && lane == 0) sT[dn] = T;
     if (TRACE) {
-      *reinterpret_cast<uint64_t*>(tbase + (uint64_t)dn * (WIN / 2) + lane * (K / 2)) = packed;
+      uint8_t* row = tbase + (uint64_t)dn * (WIN / 2) + lane * (K / 2);
+      if (K == 16) {
+        *reinterpret_cast<uint64_t*>(row) = packed;
+      } else {
+#pragma unroll
+        for (int k = 0; k < K / 4; ++k) reinterpret_cast<uint16_t*>(row)[k] = (uint16_t)(packed >> (16 * k));
+      }
       if (lane == 0) lo_arr[dn] = bn;
     }
     lmask_prev = lmask; lmask = mask;
@@ -360,8 +370,8 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
       z.m = m;
       z.n = n;
       *R = z;
-      const uint32_t slot = atomicAdd(wa.wide_count, 1u);
-      wa.wide_list[slot] = ext;
+      const uint32_t slot = atomicAdd(wa.ovf_count, 1u);   // retried with a wider window
+      wa.ovf_list[slot] = ext;
     }
     return;
   }
@@ -384,8 +394,9 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
   }
 }
 
-template <int K, bool TRACE>
-__global__ void __launch_bounds__(WARPS * 32) k_extend(Params p, WorkArgs wa) {
+// MINB: resident blocks per SM the register budget is fitted to.
+template <int K, bool TRACE, int MINB>
+__global__ void __launch_bounds__(WARPS * 32, MINB) k_extend(Params p, WorkArgs wa) {
   __shared__ int32_t s_T[WARPS][2 * EAGER_N + 1];
   __shared__ uint8_t s_tile[WARPS][(EAGER_N + 1) * (EAGER_N + 1)];
   __shared__ uint32_t s_mrow[4];
@@ -398,11 +409,13 @@ __global__ void __launch_bounds__(WARPS * 32) k_extend(Params p, WorkArgs wa) {
     uint32_t idx = 0;
     if (lane == 0) idx = atomicAdd(wa.counter, 1u);
     idx = __shfl_sync(FULL, idx, 0);
-    if (idx >= wa.n_work) break;
+    const uint32_t nw = wa.n_work_dev ? *wa.n_work_dev : wa.n_work;
+    if (idx >= nw) break;
     uint32_t ext = wa.list ? wa.list[idx] : idx;
     if (TRACE) {
-      // executor: this kernel takes the register-window extensions only
-      if (wa.rec[ext].flags & FZ_FLAG_WIDE) continue;
+      // executor: only the extensions this window size inspected
+      const ExtRec& r = wa.rec[ext];
+      if ((r.flags & FZ_FLAG_WIDE) || r.width != (uint32_t)(32 * K)) continue;
     }
     run_ext<K, TRACE>(p, wa, ext, idx, lane, s_T[warp], s_tile[warp], s_mrow, s_sub);
   }
@@ -410,24 +423,34 @@ __global__ void __launch_bounds__(WARPS * 32) k_extend(Params p, WorkArgs wa) {
 
 }  // namespace
 
-int fast_window_rows() { return 32 * 16; }
+// Two register windows: 384 rows (K = 12, fitted to 4 blocks of 4 warps per
+// SM) holds the live band of typical y-drop extensions; extensions whose band
+// could outgrow it are retried with 512 rows (K = 16), then the wide path.
+constexpr int KA = 12, KB = 16;
 
-cudaError_t launch_inspect_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  k_extend<16, false><<<grid, WARPS * 32, 0, st>>>(p, wa);
+int fast_window_rows(int tier) { return 32 * (tier == 0 ? KA : KB); }
+
+cudaError_t launch_inspect_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
+  if (tier == 0) k_extend<KA, false, 4><<<grid, WARPS * 32, 0, st>>>(p, wa);
+  else k_extend<KB, false, 1><<<grid, WARPS * 32, 0, st>>>(p, wa);
   return cudaGetLastError();
 }
 
-cudaError_t launch_execute_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  k_extend<16, true><<<grid, WARPS * 32, 0, st>>>(p, wa);
+cudaError_t launch_execute_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
+  if (tier == 0) k_extend<KA, true, 4><<<grid, WARPS * 32, 0, st>>>(p, wa);
+  else k_extend<KB, true, 1><<<grid, WARPS * 32, 0, st>>>(p, wa);
   return cudaGetLastError();
 }
 
-int extend_fast_blocks_per_sm(bool trace) {
+int extend_fast_blocks_per_sm(int tier, bool trace) {
   int nb = 0;
-  if (trace)
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<16, true>, WARPS * 32, 0);
-  else
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<16, false>, WARPS * 32, 0);
+  if (tier == 0) {
+    if (trace) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KA, true, 4>, WARPS * 32, 0);
+    else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KA, false, 4>, WARPS * 32, 0);
+  } else {
+    if (trace) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KB, true, 1>, WARPS * 32, 0);
+    else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KB, false, 1>, WARPS * 32, 0);
+  }
   return nb > 0 ? nb : 1;
 }
 

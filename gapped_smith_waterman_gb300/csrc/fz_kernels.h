@@ -10,6 +10,9 @@ namespace fz {
 struct WorkArgs {
   const uint32_t* list;        // extension ids, or nullptr for 0 .. n_work-1
   uint32_t n_work;
+  const uint32_t* n_work_dev;  // if set, the work count is read from device memory
+  uint32_t* ovf_list;          // register-window inspector: extensions to retry wider
+  uint32_t* ovf_count;
   uint32_t* counter;           // dynamic work counter, zeroed before the launch
   ExtRec* rec;
   uint32_t* wide_list;         // inspector: extensions whose band outgrew the register window
@@ -25,10 +28,11 @@ struct WorkArgs {
 };
 
 // register-window sweep (extend_fast.cu)
-int fast_window_rows();
-cudaError_t launch_inspect_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
-cudaError_t launch_execute_fast(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
-int extend_fast_blocks_per_sm(bool trace);
+// tier 0: 384-row window, tier 1: 512-row window
+int fast_window_rows(int tier);
+cudaError_t launch_inspect_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+cudaError_t launch_execute_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+int extend_fast_blocks_per_sm(int tier, bool trace);
 
 // general band sweep (extend_wide.cu)
 uint64_t wide_scratch_elems(int32_t max_len);   // per warp
