@@ -61,13 +61,6 @@ __device__ __forceinline__ uint32_t res_take(Reservoir& r, const uint8_t* s, uin
   return b;
 }
 
-__device__ __forceinline__ int32_t hi_row(uint32_t mask, int32_t base, int K) {
-  return mask ? base + (32 - __clz(mask)) * K - 1 : -0x7fffffff;
-}
-__device__ __forceinline__ int32_t lo_row(uint32_t mask, int32_t base, int K) {
-  return mask ? base + (__ffs(mask) - 1) * K : 0x7fffffff;
-}
-
 // Eager traceback inside the 16x16 corner (FastZ section 3.1.2): recompute
 // cells (i, j), i, j <= 16, with the sweep's thresholds, lane = row, then walk
 // back from (bi, bj).  Returns the walk as 2-bit ops, first op = last column.
@@ -137,12 +130,12 @@ __device__ __noinline__ void eager_corner(const Params& p, const Window& w, int 
   __syncwarp();
 }
 
-// Register state of one lane: K consecutive rows of the window.
-template <int K>
+// Register state of one lane: up to KS consecutive rows of the window.
+template <int KS>
 struct LaneState {
-  int32_t H[K], HP[K], I[K], D[K];
-  uint32_t MR[K];
-  uint32_t QP[K / 2];
+  int32_t H[KS], HP[KS], I[KS], D[KS];
+  uint32_t MR[KS];
+  uint32_t QP[KS / 2];
 };
 
 struct StepIn {
@@ -153,26 +146,28 @@ struct StepIn {
   uint32_t mr_new;     // SHIFT: substitution row entering lane 31
 };
 
-// One anti-diagonal step.  Returns the lane max of the pruned h; cnt counts
-// live cells; packed receives the direction codes in TRACE mode.
-template <int K, bool TRACE, bool SHIFT, bool EDGE>
-__device__ __forceinline__ int32_t step(LaneState<K>& L, const StepIn& in, int lane, uint32_t& cnt,
+// One anti-diagonal step over the first KA slots of every lane (a 32*KA-row
+// window).  Returns the lane max of the pruned h; cnt counts live cells;
+// packed receives the direction codes in TRACE mode.
+template <int KS, int KA, bool TRACE, bool SHIFT, bool EDGE>
+__device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int lane, uint32_t& cnt,
                                         uint64_t& packed) {
-  constexpr int KH = K / 2;
+  static_assert(KA <= KS && KA % 2 == 0, "active slots");
+  constexpr int KH = KA / 2;
   int32_t lm = NEG;
   if (!SHIFT) {
-    const int32_t dtop = __viaddmax_s32(L.D[K - 1], in.ne, L.H[K - 1]);
+    const int32_t dtop = __viaddmax_s32(L.D[KA - 1], in.ne, L.H[KA - 1]);
     int32_t dc_top = __shfl_up_sync(FULL, dtop, 1);
-    int32_t hp_top = __shfl_up_sync(FULL, L.HP[K - 1], 1);
+    int32_t hp_top = __shfl_up_sync(FULL, L.HP[KA - 1], 1);
     uint32_t qs_top = __shfl_up_sync(FULL, L.QP[KH - 1] >> 16, 1);
     int32_t hu_top = 0;
-    if (TRACE) hu_top = __shfl_up_sync(FULL, L.H[K - 1], 1);
+    if (TRACE) hu_top = __shfl_up_sync(FULL, L.H[KA - 1], 1);
     if (lane == 0) { dc_top = NEG; hp_top = NEG; qs_top = 0x4440u | in.qb; hu_top = NEG; }
 #pragma unroll
     for (int k = KH - 1; k >= 1; --k) L.QP[k] = __funnelshift_l(L.QP[k - 1], L.QP[k], 16);
     L.QP[0] = (L.QP[0] << 16) | qs_top;
 #pragma unroll
-    for (int r = K - 1; r >= 0; --r) {
+    for (int r = KA - 1; r >= 0; --r) {
       const int32_t hl = L.H[r];
       const int32_t Ic = __viaddmax_s32(L.I[r], in.ne, hl);
       const int32_t Dc = r ? __viaddmax_s32(L.D[r - 1], in.ne, L.H[r - 1]) : dc_top;
@@ -186,14 +181,14 @@ __device__ __forceinline__ int32_t step(LaneState<K>& L, const StepIn& in, int l
       if (TRACE) {
         const int32_t hu = r ? L.H[r - 1] : hu_top;
         const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
-        packed |= (uint64_t)code << (4 * r);
+        packed += (uint64_t)code * (1ull << (4 * r));   // disjoint nibbles: add = or
       }
       L.HP[r] = hl;
       L.H[r] = alive ? hn : NEG;
       L.I[r] = Ic;
       L.D[r] = Dc;
       lm = imax(lm, L.H[r]);
-      cnt += alive ? 1u : 0u;
+      if (!TRACE) cnt += alive ? 1u : 0u;                // the replay does not count
     }
   } else {
     const int32_t itop = __viaddmax_s32(L.I[0], in.ne, L.H[0]);
@@ -202,12 +197,12 @@ __device__ __forceinline__ int32_t step(LaneState<K>& L, const StepIn& in, int l
     uint32_t mr_top = __shfl_down_sync(FULL, L.MR[0], 1);
     if (lane == 31) { ic_top = NEG; h_top = NEG; mr_top = in.mr_new; }
 #pragma unroll
-    for (int r = 0; r < K - 1; ++r) L.MR[r] = L.MR[r + 1];
-    L.MR[K - 1] = mr_top;
+    for (int r = 0; r < KA - 1; ++r) L.MR[r] = L.MR[r + 1];
+    L.MR[KA - 1] = mr_top;
 #pragma unroll
-    for (int r = 0; r < K; ++r) {
-      const int32_t hl = r < K - 1 ? L.H[r + 1] : h_top;
-      const int32_t Ic = r < K - 1 ? __viaddmax_s32(L.I[r + 1], in.ne, L.H[r + 1]) : ic_top;
+    for (int r = 0; r < KA; ++r) {
+      const int32_t hl = r < KA - 1 ? L.H[r + 1] : h_top;
+      const int32_t Ic = r < KA - 1 ? __viaddmax_s32(L.I[r + 1], in.ne, L.H[r + 1]) : ic_top;
       const int32_t hu = L.H[r];
       const int32_t Dc = __viaddmax_s32(L.D[r], in.ne, hu);
       const int32_t hp = L.HP[r];
@@ -219,25 +214,133 @@ __device__ __forceinline__ int32_t step(LaneState<K>& L, const StepIn& in, int l
       if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
       if (TRACE) {
         const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
-        packed |= (uint64_t)code << (4 * r);
+        packed += (uint64_t)code * (1ull << (4 * r));
       }
       L.HP[r] = hl;
       L.H[r] = alive ? hn : NEG;
       L.I[r] = Ic;
       L.D[r] = Dc;
       lm = imax(lm, L.H[r]);
-      cnt += alive ? 1u : 0u;
+      if (!TRACE) cnt += alive ? 1u : 0u;
     }
   }
   return lm;
 }
 
-template <int K, bool TRACE>
+// Lane l's KA direction codes of one anti-diagonal: nibbles l*KA .. l*KA+KA-1
+// of the row (KA/2 bytes; 16-bit stores when they stay aligned).
+template <int KA>
+__device__ __forceinline__ void store_codes(uint8_t* row, int lane, uint64_t packed) {
+  uint8_t* dst = row + lane * (KA / 2);
+  if (KA % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < KA / 4; ++k) reinterpret_cast<uint16_t*>(dst)[k] = (uint16_t)(packed >> (16 * k));
+  } else {
+#pragma unroll
+    for (int k = 0; k < KA / 2; ++k) dst[k] = (uint8_t)(packed >> (8 * k));
+  }
+}
+
+// Per-warp shared buffer used to re-lay the window out when its size changes.
+template <int KS>
+struct Relay {
+  int32_t H[32 * KS], HP[32 * KS], I[32 * KS], D[32 * KS];
+  uint8_t t[32 * KS], q[32 * KS];
+};
+
+// Change the window from kold to knew active slots per lane, keeping its base
+// row b: row b+u moves from lane u/kold, slot u%kold to lane u/knew, slot
+// u%knew.  Rows that did not exist before (growing) are dead; their target
+// bases and query bases (column d - row) are read from memory.  When shrinking
+// the caller guarantees the dropped rows are dead.
+template <int KS>
+__device__ __forceinline__ void relayout(LaneState<KS>& L, int kold, int knew, int32_t b, int32_t d, int lane,
+                                      Relay<KS>* rb, const Params& p, const Window& w, const uint32_t* s_mrow) {
+#pragma unroll
+  for (int r = 0; r < KS; ++r) {
+    if (r < kold) {
+      const int u = lane * kold + r;
+      rb->H[u] = L.H[r];
+      rb->HP[u] = L.HP[r];
+      rb->I[u] = L.I[r];
+      rb->D[u] = L.D[r];
+      uint32_t t = 0;
+      for (uint32_t k = 3; k > 0; --k) t = (s_mrow[k] == L.MR[r]) ? k : t;   // base whose row this is
+      if (s_mrow[0] == L.MR[r]) t = 0;
+      rb->t[u] = (uint8_t)t;
+      rb->q[u] = (uint8_t)(((r & 1) ? (L.QP[r >> 1] >> 16) : L.QP[r >> 1]) & 3u);
+    }
+  }
+  __syncwarp();
+  const int rows_old = 32 * kold;
+  const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + (int64_t)lane * knew);
+  const uint32_t qw = fetch16(p.q2, p.q_len, w.qg0, w.dir, (int64_t)d - b - (int64_t)lane * knew - 15);
+  uint32_t sel[KS];
+#pragma unroll
+  for (int r = 0; r < KS; ++r) {
+    sel[r] = 0x4440u;
+    if (r < knew) {
+      const int u = lane * knew + r;
+      if (u < rows_old) {
+        L.H[r] = rb->H[u];
+        L.HP[r] = rb->HP[u];
+        L.I[r] = rb->I[u];
+        L.D[r] = rb->D[u];
+        L.MR[r] = s_mrow[rb->t[u]];
+        sel[r] = 0x4440u | rb->q[u];
+      } else {
+        L.H[r] = NEG; L.HP[r] = NEG; L.I[r] = NEG; L.D[r] = NEG;
+        L.MR[r] = s_mrow[(tw >> (2 * r)) & 3u];
+        sel[r] = 0x4440u | ((qw >> (2 * (15 - r))) & 3u);   // column d - (b + u)
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < KS / 2; ++k) L.QP[k] = sel[2 * k] | (sel[2 * k + 1] << 16);
+  __syncwarp();
+}
+
+// Runs one step with ka active slots (ka even, 4 <= ka <= KS) and stores the
+// direction codes of the anti-diagonal in TRACE mode.
+template <int KS, bool TRACE, bool SHIFT, bool EDGE>
+__device__ __forceinline__ int32_t step_any(int ka, LaneState<KS>& L, const StepIn& in, int lane, uint32_t& cnt,
+                                            uint8_t* row) {
+  uint64_t packed = 0;
+  int32_t lm = NEG;
+#define FZ_STEP_CASE(KA_)                                                   \
+  case KA_:                                                                 \
+    if constexpr (KA_ <= KS) {                                              \
+      lm = step<KS, KA_, TRACE, SHIFT, EDGE>(L, in, lane, cnt, packed);     \
+      if (TRACE) store_codes<KA_>(row, lane, packed);                       \
+    }                                                                       \
+    break;
+  switch (ka) {
+    FZ_STEP_CASE(4)
+    FZ_STEP_CASE(6)
+    FZ_STEP_CASE(8)
+    FZ_STEP_CASE(10)
+    FZ_STEP_CASE(12)
+    FZ_STEP_CASE(14)
+    default:
+      if constexpr (KS >= 16) {
+        lm = step<KS, 16, TRACE, SHIFT, EDGE>(L, in, lane, cnt, packed);
+        if (TRACE) store_codes<16>(row, lane, packed);
+      }
+      break;
+  }
+#undef FZ_STEP_CASE
+  return lm;
+}
+
+// ADAPT: resize the window to the live band (the executor, whose replays are
+// short and spend most steps on a narrow band); without it the window stays at
+// KS rows per lane (the inspector: one step variant keeps its loop small).
+template <int KS, bool TRACE, bool ADAPT>
 __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint32_t idx, int lane,
-                        int32_t* sT, uint8_t* tile, const uint32_t* s_mrow, const int32_t* s_sub) {
-  static_assert(K % 4 == 0 && K <= 16, "one 16-base fetch per lane, whole bytes of codes");
-  constexpr int KH = K / 2;
-  constexpr int32_t WIN = 32 * K;
+                        int32_t* sT, uint8_t* tile, const uint32_t* s_mrow, const int32_t* s_sub, Relay<KS>* rb) {
+  static_assert(KS % 2 == 0 && KS <= 16, "one 16-base fetch per lane");
+  constexpr int32_t WMAX = 32 * KS;          // trace row width: the widest window
+  constexpr int32_t NOROW_HI = -0x3fffffff, NOROW_LO = 0x3fffffff;
   const Window w = make_window(p, ext);
   ExtRec* R = wa.rec + ext;
   if (!w.requested) {
@@ -254,102 +357,119 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
   if (TRACE) {
     d_stop = R->i_end + R->j_end;
     tbase = wa.trace + (wa.trace_off[idx] - wa.trace_sub);
-    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(WIN, d_stop));
+    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(WMAX, d_stop));
     if (lane == 0) lo_arr[0] = 0;
   }
 
-  LaneState<K> L;
+  // The window starts with 4 rows per lane (128 rows) and is re-laid out as
+  // the live band grows and shrinks (always an even number of rows per lane).
+  int kact = ADAPT ? 4 : KS;
+  LaneState<KS> L;
   {
-    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * K);
+    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * kact);
 #pragma unroll
-    for (int r = 0; r < K; ++r) {
-      L.MR[r] = s_mrow[(tw >> (2 * r)) & 3u];
+    for (int r = 0; r < KS; ++r) {
+      L.MR[r] = s_mrow[r < kact ? (tw >> (2 * r)) & 3u : 0u];
       L.H[r] = NEG; L.HP[r] = NEG; L.I[r] = NEG; L.D[r] = NEG;
     }
 #pragma unroll
-    for (int k = 0; k < KH; ++k) L.QP[k] = 0x44404440u;
+    for (int k = 0; k < KS / 2; ++k) L.QP[k] = 0x44404440u;
     if (lane == 0) L.H[0] = -oe;                       // origin: S(0,0) = 0
   }
   Reservoir qr, tr;
-  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);        // query columns 1, 2, ...
-  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);      // target rows WIN, WIN+1, ...
+  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);        // query columns 1, 2, ... entering at row b
+  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, 32 * kact);   // target rows entering at the window top
 
   StepIn in;
   in.oe = oe;
   in.ne = -p.e;
   in.c1 = oe - 128;
-  int32_t b = 0, b_prev = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
-  uint32_t lmask = 1u, lmask_prev = 0u;
+  int32_t T = threshold(0, p.ydrop);
+  int32_t b = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
+  int32_t hi_c = 0, lo_c = 0, hi_p = NOROW_HI, lo_p = NOROW_LO;   // live row bounds at d and d-1
   bool live = true, live_prev = false, rowb_alive = true;
   uint32_t cnt = lane == 0 ? 1u : 0u;
   bool overflow = false;
+  int cool = 0;
 
   for (;;) {
     const int32_t dn = d + 1;
-    if (dn > m + n || d >= d_stop) break;
+    if (dn > m + n) break;
+    if (TRACE && d >= d_stop) break;
     const bool shift = !rowb_alive;
     const int32_t bn = b + (shift ? 1 : 0);
-    if (!TRACE && !shift && (((lmask >> 31) & 1u) || (b_prev == b && ((lmask_prev >> 31) & 1u)))) {
-      overflow = true;   // the live band may grow past the window top
+    const int32_t hi_max = imax(hi_c, hi_p);
+    // rows from the next base to the highest row that may be live
+    const int32_t need = hi_max - bn + 1;
+    if (ADAPT) {
+      int kt = kact;
+      if (need > 29 * kact) {
+        kt = imin(KS, imax(kact + 2, (((need + 64 + 31) >> 5) + 1) & ~1));
+      } else if (cool <= 0 && need + 96 <= 32 * (kact - 2)) {
+        kt = imax(4, (((need + 64 + 31) >> 5) + 1) & ~1);
+      }
+      if (kt != kact) {
+        relayout<KS>(L, kact, kt, b, d, lane, rb, p, w, s_mrow);
+        kact = kt;
+        res_init(tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + 32 * kact);
+        cool = 32;
+      }
+      --cool;
+    }
+    const int32_t WIN = 32 * kact;
+    if (!TRACE && hi_max >= bn + WIN - 1) {
+      overflow = true;   // the live band may grow past the widest window
       break;
     }
-    const int32_t T = threshold(best, p.ydrop);
     in.Th = T - oe;
-    // window bounds matter only near row m (window top past m) or column n
-    // (base at or below d - n); the lane-granular test runs only then
-    bool edge = false;
-    if (bn + WIN - 1 > m || b_prev <= d - n)
-      edge = (bn + WIN - 1 > m && (hi_row(lmask, b, K) >= m || hi_row(lmask_prev, b_prev, K) >= m)) ||
-             lo_row(lmask, b, K) <= d - n || lo_row(lmask_prev, b_prev, K) <= d - 1 - n;
-    const int32_t rowbase = bn + lane * K;
+    const bool edge = (bn + WIN - 1 > m && hi_max >= m) || lo_c <= d - n || lo_p <= d - 1 - n;
+    const int32_t rowbase = bn + lane * kact;
     in.vhi = m - rowbase;
     in.vlo = dn - n - rowbase;
-    uint64_t packed = 0;
+    uint8_t* row = TRACE ? tbase + (uint64_t)dn * (WMAX / 2) : nullptr;
     int32_t lm;
     if (!shift) {
       in.qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-      lm = edge ? step<K, TRACE, false, true>(L, in, lane, cnt, packed)
-                : step<K, TRACE, false, false>(L, in, lane, cnt, packed);
+      lm = edge ? step_any<KS, TRACE, false, true>(kact, L, in, lane, cnt, row)
+                : step_any<KS, TRACE, false, false>(kact, L, in, lane, cnt, row);
     } else {
       in.mr_new = s_mrow[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-      lm = edge ? step<K, TRACE, true, true>(L, in, lane, cnt, packed)
-                : step<K, TRACE, true, false>(L, in, lane, cnt, packed);
+      lm = edge ? step_any<KS, TRACE, true, true>(kact, L, in, lane, cnt, row)
+                : step_any<KS, TRACE, true, false>(kact, L, in, lane, cnt, row);
     }
 
     const int32_t wm = __reduce_max_sync(FULL, lm);
     const uint32_t mask = __ballot_sync(FULL, lm >= in.Th);
-    const uint32_t rb = __ballot_sync(FULL, L.H[0] >= in.Th) & 1u;
+    const uint32_t rbit = __ballot_sync(FULL, L.H[0] >= in.Th) & 1u;
     const bool any = mask != 0u;
     if (any) {
       d_last = dn;
       const int32_t sbest = wm + oe;
       if (sbest > best) {
-        int rf = K;
+        if (!TRACE) {                       // the replay needs only the threshold
+          int rf = KS;
 #pragma unroll
-        for (int r = K - 1; r >= 0; --r) rf = (L.H[r] == wm) ? r : rf;
-        const uint32_t fm = __ballot_sync(FULL, rf < K);
-        const int Ln = __ffs(fm) - 1;
-        const int rr = __shfl_sync(FULL, rf, Ln);
-        bi = bn + Ln * K + rr;
-        bj = dn - bi;
+          for (int r = KS - 1; r >= 0; --r) rf = (r < kact && L.H[r] == wm) ? r : rf;
+          const uint32_t fm = __ballot_sync(FULL, rf < KS);
+          const int Ln = __ffs(fm) - 1;
+          const int rr = __shfl_sync(FULL, rf, Ln);
+          bi = bn + Ln * kact + rr;
+          bj = dn - bi;
+        }
         best = sbest;
+        T = threshold(best, p.ydrop);
       }
     }
-    if (!TRACE && dn <= 2 * EAGER_N && lane == 0) sT[dn] = T;
-    if (TRACE) {
-      uint8_t* row = tbase + (uint64_t)dn * (WIN / 2) + lane * (K / 2);
-      if (K == 16) {
-        *reinterpret_cast<uint64_t*>(row) = packed;
-      } else {
-#pragma unroll
-        for (int k = 0; k < K / 4; ++k) reinterpret_cast<uint16_t*>(row)[k] = (uint16_t)(packed >> (16 * k));
-      }
-      if (lane == 0) lo_arr[dn] = bn;
-    }
-    lmask_prev = lmask; lmask = mask;
-    b_prev = b; b = bn;
-    live_prev = live; live = any;
-    rowb_alive = rb != 0u;
+    if (!TRACE && dn <= 2 * EAGER_N && lane == 0) sT[dn] = in.Th + oe;
+    if (TRACE && lane == 0) lo_arr[dn] = bn;
+    hi_p = hi_c;
+    lo_p = lo_c;
+    hi_c = any ? bn + (32 - __clz(mask)) * kact - 1 : NOROW_HI;
+    lo_c = any ? bn + (__ffs(mask) - 1) * kact : NOROW_LO;
+    b = bn;
+    live_prev = live;
+    live = any;
+    rowb_alive = rbit != 0u;
     d = dn;
     if (!live && !live_prev) break;
   }
@@ -360,9 +480,153 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
 
   if (TRACE) {
-    if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)tot);
+    if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)d_stop * (unsigned long long)WMAX);
     return;
   }
+  if (overflow) {
+    if (lane == 0) {
+      ExtRec z = {};
+      z.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE;
+      z.m = m;
+      z.n = n;
+      *R = z;
+      const uint32_t slot = atomicAdd(wa.ovf_count, 1u);   // retried with a wider window
+      wa.ovf_list[slot] = ext;
+    }
+    return;
+  }
+  uint64_t path = 0;
+  uint32_t npath = 0;
+  uint32_t flags = FZ_FLAG_DONE;
+  uint32_t width = WMAX;
+  if (bi <= EAGER_N && bj <= EAGER_N) {
+    flags |= FZ_FLAG_EAGER;
+    width = 0;
+    if (bi + bj > 0) eager_corner(p, w, lane, sT, tile, s_sub, bi, bj, path, npath, wa.err);
+  }
+  if (lane == 0) {
+    ExtRec o;
+    o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
+    o.live = tot; o.path = path; o.flags = flags; o.npath = npath;
+    o.m = m; o.n = n; o.width = width; o.pad = 0;
+    *R = o;
+    atomicAdd(wa.live_total, (unsigned long long)tot);
+  }
+}
+
+// Inspector sweep with a fixed window of KS rows per lane.  The executor's
+// run_ext keeps the general bookkeeping (window resizing, exact row bounds);
+// this loop keeps only what the inspector needs per step:
+//   * overflow: the top lane held a live cell at d or d-1 and the base stays;
+//   * edge mode whenever rows beyond m or columns beyond n exist inside the
+//     window (then every cell checks its bounds);
+//   * liveness of the anti-diagonal from its maximum, row b's liveness and the
+//     top lane's from one ballot;
+//   * the threshold, recomputed only when the best score changes.
+template <int KS>
+__device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, int lane, int32_t* sT,
+                            uint8_t* tile, const uint32_t* s_mrow, const int32_t* s_sub) {
+  static_assert(KS % 2 == 0 && KS <= 16, "one 16-base fetch per lane");
+  constexpr int32_t WIN = 32 * KS;
+  const Window w = make_window(p, ext);
+  ExtRec* R = wa.rec + ext;
+  if (!w.requested) {
+    if (lane == 0) {
+      ExtRec z = {};
+      *R = z;
+    }
+    return;
+  }
+  const int32_t m = w.m, n = w.n, oe = p.oe, mn = w.m + w.n;
+  LaneState<KS> L;
+  {
+    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * KS);
+#pragma unroll
+    for (int r = 0; r < KS; ++r) {
+      L.MR[r] = s_mrow[(tw >> (2 * r)) & 3u];
+      L.H[r] = NEG; L.HP[r] = NEG; L.I[r] = NEG; L.D[r] = NEG;
+    }
+#pragma unroll
+    for (int k = 0; k < KS / 2; ++k) L.QP[k] = 0x44404440u;
+    if (lane == 0) L.H[0] = -oe;                       // origin: S(0,0) = 0
+  }
+  Reservoir qr, tr;
+  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);        // query columns entering at row b
+  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);      // target rows entering at the window top
+
+  StepIn in;
+  in.oe = oe;
+  in.ne = -p.e;
+  in.c1 = oe - 128;
+  in.Th = threshold(0, p.ydrop) - oe;
+  int32_t b = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
+  bool live_prev = true, rowb_alive = true, top = false, top_prev = false;
+  uint32_t cnt = lane == 0 ? 1u : 0u;
+  bool overflow = false;
+  uint64_t no_codes = 0;   // direction codes are the executor's
+
+  for (;;) {
+    const int32_t dn = d + 1;
+    if (dn > mn) break;
+    const bool shift = !rowb_alive;
+    const int32_t bn = b + (shift ? 1 : 0);
+    if (!shift && (top || top_prev)) {
+      overflow = true;   // the live band may grow past the window top
+      break;
+    }
+    const bool edge = bn + WIN - 1 > m || bn < dn - n;
+    int32_t lm;
+    if (!shift) {
+      in.qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
+      if (edge) {
+        const int32_t rowbase = bn + lane * KS;
+        in.vhi = m - rowbase;
+        in.vlo = dn - n - rowbase;
+        lm = step<KS, KS, false, false, true>(L, in, lane, cnt, no_codes);
+      } else {
+        lm = step<KS, KS, false, false, false>(L, in, lane, cnt, no_codes);
+      }
+    } else {
+      in.mr_new = s_mrow[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+      if (edge) {
+        const int32_t rowbase = bn + lane * KS;
+        in.vhi = m - rowbase;
+        in.vlo = dn - n - rowbase;
+        lm = step<KS, KS, false, true, true>(L, in, lane, cnt, no_codes);
+      } else {
+        lm = step<KS, KS, false, true, false>(L, in, lane, cnt, no_codes);
+      }
+    }
+    const int32_t wm = __reduce_max_sync(FULL, lm);
+    const bool edge_lane = (lane == 0 && L.H[0] >= in.Th) || (lane == 31 && lm >= in.Th);
+    const uint32_t bits = __ballot_sync(FULL, edge_lane);
+    sT[imin(dn, 2 * EAGER_N + 1)] = in.Th + oe;       // thresholds of anti-diagonals 1..32 (33: scratch)
+    const bool live = wm >= in.Th;
+    if (wm + oe > best) {                                // implies live
+      int rf = KS;
+#pragma unroll
+      for (int r = KS - 1; r >= 0; --r) rf = (L.H[r] == wm) ? r : rf;
+      const uint32_t fm = __ballot_sync(FULL, rf < KS);
+      const int Ln = __ffs(fm) - 1;
+      const int rr = __shfl_sync(FULL, rf, Ln);
+      bi = bn + Ln * KS + rr;
+      bj = dn - bi;
+      best = wm + oe;
+      in.Th = threshold(best, p.ydrop) - oe;
+    }
+    d_last = live ? dn : d_last;
+    rowb_alive = bits & 1u;
+    top_prev = top && !shift;      // the old top row is still the top row only if the base stayed
+    top = (bits >> 31) != 0u;
+    b = bn;
+    d = dn;
+    if (!live && !live_prev) break;
+    live_prev = live;
+  }
+
+  uint64_t tot = cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
   if (overflow) {
     if (lane == 0) {
       ExtRec z = {};
@@ -397,10 +661,11 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
 // MINB: resident blocks per SM the register budget is fitted to.
 template <int K, bool TRACE, int MINB>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_extend(Params p, WorkArgs wa) {
-  __shared__ int32_t s_T[WARPS][2 * EAGER_N + 1];
+  __shared__ int32_t s_T[WARPS][2 * EAGER_N + 2];
   __shared__ uint8_t s_tile[WARPS][(EAGER_N + 1) * (EAGER_N + 1)];
   __shared__ uint32_t s_mrow[4];
   __shared__ int32_t s_sub[16];
+  __shared__ Relay<TRACE ? K : 2> s_relay[WARPS];
   if (threadIdx.x < 4) s_mrow[threadIdx.x] = p.mrow[threadIdx.x];
   if (threadIdx.x < 16) s_sub[threadIdx.x] = p.sub[threadIdx.x];
   __syncthreads();
@@ -417,7 +682,11 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_extend(Params p, WorkArgs 
       const ExtRec& r = wa.rec[ext];
       if ((r.flags & FZ_FLAG_WIDE) || r.width != (uint32_t)(32 * K)) continue;
     }
-    run_ext<K, TRACE>(p, wa, ext, idx, lane, s_T[warp], s_tile[warp], s_mrow, s_sub);
+    if (TRACE)
+      run_ext<K, true, true>(p, wa, ext, idx, lane, s_T[warp], s_tile[warp], s_mrow, s_sub,
+                             reinterpret_cast<Relay<K>*>(&s_relay[warp]));
+    else
+      run_inspect<K>(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow, s_sub);
   }
 }
 

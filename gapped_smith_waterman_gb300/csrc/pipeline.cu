@@ -241,6 +241,18 @@ __global__ void k_emit_exec(EmitArgs a) {
     const int32_t u = i - lo[d];
     if (u < 0 || (uint32_t)u >= W) { atomicOr(a.err, 1u); break; }
     const uint32_t c = (base[(uint64_t)d * (W / 2) + (uint32_t)(u >> 1)] >> (4 * (u & 1))) & 15u;
+    // The walk visits one row per step, going down in d: pull the row it will
+    // reach PF anti-diagonals later (around where the path should be) and the
+    // row origins further ahead into L2.  Addresses stay inside this
+    // extension's rows.
+    constexpr int32_t PF = 12;
+    if (d >= PF) {
+      const int32_t dp = d - PF;
+      int32_t up = i - PF / 2 - lo[dp];
+      up = up < 0 ? 0 : ((uint32_t)up >= W ? (int32_t)W - 1 : up);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (uint64_t)dp * (W / 2) + (uint32_t)(up >> 1)));
+      if (d >= 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(lo + (d - 64)));
+    }
     if (st == 0) {
       const uint32_t sc = c & 3u;
       if (sc == 0) { wr.push(0); --i; --j; }

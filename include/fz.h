@@ -83,7 +83,7 @@ typedef struct {
 
 typedef struct {
     uint64_t live_cells;    /* live cells of all inspector sweeps (EXTEND) or m*n cells (LOCAL) */
-    uint64_t exec_cells;    /* cells the executor recomputed */
+    uint64_t exec_cells;    /* window cells the executor recomputed (register-window path) */
     uint32_t eager;         /* extensions traced back inside the inspector */
     uint32_t bin[5];        /* executor bins: max(i*, j*) <= 512, 2048, 8192, 32768, 131072 */
     uint32_t extensions;    /* one-sided extensions computed */

@@ -31,12 +31,12 @@ class OrcResult(ctypes.Structure):
     _fields_ = [("score", ctypes.c_int32), ("i_end", ctypes.c_int32), ("j_end", ctypes.c_int32),
                 ("d_last", ctypes.c_int32), ("live_cells", ctypes.c_int64),
                 ("n_cigar", ctypes.c_int32), ("status", ctypes.c_int32), ("max_width", ctypes.c_int32),
-                ("pad", ctypes.c_int32)]
+                ("narrow_steps", ctypes.c_int32)]
 
 
 RESULT_DTYPE = np.dtype([("score", "<i4"), ("i_end", "<i4"), ("j_end", "<i4"), ("d_last", "<i4"),
                          ("live_cells", "<i8"), ("n_cigar", "<i4"), ("status", "<i4"), ("max_width", "<i4"),
-                         ("pad", "<i4")])
+                         ("narrow_steps", "<i4")])
 assert RESULT_DTYPE.itemsize == ctypes.sizeof(OrcResult)
 
 

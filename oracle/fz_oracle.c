@@ -66,7 +66,7 @@ typedef struct {
     int32_t n_cigar;         /* CIGAR runs written */
     int32_t status;          /* 0 ok, -1 out of memory, -2 CIGAR buffer too small */
     int32_t max_width;       /* diagnostic: widest candidate row range of one anti-diagonal */
-    int32_t pad;
+    int32_t narrow_steps;    /* diagnostic: anti-diagonals whose candidate range spans <= 160 rows */
 } orc_result;
 
 static void store_free(store* st) {
@@ -169,6 +169,7 @@ int orc_extend(const uint8_t* t, int32_t m, const uint8_t* q, int32_t n, const i
         if (lo > hi) break;                      /* d-1 and d-2 hold no live cell */
         if (store_push_diag(&st, lo, hi)) { store_free(&st); res->status = -1; return -1; }
         if (hi - lo + 1 > res->max_width) res->max_width = hi - lo + 1;
+        if (hi - lo + 1 <= 160) res->narrow_steps++;
         diag_rec* r = &st.dg[d];
         const int64_t T = (int64_t)best - ydrop;   /* prune threshold of this anti-diagonal */
         int32_t dmax = NEG, dmax_i = -1;
