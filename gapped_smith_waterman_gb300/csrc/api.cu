@@ -383,6 +383,7 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
   p.oe = gap_open + gap_extend;
   p.ydrop = ydrop;
   p.max_len = max_len;
+  p.one = 1;
   for (int k = 0; k < 16; ++k) {
     p.sub[k] = sub[k];
     ctx->max_sub = std::max(ctx->max_sub, sub[k]);

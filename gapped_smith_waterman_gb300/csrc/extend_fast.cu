@@ -142,6 +142,7 @@ struct StepIn {
   int32_t Th;          // threshold on h = S - o - e for the new anti-diagonal
   int32_t vhi, vlo;    // edge mode: slot r is inside the window iff vlo <= r <= vhi
   int32_t oe, ne, c1;
+  int32_t one;         // 1 (Params::one)
   uint32_t qb;         // NOSHIFT: query base entering lane 0
   uint32_t mr_new;     // SHIFT: substitution row entering lane 31
 };
@@ -159,7 +160,7 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
     const int32_t dtop = __viaddmax_s32(L.D[KA - 1], in.ne, L.H[KA - 1]);
     int32_t dc_top = __shfl_up_sync(FULL, dtop, 1);
     int32_t hp_top = __shfl_up_sync(FULL, L.HP[KA - 1], 1);
-    uint32_t qs_top = __shfl_up_sync(FULL, L.QP[KH - 1] >> 16, 1);
+    uint32_t qs_top = __shfl_up_sync(FULL, __umulhi(L.QP[KH - 1], 65536u), 1);
     int32_t hu_top = 0;
     if (TRACE) hu_top = __shfl_up_sync(FULL, L.H[KA - 1], 1);
     if (lane == 0) { dc_top = NEG; hp_top = NEG; qs_top = 0x4440u | in.qb; hu_top = NEG; }
@@ -172,10 +173,10 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       const int32_t Ic = __viaddmax_s32(L.I[r], in.ne, hl);
       const int32_t Dc = r ? __viaddmax_s32(L.D[r - 1], in.ne, L.H[r - 1]) : dc_top;
       const int32_t hp = r ? L.HP[r - 1] : hp_top;
-      const uint32_t sel = (r & 1) ? (L.QP[r >> 1] >> 16) : L.QP[r >> 1];
-      const int32_t G = hp + (int32_t)prmt(L.MR[r], 0u, sel) + in.c1;
+      const uint32_t sel = (r & 1) ? __umulhi(L.QP[r >> 1], 65536u) : L.QP[r >> 1];
+      const int32_t G = imad((int32_t)prmt(L.MR[r], 0u, sel), in.one, hp);   // hp carries + o + e - 128
       const int32_t S = __vimax3_s32(G, Ic, Dc);
-      const int32_t hn = S - in.oe;
+      const int32_t hn = imad(S, in.one, -in.oe);
       bool alive = hn >= in.Th;
       if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
       if (TRACE) {
@@ -183,11 +184,11 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
         const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
         packed += (uint64_t)code * (1ull << (4 * r));   // disjoint nibbles: add = or
       }
-      L.HP[r] = hl;
+      L.HP[r] = imad(hl, in.one, in.c1);   // next step's diagonal source, offset by o + e - 128
       L.H[r] = alive ? hn : NEG;
       L.I[r] = Ic;
       L.D[r] = Dc;
-      lm = imax(lm, L.H[r]);
+      if ((r & 1) == 0) lm = __vimax3_s32(lm, L.H[r], L.H[r + 1]);   // rows r, r+1 are both new
       if (!TRACE) cnt += alive ? 1u : 0u;                // the replay does not count
     }
   } else {
@@ -206,21 +207,21 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       const int32_t hu = L.H[r];
       const int32_t Dc = __viaddmax_s32(L.D[r], in.ne, hu);
       const int32_t hp = L.HP[r];
-      const uint32_t sel = (r & 1) ? (L.QP[r >> 1] >> 16) : L.QP[r >> 1];
-      const int32_t G = hp + (int32_t)prmt(L.MR[r], 0u, sel) + in.c1;
+      const uint32_t sel = (r & 1) ? __umulhi(L.QP[r >> 1], 65536u) : L.QP[r >> 1];
+      const int32_t G = imad((int32_t)prmt(L.MR[r], 0u, sel), in.one, hp);   // hp carries + o + e - 128
       const int32_t S = __vimax3_s32(G, Ic, Dc);
-      const int32_t hn = S - in.oe;
+      const int32_t hn = imad(S, in.one, -in.oe);
       bool alive = hn >= in.Th;
       if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
       if (TRACE) {
         const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
         packed += (uint64_t)code * (1ull << (4 * r));
       }
-      L.HP[r] = hl;
+      L.HP[r] = imad(hl, in.one, in.c1);
       L.H[r] = alive ? hn : NEG;
       L.I[r] = Ic;
       L.D[r] = Dc;
-      lm = imax(lm, L.H[r]);
+      if (r & 1) lm = __vimax3_s32(lm, L.H[r - 1], L.H[r]);           // rows r-1, r are both new
       if (!TRACE) cnt += alive ? 1u : 0u;
     }
   }
@@ -384,6 +385,7 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
   in.oe = oe;
   in.ne = -p.e;
   in.c1 = oe - 128;
+  in.one = p.one;
   int32_t T = threshold(0, p.ydrop);
   int32_t b = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
   int32_t hi_c = 0, lo_c = 0, hi_p = NOROW_HI, lo_p = NOROW_LO;   // live row bounds at d and d-1
@@ -558,6 +560,7 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
   in.oe = oe;
   in.ne = -p.e;
   in.c1 = oe - 128;
+  in.one = p.one;
   in.Th = threshold(0, p.ydrop) - oe;
   int32_t b = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
   bool live_prev = true, rowb_alive = true, top = false, top_prev = false;

@@ -35,6 +35,7 @@ struct Params {
   int32_t o, e, oe;
   int32_t ydrop;          // >= 0, or FZ_YDROP_INF
   int32_t max_len;
+  int32_t one;            // 1, opaque to the compiler (see imad)
   uint32_t mrow[4];       // fast path: byte q of mrow[t] = sub[t][q] + 128
   int32_t sub[16];
 };
@@ -91,6 +92,15 @@ __device__ __forceinline__ uint32_t fetch16(const uint8_t* __restrict__ s, uint6
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// a * b + c as an integer multiply-add.  With b = Params::one (a runtime 1)
+// the compiler keeps the multiply-add, which issues on the FMA pipe and
+// leaves the ALU pipe (DPX max, byte permute, compares) to the rest of a cell.
+__device__ __forceinline__ int32_t imad(int32_t a, int32_t b, int32_t c) {
+  int32_t d;
+  asm("mad.lo.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
 

@@ -319,7 +319,7 @@ extern "C" fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_op
   p.t2 = d_target2; p.q2 = d_query2; p.t_len = t_len; p.q_len = q_len;
   p.seeds = d_seeds; p.n_seeds = n_seeds;
   p.o = gap_open; p.e = gap_extend; p.oe = gap_open + gap_extend;
-  p.ydrop = FZ_YDROP_INF; p.max_len = max_len;
+  p.ydrop = FZ_YDROP_INF; p.max_len = max_len; p.one = 1;
   for (int k = 0; k < 16; ++k) p.sub[k] = sub[k];
   uint32_t mc[4];
   for (int t = 0; t < 4; ++t) {
