@@ -40,7 +40,11 @@ METRIC = "GCUPS and seed extensions/s (affine y-drop batch) at 1 GB300; % of DPX
 # i.e. 16 cells/clk/SM; x 152 SMs x 2.07 GHz max SM clock.
 SMS, SM_MAX_GHZ, CELLS_PER_CLK_SM = 152, 2.07, 16.0
 PEAK_GCUPS = SMS * SM_MAX_GHZ * CELLS_PER_CLK_SM
-PROFILE_JSON = os.path.join(ROOT, "profiles", "inspector_traffic.json")
+# Dominant kernel per mode: (name, source file, committed DRAM-traffic summary).
+DOMINANT = {
+    "extend": ("inspector (register-window sweep)", "extend_fast.cu", "inspector_traffic.json"),
+    "local": ("local fill (k_local)", "local.cu", "local_traffic.json"),
+}
 
 
 def parse():
@@ -134,13 +138,14 @@ def cpu_baseline(w, seconds: float):
                                     np.count_nonzero(w.seeds[idx]["side"] & 2)) / dt}
 
 
-def traffic_for_current_kernel():
-    """Per-launch DRAM bytes of the inspector from the committed ncu summary, if
-    the kernel source has not changed since it was captured; else None."""
+def traffic_for_current_kernel(mode):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if its source has not changed since the capture; else None."""
     import hashlib
+    _, src_name, prof_name = DOMINANT[mode]
     try:
-        prof = json.load(open(PROFILE_JSON))
-        src = open(os.path.join(ROOT, "gapped_smith_waterman_gb300", "csrc", "extend_fast.cu"), "rb").read()
+        prof = json.load(open(os.path.join(ROOT, "profiles", prof_name)))
+        src = open(os.path.join(ROOT, "gapped_smith_waterman_gb300", "csrc", src_name), "rb").read()
         if prof.get("source_sha1") == hashlib.sha1(src).hexdigest():
             return prof.get("dram_bytes_per_launch_full_batch")
     except Exception:
@@ -202,6 +207,8 @@ def main():
     fz.fz_set_profiling(ext.ctx, True)
     d_t, d_q, d_s = ext.upload(t2, q2, seeds)
     d_out = ext.alloc_out(len(seeds))
+    side = seeds["side"].astype(np.int64)
+    n_req = int(((side & 1) != 0).sum() + ((side & 2) != 0).sum())   # one-sided problems per step
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     rates = fz.fz_bench_int_rates() if rank == 0 else None
@@ -227,7 +234,7 @@ def main():
         insp_ms.append(st.phase_ms[0])
         cells += st.live_cells
         launches += st.launches
-        exts += st.extensions
+        exts += st.extensions if w.mode == 0 else n_req
     torch.cuda.synchronize()
     clocks = sampler.stop()
     if ws > 1:
@@ -260,7 +267,7 @@ def main():
             e2e_cells += ext.stats().live_cells
             d2h = h_out.nbytes + 4 * used
         e2e = {"value": ws * e2e_cells / e2e_s / 1e9, "unit": "GCUPS",
-               "extensions_per_s": ws * ne * len(seeds) * (1 if w.mode else 1) / e2e_s,
+               "extensions_per_s": ws * ne * n_req / e2e_s,
                "h2d_bytes_per_step": int(t2.nbytes + q2.nbytes + seeds.nbytes), "d2h_bytes_per_step": int(d2h)}
 
     if rank != 0:
@@ -271,6 +278,7 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, args.cpu_seconds)
+    mode = "local" if w.mode == W.MODE_LOCAL else "extend"
     measured_peak = None
     if rates:
         r = rates
@@ -284,16 +292,20 @@ def main():
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{ws}"},
         "extensions_per_s": ext_per_s,
         "live_cells_per_step": int(cells / args.steps),
-        "roofline": {"bound": "alu", "kernel": "inspector (register-window sweep)",
+        "roofline": {"bound": "alu", "kernel": DOMINANT[mode][0],
                      "achieved": insp_gcups, "peak": PEAK_GCUPS, "unit": "Gcell/s",
                      "frac": (insp_gcups / PEAK_GCUPS) if insp_gcups else None,
                      "peak_basis": "152 SM x 2.07 GHz x 16 cells/clk/SM (2 DPX add-max + 1 DPX max3 at 64/clk, "
                                    "2 IADD at 128/clk per cell)",
                      "peak_measured_int_pipes": measured_peak,
                      "int_rates_gops": {k: v / 1e9 for k, v in (rates or {}).items()},
-                     "traffic": traffic_for_current_kernel(),
-                     "inspector_ms_per_step": sum(insp_ms) / args.steps},
+                     "traffic": traffic_for_current_kernel(mode),
+                     "kernel_ms_per_step": sum(insp_ms) / args.steps},
         "phase_ms_last_step": [round(x, 4) for x in st.phase_ms],
+        "phases": "inspector, wide inspector, bins+scans, executors, traceback+records, whole batch",
+        "batch_stats": {"eager": int(st.eager), "bins": [int(b) for b in st.bin], "wide": int(st.wide),
+                        "executor_window_cells": int(st.exec_cells), "trace_bytes": int(st.trace_bytes),
+                        "cigar_slot_runs": int(st.cigar_runs)},
         "gpu_launches": int(launches),
         "clocks": clocks,
         "e2e": e2e,

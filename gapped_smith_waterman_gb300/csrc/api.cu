@@ -44,6 +44,7 @@ struct Counters {
   unsigned long long exec_total;
   uint64_t trace_total;
   uint64_t cig_total;
+  uint64_t cig_packed;         // runs actually written (host-copy packing)
   uint32_t work[8];            // dynamic work counters: 0..2 inspectors, 3..5 executors
   uint32_t retry_count;        // extensions retried with the 512-row window
   uint32_t wide_count;
@@ -66,7 +67,7 @@ struct fz_ctx {
   uint32_t mcol[4] = {0, 0, 0, 0};
   std::string err;
   DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, retry_list, counters;
-  DevBuf cigar, trace, scratch, spill;
+  DevBuf cigar, cigar_packed, trace, scratch, spill;
   DevBuf in_t, in_q, in_seeds, out_res;
   Counters* h_cnt = nullptr;         // pinned
   cudaStream_t last_stream = nullptr;
@@ -254,6 +255,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   const Counters& hc = *ctx->h_cnt;
   uint32_t n_exec = 0;
   for (int k = 1; k <= 5; ++k) n_exec += hc.bin_count[k];
+  const uint32_t long_end = n_exec - hc.bin_count[1];   // bins 5..2 come first: walked by warps
   if (hc.cig_total >= (1ull << 32)) return fail(ctx, FZ_ERR_ARG, "CIGAR arena would exceed 2^32 runs; split the batch");
   CU(ctx->cigar.ensure(std::max<uint64_t>(hc.cig_total, 1) * 4));
   ctx->stats.trace_bytes = hc.trace_total;
@@ -325,7 +327,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
       ex.exec_begin = c.first;
       ex.exec_end = c.second;
       ex.trace_sub = sub;
-      CU(launch_emit_exec(ex, st));
+      CU(launch_emit_exec(ex, long_end, ctx->sms, st));
       ctx->launches += 1;
     }
   }
@@ -337,7 +339,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
     ex.exec_begin = 0;
     ex.exec_end = n_exec;
     ex.trace_sub = 0;
-    CU(launch_emit_exec(ex, st));
+    CU(launch_emit_exec(ex, long_end, ctx->sms, st));
     ctx->launches += 1;
   }
   mark(ctx, 5, st);
@@ -490,8 +492,24 @@ fz_status fz_extend_batch_host(fz_ctx* ctx, const uint8_t* h_target2, uint64_t t
   fz_status s = fz_extend_batch(ctx, ctx->in_t.as<uint8_t>(), t_len, ctx->in_q.as<uint8_t>(), q_len,
                                 ctx->in_seeds.as<fz_seed>(), n_seeds, ctx->out_res.as<fz_result>(), &dc, cuda_stream);
   if (s != FZ_OK) return s;
+  uint64_t used = 0;
+  if (ctx->mode == FZ_EXTEND && n_seeds && ctx->stats.cigar_runs) {
+    // pack the runs written (slots are sized for the worst case) so that only
+    // they are copied; the records' cigar_off then index h_cigar
+    const uint32_t n_ext = 2 * n_seeds;
+    Counters* dcn = ctx->counters.as<Counters>();
+    fz_result* d_out = ctx->out_res.as<fz_result>();
+    CU(launch_cig_lens(d_out, n_ext, ctx->cig_cap.as<uint64_t>(), st));
+    CU(launch_scan_u64(ctx->cig_cap.as<uint64_t>(), n_ext, ctx->scan_tmp.as<uint64_t>(), &dcn->cig_packed, st));
+    CU(cudaMemcpyAsync(&ctx->h_cnt->cig_packed, &dcn->cig_packed, sizeof(uint64_t), cudaMemcpyDeviceToHost, st));
+    CU(cudaStreamSynchronize(st));
+    used = ctx->h_cnt->cig_packed;
+    CU(ctx->cigar_packed.ensure(std::max<uint64_t>(used, 1) * 4));
+    CU(launch_cig_pack(d_out, n_ext, ctx->cig_cap.as<uint64_t>(), dc, ctx->cigar_packed.as<uint32_t>(), st));
+    ctx->launches += 5;
+    dc = ctx->cigar_packed.as<uint32_t>();
+  }
   if (n_seeds) CU(cudaMemcpyAsync(h_out, ctx->out_res.p, (size_t)n_seeds * 2 * sizeof(fz_result), cudaMemcpyDeviceToHost, st));
-  const uint64_t used = ctx->mode == FZ_EXTEND ? ctx->stats.cigar_runs : 0;
   if (cigar_used) *cigar_used = used;
   if (used && used <= cigar_cap) CU(cudaMemcpyAsync(h_cigar, dc, used * 4, cudaMemcpyDeviceToHost, st));
   CU(cudaStreamSynchronize(st));

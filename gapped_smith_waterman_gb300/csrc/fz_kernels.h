@@ -90,13 +90,23 @@ struct EmitArgs {
   const uint8_t* trace;
   uint64_t trace_sub;
   uint32_t exec_begin, exec_end;
+  uint32_t exec_split;         // set by launch_emit_exec: [begin, split) walked by warps
+  uint32_t long_blocks;        // set by launch_emit_exec
   uint32_t* err;
   int local;
   int32_t oe;
   int32_t max_sub;
 };
 cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st);   // eager, empty, local, not requested
-cudaError_t launch_emit_exec(const EmitArgs& a, cudaStream_t st);     // executor items [exec_begin, exec_end)
+// executor items [exec_begin, exec_end); items before long_end (the bins of
+// longer alignments) get a warp each, the rest a thread each
+cudaError_t launch_emit_exec(EmitArgs a, uint32_t long_end, int sms, cudaStream_t st);
+
+// CIGAR packing for host copies: lens[x] = out[x].cigar_len; then, with poff
+// the exclusive scan of lens, runs copied to dst[poff[x]..] and cigar_off repointed
+cudaError_t launch_cig_lens(const fz_result* out, uint32_t n, uint64_t* lens, cudaStream_t st);
+cudaError_t launch_cig_pack(fz_result* out, uint32_t n, const uint64_t* poff, const uint32_t* src, uint32_t* dst,
+                            cudaStream_t st);
 
 // integer pipe microbenchmark (microbench.cu)
 cudaError_t bench_int_rates(double rates[4]);

@@ -59,11 +59,13 @@ template <bool PARTIAL>
 __device__ __forceinline__ void strip(const Params& p, const Window& w, int lane, int32_t s, int32_t nstrips,
                                       const uint32_t* s_mcol, int32_t* spH, int32_t* spE, int32_t& bv,
                                       int32_t& bd, int32_t& bi) {
-  const int32_t m = w.m, n = w.n, oe = p.oe, ne = -p.e;
+  // Scores are kept as h = H - o - e (the gap-open source of both neighbours),
+  // so each cell subtracts o + e once.
+  const int32_t m = w.m, n = w.n, oe = p.oe, ne = -p.e, c1 = oe - 128;
   const int32_t c0 = s * SW + lane * KC + 1;
   const int32_t kv = imax(0, imin(KC, n - c0 + 1));
   uint32_t QPF[KC];
-  int32_t Hc[KC], F[KC];
+  int32_t hc[KC], F[KC];
   {
     const uint32_t q0 = fetch16(p.q2, p.q_len, w.qg0, w.dir, c0);
     const uint32_t q1 = fetch16(p.q2, p.q_len, w.qg0, w.dir, c0 + 16);
@@ -71,13 +73,13 @@ __device__ __forceinline__ void strip(const Params& p, const Window& w, int lane
     for (int k = 0; k < KC; ++k) {
       const uint32_t qb = ((k < 16 ? q0 : q1) >> (2 * (k & 15))) & 3u;
       QPF[k] = s_mcol[qb];
-      Hc[k] = 0;
+      hc[k] = -oe;                                       // row 0: H = 0
       F[k] = NEG;
     }
   }
   Res tr;
   rinit(tr, p.t2, p.t_len, w.tg0, w.dir, 1);
-  int32_t h_out = 0, e_out = NEG, hh_prev = 0;
+  int32_t h_out = -oe, e_out = NEG, hh_prev = -oe;
   uint32_t t_cur = 0;
   const bool first = s == 0, last = s == nstrips - 1;
   for (int32_t tau = 0; tau < m + 31; ++tau) {
@@ -88,7 +90,7 @@ __device__ __forceinline__ void strip(const Params& p, const Window& w, int lane
     const uint32_t t0 = rtake(tr, p.t2, p.t_len, w.tg0, w.dir);
     if (lane == 0) {
       tb = t0;
-      if (first) { hh = 0; eh = NEG; }
+      if (first) { hh = -oe; eh = NEG; }                 // column 0: H = 0
       else if (i <= m) { hh = spH[i]; eh = spE[i]; }
     }
     if (i >= 1 && i <= m) {
@@ -96,22 +98,24 @@ __device__ __forceinline__ void strip(const Params& p, const Window& w, int lane
       int32_t E = eh, hl = hh, hd = hh_prev, rmax = 0;
 #pragma unroll
       for (int k = 0; k < KC; ++k) {
-        E = __viaddmax_s32(E, ne, hl - oe);
-        F[k] = __viaddmax_s32(F[k], ne, Hc[k] - oe);
-        const int32_t G = hd + (int32_t)prmt(QPF[k], 0u, tsel) - 128;
+        E = __viaddmax_s32(E, ne, hl);
+        F[k] = __viaddmax_s32(F[k], ne, hc[k]);
+        const int32_t G = hd + (int32_t)prmt(QPF[k], 0u, tsel) + c1;
         int32_t H = __vimax3_s32_relu(G, E, F[k]);
         if (PARTIAL) H = k < kv ? H : 0;
-        hd = Hc[k];
-        Hc[k] = H;
-        hl = H;
-        rmax = imax(rmax, H);
+        const int32_t h = H - oe;
+        hd = hc[k];
+        hc[k] = h;
+        hl = h;
+        rmax = imax(rmax, H);   // row max in score space
       }
       h_out = hl;
       e_out = E;
       if (rmax >= bv && rmax > 0) {
+        const int32_t rh = rmax - oe;
         int kf = KC;
 #pragma unroll
-        for (int k = KC - 1; k >= 0; --k) kf = Hc[k] == rmax ? k : kf;
+        for (int k = KC - 1; k >= 0; --k) kf = hc[k] == rh ? k : kf;
         const int32_t c = c0 + kf, d = i + c;
         if (rmax > bv || d < bd || (d == bd && i < bi)) { bv = rmax; bd = d; bi = i; }
       }
@@ -123,7 +127,7 @@ __device__ __forceinline__ void strip(const Params& p, const Window& w, int lane
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(WL * 32) k_local(Params p, LocalArgs la) {
+__global__ void __launch_bounds__(WL * 32, 3) k_local(Params p, LocalArgs la) {
   extern __shared__ int32_t smem[];
   __shared__ uint32_t s_mcol[4];
   if (threadIdx.x < 4) s_mcol[threadIdx.x] = la.mcol[threadIdx.x];
@@ -179,6 +183,7 @@ size_t local_smem_bytes(int32_t max_len) { return (size_t)WL * 2 * (size_t)(max_
 
 int local_blocks_per_sm(size_t smem) {
   int nb = 0;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(k_local, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_local, WL * 32, smem);
   return nb > 0 ? nb : 1;
 }

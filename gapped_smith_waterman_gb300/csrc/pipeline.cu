@@ -8,6 +8,8 @@
 // bin first so that the longest extensions start first.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "fz_dev.cuh"
 #include "fz_kernels.h"
 
@@ -221,26 +223,70 @@ __global__ void k_emit_direct(EmitArgs a) {
   write_out(a.out + x, r, wr.nruns ? wr.first() : (uint32_t)off, wr.nruns, 0);
 }
 
-__global__ void k_emit_exec(EmitArgs a) {
-  const uint32_t pos = a.exec_begin + blockIdx.x * blockDim.x + threadIdx.x;
-  if (pos >= a.exec_end) return;
+// One executor extension's walk state and trace rows.
+struct Walk {
+  const uint8_t* base;       // rows of W/2 bytes, anti-diagonal 0 first
+  const int32_t* lo;         // row origin per anti-diagonal
+  uint64_t bytes;            // size of this extension's trace block
+  uint32_t W;
+  int32_t i, j, st;
+};
+
+__device__ __forceinline__ void walk_init(const EmitArgs& a, uint32_t pos, const ExtRec& r, Walk& w) {
+  const int32_t dend = r.i_end + r.j_end;
+  w.W = r.width;
+  w.base = a.trace + (a.trace_off[pos] - a.trace_sub);
+  w.lo = reinterpret_cast<const int32_t*>(w.base + trace_lo_offset(w.W, dend));
+  w.bytes = trace_bytes(w.W, dend);
+  w.i = r.i_end;
+  w.j = r.j_end;
+  w.st = 0;
+}
+
+// One step of the walk from the code c of the current cell; returns false
+// (with an error bit set) on an impossible code.
+__device__ __forceinline__ bool walk_step(Walk& w, uint32_t c, RunWriter& wr, uint32_t* err) {
+  if (w.st == 0) {
+    const uint32_t sc = c & 3u;
+    if (sc == 0) { wr.push(0); --w.i; --w.j; }
+    else if (sc == 3) { atomicOr(err, 2u); return false; }
+    else w.st = (int)sc;
+  } else if (w.st == 1) {
+    wr.push(1);
+    w.st = (c & 4u) ? 0 : 1;
+    --w.j;
+  } else {
+    wr.push(2);
+    w.st = (c & 8u) ? 0 : 2;
+    --w.i;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void emit_done(const EmitArgs& a, uint32_t x, const ExtRec& r, RunWriter& wr,
+                                          uint64_t off, int64_t guard) {
+  if (guard <= 0) atomicOr(a.err, 4u);
+  wr.flush();
+  if (wr.overflow) atomicOr(a.err, 16u);
+  write_out(a.out + x, r, wr.nruns ? wr.first() : (uint32_t)off, wr.nruns, a.local ? 0u : bin_of(r.i_end, r.j_end));
+}
+
+// Thread per extension: each step reads the row origin and the code byte.
+__device__ void walk_thread(const EmitArgs& a, uint32_t pos) {
   const uint32_t x = a.exec_list[pos];
   const ExtRec r = a.rec[x];
-  const int32_t dend = r.i_end + r.j_end;
-  const uint32_t W = r.width;
-  const uint8_t* base = a.trace + (a.trace_off[pos] - a.trace_sub);
-  const int32_t* lo = reinterpret_cast<const int32_t*>(base + trace_lo_offset(W, dend));
+  Walk w;
+  walk_init(a, pos, r, w);
   const uint64_t off = a.cig_off[x];
   RunWriter wr;
   wr.init(a.cigar, off, cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub), (x & 1u) == 0u);
-  int32_t i = r.i_end, j = r.j_end, st = 0;
-  int64_t guard = 2 * (int64_t)dend + 4;
-  while ((i > 0 || j > 0) && --guard > 0) {
-    if (i < 0 || j < 0) { atomicOr(a.err, 1u); break; }
-    const int32_t d = i + j;
-    const int32_t u = i - lo[d];
-    if (u < 0 || (uint32_t)u >= W) { atomicOr(a.err, 1u); break; }
-    const uint32_t c = (base[(uint64_t)d * (W / 2) + (uint32_t)(u >> 1)] >> (4 * (u & 1))) & 15u;
+  int64_t guard = 2 * (int64_t)(r.i_end + r.j_end) + 4;
+  while ((w.i > 0 || w.j > 0) && --guard > 0) {
+    if (w.i < 0 || w.j < 0) { atomicOr(a.err, 1u); break; }
+    const int32_t d = w.i + w.j;
+    const int32_t u = w.i - w.lo[d];
+    if (u < 0 || (uint32_t)u >= w.W) { atomicOr(a.err, 1u); break; }
+    const uint32_t c = (w.base[(uint64_t)d * (w.W / 2) + (uint32_t)(u >> 1)] >> (4 * (u & 1))) & 15u;
     // The walk visits one row per step, going down in d: pull the row it will
     // reach PF anti-diagonals later (around where the path should be) and the
     // row origins further ahead into L2.  Addresses stay inside this
@@ -248,30 +294,118 @@ __global__ void k_emit_exec(EmitArgs a) {
     constexpr int32_t PF = 12;
     if (d >= PF) {
       const int32_t dp = d - PF;
-      int32_t up = i - PF / 2 - lo[dp];
-      up = up < 0 ? 0 : ((uint32_t)up >= W ? (int32_t)W - 1 : up);
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (uint64_t)dp * (W / 2) + (uint32_t)(up >> 1)));
-      if (d >= 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(lo + (d - 64)));
+      int32_t up = w.i - PF / 2 - w.lo[dp];
+      up = up < 0 ? 0 : ((uint32_t)up >= w.W ? (int32_t)w.W - 1 : up);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(w.base + (uint64_t)dp * (w.W / 2) + (uint32_t)(up >> 1)));
+      if (d >= 64) asm volatile("prefetch.global.L2 [%0];" ::"l"(w.lo + (d - 64)));
     }
-    if (st == 0) {
-      const uint32_t sc = c & 3u;
-      if (sc == 0) { wr.push(0); --i; --j; }
-      else if (sc == 3) { atomicOr(a.err, 2u); break; }
-      else st = (int)sc;
-    } else if (st == 1) {
-      wr.push(1);
-      st = (c & 4u) ? 0 : 1;
-      --j;
-    } else {
-      wr.push(2);
-      st = (c & 8u) ? 0 : 2;
-      --i;
-    }
+    if (!walk_step(w, c, wr, a.err)) break;
   }
-  if (guard <= 0) atomicOr(a.err, 4u);
-  wr.flush();
-  if (wr.overflow) atomicOr(a.err, 16u);
-  write_out(a.out + x, r, wr.nruns ? wr.first() : (uint32_t)off, wr.nruns, a.local ? 0u : bin_of(r.i_end, r.j_end));
+  emit_done(a, x, r, wr, off, guard);
+}
+
+// Warp per extension, for long walks.  From the walker's cell (i, d = i + j)
+// the next 32 anti-diagonals d, d-1, ..., d-31 can only be met in rows
+// i-t .. i of anti-diagonal d-t (each step lowers i by at most the drop in d),
+// at most 32 nibbles.  Lane t loads that row segment (5 aligned words) and the
+// row origin into shared memory; lane 0 then walks through them, and the warp
+// reloads once the walk leaves the 32 anti-diagonals.  A cell outside the
+// loaded segment (only possible on a corrupt trace) is read from global memory.
+constexpr int SEG_W = 5;
+
+__device__ void walk_warp(const EmitArgs& a, uint32_t pos, int lane, uint32_t (*seg)[SEG_W], int32_t* seg_off,
+                          int32_t* seg_lo) {
+  const uint32_t x = a.exec_list[pos];
+  const ExtRec r = a.rec[x];
+  Walk w;
+  walk_init(a, pos, r, w);
+  const uint64_t off = a.cig_off[x];
+  RunWriter wr;
+  wr.init(a.cigar, off, cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub), (x & 1u) == 0u);
+  int64_t guard = 2 * (int64_t)(r.i_end + r.j_end) + 4;
+  const uint32_t rowb = w.W / 2;
+  const uintptr_t blk_lo = reinterpret_cast<uintptr_t>(w.base);
+  const uintptr_t blk_hi = blk_lo + w.bytes;               // loads stay below this
+  bool run = true;
+  while (run) {
+    // anchor of this batch, broadcast from the walker
+    const int32_t iA = __shfl_sync(FULL, w.i, 0);
+    const int32_t dA = __shfl_sync(FULL, w.i + w.j, 0);
+    const int32_t dt = dA - lane;
+    if (dt >= 0) {
+      const int32_t lot = w.lo[dt];
+      int32_t u0 = iA - lane - lot;
+      u0 = u0 < 0 ? 0 : ((uint32_t)u0 >= w.W ? (int32_t)w.W - 1 : u0);
+      const uintptr_t row = blk_lo + (uint64_t)dt * rowb;
+      uintptr_t a0 = (row + (uint32_t)(u0 >> 1)) & ~uintptr_t(3);
+      const uintptr_t amax = (blk_hi - 4 * SEG_W) & ~uintptr_t(3);
+      if (a0 > amax) a0 = amax;
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(a0);
+#pragma unroll
+      for (int k = 0; k < SEG_W; ++k) seg[lane][k] = src[k];
+      seg_off[lane] = (int32_t)(a0 - row);                  // byte offset of the segment in its row
+      seg_lo[lane] = lot;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (;;) {
+        if (!(w.i > 0 || w.j > 0)) { run = false; break; }
+        if (--guard <= 0) { run = false; break; }
+        if (w.i < 0 || w.j < 0) { atomicOr(a.err, 1u); run = false; break; }
+        const int32_t d = w.i + w.j, t = dA - d;
+        if (t >= 32) break;                                 // left the loaded anti-diagonals
+        const int32_t u = w.i - seg_lo[t];
+        if (u < 0 || (uint32_t)u >= w.W) { atomicOr(a.err, 1u); run = false; break; }
+        const int32_t b = (u >> 1) - seg_off[t];
+        uint32_t byte;
+        if (b >= 0 && b < 4 * SEG_W) byte = (seg[t][b >> 2] >> (8 * (b & 3))) & 0xffu;
+        else byte = w.base[(uint64_t)d * rowb + (uint32_t)(u >> 1)];
+        const uint32_t c = (byte >> (4 * (u & 1))) & 15u;
+        if (!walk_step(w, c, wr, a.err)) { run = false; break; }
+      }
+    }
+    run = __shfl_sync(FULL, run, 0);
+    __syncwarp();
+  }
+  if (lane == 0) emit_done(a, x, r, wr, off, guard);
+}
+
+// ---- packing the CIGAR runs for a host copy ----
+// The arena holds one slot per extension sized by cigar_cap; most slots are
+// partly used.  For a copy to the host the runs are packed in extension order.
+__global__ void k_cig_lens(const fz_result* out, uint32_t n, uint64_t* lens) {
+  const uint32_t x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x < n) lens[x] = out[x].cigar_len;
+}
+
+// warp per extension: copy its runs to their packed offset and repoint the record
+__global__ void k_cig_pack(fz_result* out, uint32_t n, const uint64_t* poff, const uint32_t* src, uint32_t* dst) {
+  const uint32_t x = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (x >= n) return;
+  const uint32_t len = out[x].cigar_len, from = out[x].cigar_off;
+  const uint64_t to = poff[x];
+  for (uint32_t k = lane; k < len; k += 32) dst[to + k] = src[(uint64_t)from + k];
+  __syncwarp();
+  if (lane == 0) out[x].cigar_off = (uint32_t)to;
+}
+
+// Blocks [0, long_blocks): one warp per item of [exec_begin, exec_split), the
+// long walks (the executor list holds the largest bins first).  The other
+// blocks: one thread per item of [exec_split, exec_end).
+constexpr int EMIT_T = 128;
+
+__global__ void __launch_bounds__(EMIT_T) k_emit_exec(EmitArgs a) {
+  __shared__ uint32_t seg[EMIT_T / 32][32][SEG_W];
+  __shared__ int32_t seg_off[EMIT_T / 32][32], seg_lo[EMIT_T / 32][32];
+  if (blockIdx.x < a.long_blocks) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t nw = a.long_blocks * (EMIT_T / 32);
+    for (uint32_t pos = a.exec_begin + blockIdx.x * (EMIT_T / 32) + warp; pos < a.exec_split; pos += nw)
+      walk_warp(a, pos, lane, seg[warp], seg_off[warp], seg_lo[warp]);
+    return;
+  }
+  const uint32_t pos = a.exec_split + (blockIdx.x - a.long_blocks) * EMIT_T + threadIdx.x;
+  if (pos < a.exec_end) walk_thread(a, pos);
 }
 
 }  // namespace
@@ -309,10 +443,26 @@ cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_emit_exec(const EmitArgs& a, cudaStream_t st) {
-  const uint32_t n = a.exec_end - a.exec_begin;
-  const uint32_t g = (n + 127) / 128;
-  if (g) k_emit_exec<<<g, 128, 0, st>>>(a);
+cudaError_t launch_cig_lens(const fz_result* out, uint32_t n, uint64_t* lens, cudaStream_t st) {
+  if (n) k_cig_lens<<<(n + TB - 1) / TB, TB, 0, st>>>(out, n, lens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cig_pack(fz_result* out, uint32_t n, const uint64_t* poff, const uint32_t* src, uint32_t* dst,
+                            cudaStream_t st) {
+  const uint64_t threads = (uint64_t)n * 32;
+  if (n) k_cig_pack<<<(uint32_t)((threads + TB - 1) / TB), TB, 0, st>>>(out, n, poff, src, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_emit_exec(EmitArgs a, uint32_t long_end, int sms, cudaStream_t st) {
+  a.exec_split = long_end < a.exec_begin ? a.exec_begin : (long_end > a.exec_end ? a.exec_end : long_end);
+  const uint32_t n_long = a.exec_split - a.exec_begin, n_short = a.exec_end - a.exec_split;
+  const uint32_t warps = EMIT_T / 32;
+  const uint32_t cap = (uint32_t)(sms > 0 ? sms : 1) * 16;  // warp blocks: at most 16 per SM
+  a.long_blocks = n_long ? std::min<uint32_t>((n_long + warps - 1) / warps, cap) : 0u;
+  const uint32_t g = a.long_blocks + (n_short + EMIT_T - 1) / EMIT_T;
+  if (g) k_emit_exec<<<g, EMIT_T, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -132,10 +132,13 @@ fz_status fz_extend_batch(fz_ctx* ctx, const uint8_t* d_target2, uint64_t t_len,
  * Same computation from HOST buffers: copies the packed sequences and seeds to
  * context-owned device memory, runs fz_extend_batch, copies the results to
  * h_out (2*n_seeds) and the CIGAR runs to h_cigar, and synchronises the
- * stream before returning.  h_cigar may be NULL when cigar_cap is 0.  If the
- * CIGAR needs more than cigar_cap runs, the results are still written,
- * *cigar_used holds the size needed and FZ_ERR_ARG is returned.  Host buffers
- * may be pageable; page-locked buffers copy faster.
+ * stream before returning.  The runs are packed: extension x's runs are
+ * h_cigar[h_out[x].cigar_off .. + h_out[x].cigar_len), extensions in order, and
+ * *cigar_used is the number of runs written (the device entry's arena instead
+ * keeps one worst-case slot per extension).  h_cigar may be NULL when
+ * cigar_cap is 0.  If the CIGAR needs more than cigar_cap runs, the results
+ * are still written, *cigar_used holds the size needed and FZ_ERR_ARG is
+ * returned.  Host buffers may be pageable; page-locked buffers copy faster.
  */
 fz_status fz_extend_batch_host(fz_ctx* ctx, const uint8_t* h_target2, uint64_t t_len,
                                const uint8_t* h_query2, uint64_t q_len, const fz_seed* h_seeds,
