@@ -51,6 +51,9 @@ struct Counters {
   uint32_t err;
   uint32_t bin_count[8];
   uint32_t bin_cursor[8];
+  uint32_t ckpt_used;          // window checkpoint slots taken (may exceed the pool)
+  uint32_t pad_;
+  uint64_t seg_total;          // executor segments
 };
 
 constexpr uint64_t TRACE_CAP_DEFAULT = 1ull << 30;   // smallest executor arena cap before chunking
@@ -68,12 +71,16 @@ struct fz_ctx {
   std::string err;
   DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, retry_list, counters;
   DevBuf cigar, cigar_packed, trace, scratch, spill;
+  DevBuf ckpt, seg_cnt, seg;         // window checkpoints, executor segments
   DevBuf in_t, in_q, in_seeds, out_res;
   Counters* h_cnt = nullptr;         // pinned
   cudaStream_t last_stream = nullptr;
   fz_stats stats{};
   bool have_batch = false;
   uint64_t trace_cap = TRACE_CAP_DEFAULT;
+  uint64_t ckpt_slot_cap = 0;        // most checkpoint slots the pool may hold (0: none written)
+  uint64_t ckpt_demand = 0;          // slots the last batch asked for (the pool grows to it)
+  int32_t ckpt_every = 256;          // checkpoint interval in anti-diagonals (a power of two)
   int grid_fast[2] = {0, 0}, grid_fast_trace[2] = {0, 0}, grid_wide = 0, grid_local = 0;
   size_t local_smem = 0;
   bool local_use_smem = true;
@@ -122,6 +129,7 @@ fz_status ensure_batch_buffers(fz_ctx* ctx, uint32_t n_ext) {
   CU(ctx->scan_tmp.ensure((size_t)scan_tmp_elems((uint32_t)n) * 8));
   CU(ctx->wide_list.ensure(n * 4));
   CU(ctx->retry_list.ensure(n * 4));
+  CU(ctx->seg_cnt.ensure(n * 8));
   CU(ctx->counters.ensure(sizeof(Counters)));
   if (ctx->mode == FZ_EXTEND) {
     const uint64_t per = wide_scratch_elems(ctx->p.max_len) * 4;
@@ -186,6 +194,17 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   wa.err = &dc->err;
   wa.scratch = ctx->scratch.as<int32_t>();
   wa.scratch_stride = wide_scratch_elems(ctx->p.max_len);
+  // window checkpoints: up to 4 per extension, within the pool cap
+  if (ctx->ckpt_slot_cap && ctx->fast_ok) {
+    const uint64_t slots = std::min<uint64_t>(std::max<uint64_t>(4ull * n_ext + 64, ctx->ckpt_demand),
+                                              ctx->ckpt_slot_cap);
+    CU(ctx->ckpt.ensure(slots * CK_SLOT_WORDS * sizeof(int32_t)));
+    wa.ckpt = ctx->ckpt.as<int32_t>();
+    wa.ckpt_cap = (uint32_t)std::min<uint64_t>(ctx->ckpt.bytes / (CK_SLOT_WORDS * sizeof(int32_t)), 0xffffff00ull);
+    wa.ckpt_used = &dc->ckpt_used;
+    wa.ckpt_every = ctx->ckpt_every;
+    wa.ckpt_recent = ctx->ckpt_every;
+  }
 
   // 1. inspector
   mark(ctx, 0, st);
@@ -205,6 +224,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
     b.counter = &dc->work[1];
     b.ovf_list = ctx->wide_list.as<uint32_t>();
     b.ovf_count = &dc->wide_count;
+    b.resume = 1;                        // continue from the overflow checkpoint
     CU(launch_inspect_fast(1, ctx->p, b, ctx->grid_fast[1], st));
     mark(ctx, 1, st);
     wa.list = ctx->wide_list.as<uint32_t>();
@@ -246,7 +266,10 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   CU(launch_scatter(pa, st));
   CU(launch_scan_u64(pa.cig_cap, n_ext, ctx->scan_tmp.as<uint64_t>(), &dc->cig_total, st));
   CU(launch_scan_u64(pa.trace_sz, n_ext, ctx->scan_tmp.as<uint64_t>(), &dc->trace_total, st));
-  ctx->launches += 3 + 6;
+  // executor segments: count per executor item, then their offsets
+  CU(launch_seg_count(pa.rec, pa.exec_list, n_ext, &dc->bin_cursor[0], wa.ckpt, ctx->seg_cnt.as<uint64_t>(), st));
+  CU(launch_scan_u64(ctx->seg_cnt.as<uint64_t>(), n_ext, ctx->scan_tmp.as<uint64_t>(), &dc->seg_total, st));
+  ctx->launches += 3 + 6 + 4;
   mark(ctx, 3, st);
   CU(cudaMemcpyAsync(ctx->h_cnt, dc, sizeof(Counters), cudaMemcpyDeviceToHost, st));
   CU(cudaStreamSynchronize(st));
@@ -260,18 +283,30 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   CU(ctx->cigar.ensure(std::max<uint64_t>(hc.cig_total, 1) * 4));
   ctx->stats.trace_bytes = hc.trace_total;
   ctx->stats.cigar_runs = hc.cig_total;
+  const uint64_t n_seg = hc.seg_total;
+  if (wa.ckpt && hc.ckpt_used > wa.ckpt_cap)   // checkpoints were dropped: a larger pool next batch
+    ctx->ckpt_demand = std::max<uint64_t>(ctx->ckpt_demand, (uint64_t)hc.ckpt_used + hc.ckpt_used / 4);
+  if (n_exec) {
+    CU(ctx->seg.ensure(std::max<uint64_t>(n_seg, 1) * sizeof(uint4)));
+    CU(launch_seg_fill(pa.rec, pa.exec_list, n_ext, &dc->bin_cursor[0], wa.ckpt, ctx->seg_cnt.as<uint64_t>(),
+                       ctx->seg.as<uint4>(), st));
+    ctx->launches += 1;
+  }
 
   // 3. executor + traceback, chunked by the arena cap
   std::vector<std::pair<uint32_t, uint32_t>> chunks;
-  std::vector<uint64_t> toff;
+  std::vector<uint64_t> toff, soff;          // per position: trace offset, first segment
   if (n_exec) {
     if (hc.trace_total <= ctx->trace_cap) {
       chunks.push_back({0u, n_exec});
       CU(ctx->trace.ensure(std::max<uint64_t>(hc.trace_total, 16)));
     } else {
       toff.resize(n_exec + 1);
+      soff.resize(n_exec + 1);
       CU(cudaMemcpy(toff.data(), ctx->trace_sz.p, (size_t)n_exec * 8, cudaMemcpyDeviceToHost));
+      CU(cudaMemcpy(soff.data(), ctx->seg_cnt.p, (size_t)n_exec * 8, cudaMemcpyDeviceToHost));
       toff[n_exec] = hc.trace_total;
+      soff[n_exec] = n_seg;
       uint32_t a = 0;
       while (a < n_exec) {
         uint32_t b = a + 1;
@@ -303,12 +338,14 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   bool first_chunk = true;
   for (auto& c : chunks) {
     const uint64_t sub = toff.empty() ? 0 : toff[c.first];
+    const uint64_t s0 = soff.empty() ? 0 : soff[c.first], s1 = soff.empty() ? n_seg : soff[c.second];
     WorkArgs we = wa;
-    we.list = ctx->exec_list.as<uint32_t>() + c.first;
-    we.n_work = c.second - c.first;
+    we.list = ctx->exec_list.as<uint32_t>();    // segments name executor positions
+    we.seg = ctx->seg.as<uint4>() + s0;
+    we.n_work = (uint32_t)(s1 - s0);
     we.n_work_dev = nullptr;
     we.trace = ctx->trace.as<uint8_t>();
-    we.trace_off = ctx->trace_sz.as<uint64_t>() + c.first;
+    we.trace_off = ctx->trace_sz.as<uint64_t>();
     we.trace_sub = sub;
     if (!first_chunk) CU(cudaMemsetAsync(&dc->work[3], 0, 3 * sizeof(uint32_t), st));
     first_chunk = false;
@@ -428,6 +465,25 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
   }
   const char* cap = getenv("FZ_TRACE_CAP");
   if (cap) ctx->trace_cap = std::max<uint64_t>(strtoull(cap, nullptr, 10), 4096);
+  {
+    // checkpoint pool cap: 10% of the device memory free now
+    size_t fr = 0, tot = 0;
+    if (cudaMemGetInfo(&fr, &tot) == cudaSuccess)
+      ctx->ckpt_slot_cap = (uint64_t)(fr * 0.1) / (CK_SLOT_WORDS * sizeof(int32_t));
+    (void)cudaGetLastError();
+  }
+  const char* cks = getenv("FZ_CKPT_SLOTS");
+  if (cks) ctx->ckpt_slot_cap = strtoull(cks, nullptr, 10);
+  // checkpoint interval: 256 anti-diagonals, longer for long windows so that
+  // an extension holds at most ~64 checkpoints
+  while (ctx->ckpt_every < (1 << 20) && (int64_t)ctx->ckpt_every * 64 < 2 * (int64_t)max_len) ctx->ckpt_every <<= 1;
+  const char* cke = getenv("FZ_CKPT_EVERY");
+  if (cke) {
+    const long v = strtol(cke, nullptr, 10);
+    int32_t e = 32;
+    while (e < v && e < (1 << 20)) e <<= 1;   // a power of two, at least 32
+    ctx->ckpt_every = e;
+  }
   *out = ctx;
   return FZ_OK;
 }

@@ -249,14 +249,17 @@ struct Relay {
   uint8_t t[32 * KS], q[32 * KS];
 };
 
-// Change the window from kold to knew active slots per lane, keeping its base
+// Changing the window from kold to knew active slots per lane keeps its base
 // row b: row b+u moves from lane u/kold, slot u%kold to lane u/knew, slot
-// u%knew.  Rows that did not exist before (growing) are dead; their target
-// bases and query bases (column d - row) are read from memory.  When shrinking
-// the caller guarantees the dropped rows are dead.
+// u%knew, through the per-warp shared buffer.  relay_store writes the rows
+// out; relay_load reads rows 0 .. rows_old-1 back (rows that did not exist
+// before are dead; their target bases and query bases, column d - row, are
+// read from memory).  When shrinking the caller guarantees the dropped rows
+// are dead.  A checkpoint restore stages its rows with ck_stage and then
+// takes the same relay_load.
 template <int KS>
-__device__ __forceinline__ void relayout(LaneState<KS>& L, int kold, int knew, int32_t b, int32_t d, int lane,
-                                      Relay<KS>* rb, const Params& p, const Window& w, const uint32_t* s_mrow) {
+__device__ __forceinline__ void relay_store(const LaneState<KS>& L, int kold, int lane, Relay<KS>* rb,
+                                            const uint32_t* s_mrow) {
 #pragma unroll
   for (int r = 0; r < KS; ++r) {
     if (r < kold) {
@@ -273,7 +276,12 @@ __device__ __forceinline__ void relayout(LaneState<KS>& L, int kold, int knew, i
     }
   }
   __syncwarp();
-  const int rows_old = 32 * kold;
+}
+
+template <int KS>
+__device__ __forceinline__ void relay_load(LaneState<KS>& L, int rows_old, int knew, int32_t b, int32_t d,
+                                           int lane, Relay<KS>* rb, const Params& p, const Window& w,
+                                           const uint32_t* s_mrow) {
   const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + (int64_t)lane * knew);
   const uint32_t qw = fetch16(p.q2, p.q_len, w.qg0, w.dir, (int64_t)d - b - (int64_t)lane * knew - 15);
   uint32_t sel[KS];
@@ -299,6 +307,129 @@ __device__ __forceinline__ void relayout(LaneState<KS>& L, int kold, int knew, i
 #pragma unroll
   for (int k = 0; k < KS / 2; ++k) L.QP[k] = sel[2 * k] | (sel[2 * k + 1] << 16);
   __syncwarp();
+}
+
+// ---- window checkpoints (layout in fz_dev.cuh) ----
+
+// Sweep state after anti-diagonal d kept in a checkpoint header.
+struct CkScalars {
+  int32_t b, d, best, bi, bj, d_last;
+};
+
+// Writes the state after anti-diagonal d (all KS slots of every lane) to a new
+// slot linked to `head`; returns the new head (slot + 1), or `head` unchanged
+// when the pool is full.  cnt: this lane's live cells so far (lane 0 adds
+// 2^32 cnt_hi).
+template <int KS>
+__device__ __forceinline__ uint32_t ck_write(const WorkArgs& wa, const LaneState<KS>& L, int lane, uint32_t head,
+                                             const CkScalars& cs, uint32_t cnt, uint32_t cnt_hi,
+                                             const int32_t* sT) {
+  uint32_t slot = 0;
+  if (lane == 0) slot = atomicAdd(wa.ckpt_used, 1u);
+  slot = __shfl_sync(FULL, slot, 0);
+  if (slot >= wa.ckpt_cap) return head;
+  int32_t* c = wa.ckpt + (uint64_t)slot * CK_SLOT_WORDS;
+#pragma unroll
+  for (int r = 0; r < KS; ++r) {
+    c[CK_HDR + r * 32 + lane] = L.H[r];
+    c[CK_HDR + CK_WIN_MAX + r * 32 + lane] = L.HP[r];
+    c[CK_HDR + 2 * CK_WIN_MAX + r * 32 + lane] = L.I[r];
+    c[CK_HDR + 3 * CK_WIN_MAX + r * 32 + lane] = L.D[r];
+  }
+  c[CK_T + lane] = sT[lane];
+  c[CK_CNT + lane] = (int32_t)cnt;
+  if (lane == 0) {
+    c[CK_T + 32] = sT[32];
+    c[CK_D] = cs.d; c[CK_B] = cs.b; c[CK_K] = KS; c[CK_BEST] = cs.best; c[CK_BI] = cs.bi; c[CK_BJ] = cs.bj;
+    c[CK_DLAST] = cs.d_last; c[CK_FLAGS] = 0; c[CK_PREV] = (int32_t)head;
+    c[CK_CNT_HI] = (int32_t)cnt_hi;
+  }
+  return slot + 1;
+}
+
+// Loads a checkpoint into a KS-row-per-lane window (KS >= the writer's K; rows
+// the writer did not hold are dead) and rebuilds each row's substitution row
+// and query selector from the sequences: row b + u has target base b + u and
+// sits at column d - (b + u).
+template <int KS>
+__device__ __forceinline__ void ck_load(LaneState<KS>& L, const int32_t* c, int lane, const Params& p,
+                                        const Window& w, const uint32_t* s_mrow, CkScalars& cs) {
+  cs.b = c[CK_B]; cs.d = c[CK_D]; cs.best = c[CK_BEST]; cs.bi = c[CK_BI]; cs.bj = c[CK_BJ];
+  cs.d_last = c[CK_DLAST];
+  const int ks = c[CK_K];
+  const int rows_src = 32 * ks;
+  const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)cs.b + (int64_t)lane * KS);
+  const uint32_t qw = fetch16(p.q2, p.q_len, w.qg0, w.dir, (int64_t)cs.d - cs.b - (int64_t)lane * KS - 15);
+  uint32_t sel[KS];
+#pragma unroll
+  for (int r = 0; r < KS; ++r) {
+    const int u = lane * KS + r;
+    L.H[r] = NEG; L.HP[r] = NEG; L.I[r] = NEG; L.D[r] = NEG;
+    if (u < rows_src) {
+      const int sl = u / ks, sr = u - sl * ks;
+      const int pos = sr * 32 + sl;
+      L.H[r] = c[CK_HDR + pos];
+      L.HP[r] = c[CK_HDR + CK_WIN_MAX + pos];
+      L.I[r] = c[CK_HDR + 2 * CK_WIN_MAX + pos];
+      L.D[r] = c[CK_HDR + 3 * CK_WIN_MAX + pos];
+    }
+    L.MR[r] = s_mrow[(tw >> (2 * r)) & 3u];
+    sel[r] = 0x4440u | ((qw >> (2 * (15 - r))) & 3u);
+  }
+#pragma unroll
+  for (int k = 0; k < KS / 2; ++k) L.QP[k] = sel[2 * k] | (sel[2 * k + 1] << 16);
+}
+
+// Lanes whose rows hold a live cell at d (from h) and at d - 1 (from the
+// previous anti-diagonal's h, kept offset by o + e - 128: dead is near NEG).
+template <int KS>
+__device__ __forceinline__ void ck_live_lanes(const LaneState<KS>& L, uint32_t& now, uint32_t& prev) {
+  bool a = false, q = false;
+#pragma unroll
+  for (int r = 0; r < KS; ++r) {
+    a = a || L.H[r] > NEG / 2;
+    q = q || L.HP[r] > NEG / 2;
+  }
+  now = __ballot_sync(FULL, a);
+  prev = __ballot_sync(FULL, q);
+}
+
+// Stages a checkpoint's rows in the relay buffer for relay_load, with each
+// row's target base and query base (column d - row), and returns the live row
+// bounds at d (from h) and d - 1 (from the previous anti-diagonal's h, kept
+// offset by o + e - 128: dead is near NEG) as absolute rows, or NOROW values.
+template <int KS>
+__device__ __forceinline__ int ck_stage(Relay<KS>* rb, const int32_t* c, int lane, const Params& p, const Window& w,
+                                        int32_t& hi_c, int32_t& lo_c, int32_t& hi_p, int32_t& lo_p) {
+  constexpr int32_t NOROW_HI = -0x3fffffff, NOROW_LO = 0x3fffffff;
+  const int32_t b = c[CK_B], d = c[CK_D];
+  const int ks = c[CK_K];
+  const int rows = imin(32 * ks, 32 * KS);
+  const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + 16 * lane);
+  const uint32_t qw = fetch16(p.q2, p.q_len, w.qg0, w.dir, (int64_t)d - b - 16 * lane - 15);
+  int32_t hc = NOROW_HI, lc = NOROW_LO, hp = NOROW_HI, lp = NOROW_LO;
+#pragma unroll 4
+  for (int k = 0; k < 16; ++k) {
+    const int u = 16 * lane + k;
+    if (u < rows) {
+      const int sl = u / ks, pos = (u - sl * ks) * 32 + sl;
+      const int32_t h = c[CK_HDR + pos], hq = c[CK_HDR + CK_WIN_MAX + pos];
+      rb->H[u] = h;
+      rb->HP[u] = hq;
+      rb->I[u] = c[CK_HDR + 2 * CK_WIN_MAX + pos];
+      rb->D[u] = c[CK_HDR + 3 * CK_WIN_MAX + pos];
+      rb->t[u] = (uint8_t)((tw >> (2 * k)) & 3u);
+      rb->q[u] = (uint8_t)((qw >> (2 * (15 - k))) & 3u);
+      if (h > NEG / 2) { hc = imax(hc, b + u); lc = imin(lc, b + u); }
+      if (hq > NEG / 2) { hp = imax(hp, b + u); lp = imin(lp, b + u); }
+    }
+  }
+  hi_c = __reduce_max_sync(FULL, hc);
+  lo_c = __reduce_min_sync(FULL, lc);
+  hi_p = __reduce_max_sync(FULL, hp);
+  lo_p = __reduce_min_sync(FULL, lp);
+  __syncwarp();
+  return rows;
 }
 
 // Runs one step with ka active slots (ka even, 4 <= ka <= KS) and stores the
@@ -337,7 +468,7 @@ __device__ __forceinline__ int32_t step_any(int ka, LaneState<KS>& L, const Step
 // short and spend most steps on a narrow band); without it the window stays at
 // KS rows per lane (the inspector: one step variant keeps its loop small).
 template <int KS, bool TRACE, bool ADAPT>
-__device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint32_t idx, int lane,
+__device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint4 sg, int lane,
                         int32_t* sT, uint8_t* tile, const uint32_t* s_mrow, const int32_t* s_sub, Relay<KS>* rb) {
   static_assert(KS % 2 == 0 && KS <= 16, "one 16-base fetch per lane");
   constexpr int32_t WMAX = 32 * KS;          // trace row width: the widest window
@@ -356,10 +487,13 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
   uint8_t* tbase = nullptr;
   int32_t* lo_arr = nullptr;
   if (TRACE) {
-    d_stop = R->i_end + R->j_end;
-    tbase = wa.trace + (wa.trace_off[idx] - wa.trace_sub);
-    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(WMAX, d_stop));
-    if (lane == 0) lo_arr[0] = 0;
+    // segment sg: replay from anti-diagonal sg.w (the origin, or checkpoint
+    // sg.y - 1) to sg.z; the rows are laid out for the whole extension
+    const int32_t dstar = R->i_end + R->j_end;
+    d_stop = (int32_t)sg.z;
+    tbase = wa.trace + (wa.trace_off[sg.x] - wa.trace_sub);
+    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(WMAX, dstar));
+    if (lane == 0 && sg.y == 0u) lo_arr[0] = 0;
   }
 
   // The window starts with 4 rows per lane (128 rows) and is re-laid out as
@@ -393,6 +527,22 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
   uint32_t cnt = lane == 0 ? 1u : 0u;
   bool overflow = false;
   int cool = 0;
+  // a segment that starts at a checkpoint: its rows go to the relay buffer and
+  // the first step's window sizing loads them (staged)
+  bool staged = false;
+  int rows_staged = 0;
+  if (TRACE && ADAPT && sg.y != 0u) {
+    const int32_t* c = wa.ckpt + (uint64_t)(sg.y - 1u) * CK_SLOT_WORDS;
+    b = c[CK_B]; d = c[CK_D]; best = c[CK_BEST]; d_last = c[CK_DLAST];
+    T = threshold(best, p.ydrop);
+    rows_staged = ck_stage<KS>(rb, c, lane, p, w, hi_c, lo_c, hi_p, lo_p);
+    live = hi_c != NOROW_HI;
+    live_prev = hi_p != NOROW_HI;
+    rowb_alive = lo_c == b;
+    staged = true;
+    cool = 0;
+    res_init(qr, p.q2, p.q_len, w.qg0, w.dir, (int64_t)d + 1 - b);
+  }
 
   for (;;) {
     const int32_t dn = d + 1;
@@ -410,8 +560,10 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
       } else if (cool <= 0 && need + 96 <= 32 * (kact - 2)) {
         kt = imax(4, (((need + 64 + 31) >> 5) + 1) & ~1);
       }
-      if (kt != kact) {
-        relayout<KS>(L, kact, kt, b, d, lane, rb, p, w, s_mrow);
+      if (kt != kact || staged) {
+        if (!staged) relay_store<KS>(L, kact, lane, rb, s_mrow);
+        relay_load<KS>(L, staged ? rows_staged : 32 * kact, kt, b, d, lane, rb, p, w, s_mrow);
+        staged = false;
         kact = kt;
         res_init(tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + 32 * kact);
         cool = 32;
@@ -482,7 +634,7 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
 
   if (TRACE) {
-    if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)d_stop * (unsigned long long)WMAX);
+    if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)(d_stop - (int32_t)sg.w) * (unsigned long long)WMAX);
     return;
   }
   if (overflow) {
@@ -510,7 +662,7 @@ __device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint3
     ExtRec o;
     o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
     o.live = tot; o.path = path; o.flags = flags; o.npath = npath;
-    o.m = m; o.n = n; o.width = width; o.pad = 0;
+    o.m = m; o.n = n; o.width = width; o.ckpt = 0;
     *R = o;
     atomicAdd(wa.live_total, (unsigned long long)tot);
   }
@@ -540,6 +692,7 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
     return;
   }
   const int32_t m = w.m, n = w.n, oe = p.oe, mn = w.m + w.n;
+  uint32_t cnt_hi_carry = 0;   // high word of a live count carried from a checkpoint
   LaneState<KS> L;
   {
     const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * KS);
@@ -552,31 +705,52 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
     for (int k = 0; k < KS / 2; ++k) L.QP[k] = 0x44404440u;
     if (lane == 0) L.H[0] = -oe;                       // origin: S(0,0) = 0
   }
+  int32_t b = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
+  bool live_prev = true, rowb_alive = true, top = false, top_prev = false;
+  uint32_t cnt = lane == 0 ? 1u : 0u;
+  // resume (the widest window, after an overflow): continue from the newest checkpoint
+  uint32_t head = KS >= 16 && wa.resume && wa.ckpt ? R->ckpt : 0u;
+  if constexpr (KS >= 16) if (head) {
+    const int32_t* c = wa.ckpt + (uint64_t)(head - 1) * CK_SLOT_WORDS;
+    CkScalars cs;
+    ck_load<KS>(L, c, lane, p, w, s_mrow, cs);
+    b = cs.b; d = cs.d; best = cs.best; bi = cs.bi; bj = cs.bj; d_last = cs.d_last;
+    cnt = (uint32_t)c[CK_CNT + lane];
+    if (lane == 0) cnt_hi_carry = (uint32_t)c[CK_CNT_HI];
+    sT[lane] = c[CK_T + lane];
+    if (lane == 0) sT[32] = c[CK_T + 32];
+    uint32_t now, prev;
+    ck_live_lanes<KS>(L, now, prev);
+    live_prev = now != 0u;                          // the loop's live_prev is the live flag of d
+    rowb_alive = __shfl_sync(FULL, L.H[0] > NEG / 2 ? 1 : 0, 0) != 0;
+    top = (now >> 31) != 0u;
+    top_prev = (prev >> 31) != 0u;                  // conservative: may only add an overflow
+    __syncwarp();
+  }
   Reservoir qr, tr;
-  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);        // query columns entering at row b
-  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);      // target rows entering at the window top
+  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, (int64_t)d + 1 - b);   // query columns entering at row b
+  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + WIN);     // target rows entering at the window top
 
   StepIn in;
   in.oe = oe;
   in.ne = -p.e;
   in.c1 = oe - 128;
   in.one = p.one;
-  in.Th = threshold(0, p.ydrop) - oe;
-  int32_t b = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
-  bool live_prev = true, rowb_alive = true, top = false, top_prev = false;
-  uint32_t cnt = lane == 0 ? 1u : 0u;
+  in.Th = threshold(best, p.ydrop) - oe;
   bool overflow = false;
   uint64_t no_codes = 0;   // direction codes are the executor's
+  const uint32_t ck_mask = wa.ckpt ? (uint32_t)wa.ckpt_every - 1u : 0xffffffffu;
 
+  // The step loop leaves at the end of the sweep, on an overflow, and at every
+  // checkpoint boundary; the checkpoint writes stay out of the step loop.
+  int why = 0;   // 0: checkpoint boundary, 1: overflow, 2: the sweep ended
+  for (;;) {
   for (;;) {
     const int32_t dn = d + 1;
-    if (dn > mn) break;
+    if (dn > mn) { why = 2; break; }
     const bool shift = !rowb_alive;
     const int32_t bn = b + (shift ? 1 : 0);
-    if (!shift && (top || top_prev)) {
-      overflow = true;   // the live band may grow past the window top
-      break;
-    }
+    if (!shift && (top || top_prev)) { why = 1; break; }   // the live band may grow past the window top
     const bool edge = bn + WIN - 1 > m || bn < dn - n;
     int32_t lm;
     if (!shift) {
@@ -623,11 +797,29 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
     top = (bits >> 31) != 0u;
     b = bn;
     d = dn;
-    if (!live && !live_prev) break;
+    if (!live && !live_prev) { why = 2; break; }
     live_prev = live;
+    if (((uint32_t)d & ck_mask) == 0u) { why = 0; break; }
+  }
+    if (why == 2) break;
+    if (why == 1) {
+      overflow = true;
+      if (wa.ckpt) {     // the wider window resumes here
+        const CkScalars cs{b, d, best, bi, bj, d_last};
+        head = ck_write<KS>(wa, L, lane, head, cs, cnt, cnt_hi_carry, sT);
+      }
+      break;
+    }
+    // periodic checkpoint while the best cell is recent: executor segments
+    // start from these
+    if (d - (bi + bj) <= wa.ckpt_recent) {
+      const CkScalars cs{b, d, best, bi, bj, d_last};
+      head = ck_write<KS>(wa, L, lane, head, cs, cnt, cnt_hi_carry, sT);
+    }
   }
 
   uint64_t tot = cnt;
+  if (lane == 0) tot += (uint64_t)cnt_hi_carry << 32;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
   if (overflow) {
@@ -636,6 +828,7 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
       z.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE;
       z.m = m;
       z.n = n;
+      z.ckpt = head;
       *R = z;
       const uint32_t slot = atomicAdd(wa.ovf_count, 1u);   // retried with a wider window
       wa.ovf_list[slot] = ext;
@@ -655,7 +848,7 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
     ExtRec o;
     o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
     o.live = tot; o.path = path; o.flags = flags; o.npath = npath;
-    o.m = m; o.n = n; o.width = width; o.pad = 0;
+    o.m = m; o.n = n; o.width = width; o.ckpt = head;
     *R = o;
     atomicAdd(wa.live_total, (unsigned long long)tot);
   }
@@ -679,17 +872,18 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_extend(Params p, WorkArgs 
     idx = __shfl_sync(FULL, idx, 0);
     const uint32_t nw = wa.n_work_dev ? *wa.n_work_dev : wa.n_work;
     if (idx >= nw) break;
-    uint32_t ext = wa.list ? wa.list[idx] : idx;
     if (TRACE) {
-      // executor: only the extensions this window size inspected
+      // executor segment; only the extensions this window size inspected
+      const uint4 sg = wa.seg[idx];
+      const uint32_t ext = wa.list[sg.x];
       const ExtRec& r = wa.rec[ext];
       if ((r.flags & FZ_FLAG_WIDE) || r.width != (uint32_t)(32 * K)) continue;
-    }
-    if (TRACE)
-      run_ext<K, true, true>(p, wa, ext, idx, lane, s_T[warp], s_tile[warp], s_mrow, s_sub,
+      run_ext<K, true, true>(p, wa, ext, sg, lane, s_T[warp], s_tile[warp], s_mrow, s_sub,
                              reinterpret_cast<Relay<K>*>(&s_relay[warp]));
-    else
+    } else {
+      const uint32_t ext = wa.list ? wa.list[idx] : idx;
       run_inspect<K>(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow, s_sub);
+    }
   }
 }
 

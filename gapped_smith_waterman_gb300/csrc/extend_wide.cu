@@ -145,7 +145,7 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
     ExtRec o;
     o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
     o.live = tot; o.path = 0; o.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE; o.npath = 0;
-    o.m = m; o.n = n; o.width = (uint32_t)((wbest + 31) & ~31); o.pad = 0;
+    o.m = m; o.n = n; o.width = (uint32_t)((wbest + 31) & ~31); o.ckpt = 0;
     *R = o;
     atomicAdd(wa.live_total, (unsigned long long)tot);
   }
@@ -166,9 +166,15 @@ __global__ void __launch_bounds__(WW * 32) k_wide(Params p, WorkArgs wa) {
     idx = __shfl_sync(FULL, idx, 0);
     const uint32_t nw = TRACE ? wa.n_work : *wa.wide_count;
     if (idx >= nw) break;
-    const uint32_t ext = wa.list[idx];
-    if (TRACE && !(wa.rec[ext].flags & FZ_FLAG_WIDE)) continue;
-    wide_ext<TRACE>(p, wa, ext, idx, lane, buf, cap, s_sub);
+    if (TRACE) {
+      // executor segment (wide-band extensions have only the origin segment)
+      const uint4 sg = wa.seg[idx];
+      const uint32_t ext = wa.list[sg.x];
+      if (!(wa.rec[ext].flags & FZ_FLAG_WIDE)) continue;
+      wide_ext<TRACE>(p, wa, ext, sg.x, lane, buf, cap, s_sub);
+    } else {
+      wide_ext<TRACE>(p, wa, wa.list[idx], idx, lane, buf, cap, s_sub);
+    }
   }
 }
 

@@ -22,7 +22,7 @@ struct ExtRec {
   uint32_t npath;                         // ops in path
   int32_t m, n;                           // window sizes
   uint32_t width;                         // executor trace row width (cells), 0 = no executor
-  uint32_t pad;
+  uint32_t ckpt;                          // newest window checkpoint + 1 (0 = none)
 };
 static_assert(sizeof(ExtRec) == 56, "ExtRec layout");
 
@@ -114,6 +114,28 @@ __device__ __forceinline__ int32_t threshold(int32_t best, int32_t ydrop) {
   const int64_t t = (int64_t)best - (int64_t)ydrop;
   return t < (int64_t)TFLOOR ? TFLOOR : (int32_t)t;
 }
+
+// Window checkpoint: the register-window sweep's complete state after one
+// anti-diagonal, so that a sweep can resume there (a wider window after an
+// overflow, or an executor segment).  One slot of CK_SLOT_WORDS int32:
+//   header (CK_HDR words): anti-diagonal d, base row b, rows per lane K of the
+//     writer, best score and its cell, last live anti-diagonal, flags, the
+//     previous checkpoint of the same extension (+1, 0 = none), the high word
+//     of lane 0's live-cell count, thresholds of anti-diagonals 0..32 (eager
+//     corner), each lane's live-cell count so far;
+//   then h, h of the previous anti-diagonal + (o + e - 128), I and D of the
+//     window rows, CK_WIN_MAX words each, row u = lane * K + r stored at
+//     r * 32 + lane (coalesced per slot).
+// Target and query bases of each row are functions of (b, d) and are not stored.
+constexpr int CK_HDR = 96;
+constexpr int CK_WIN_MAX = 512;
+constexpr int CK_SLOT_WORDS = CK_HDR + 4 * CK_WIN_MAX;   // 8,576 bytes
+enum CkHdr : int {
+  CK_D = 0, CK_B = 1, CK_K = 2, CK_BEST = 3, CK_BI = 4, CK_BJ = 5, CK_DLAST = 6, CK_FLAGS = 7,
+  CK_PREV = 8, CK_CNT_HI = 11,
+  CK_T = 12,     // CK_T .. CK_T + 32: thresholds
+  CK_CNT = 48    // CK_CNT .. CK_CNT + 31: per-lane live-cell counts
+};
 
 // Trace arena layout of one executor extension: (d_end + 1) rows of `width`
 // 4-bit cells (row d covers rows lo[d] .. lo[d] + width - 1 of anti-diagonal

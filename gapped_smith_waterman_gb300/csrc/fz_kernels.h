@@ -25,6 +25,17 @@ struct WorkArgs {
   uint32_t* err;               // device error word (0 = fine)
   int32_t* scratch;            // wide path: per-warp anti-diagonal buffers
   uint64_t scratch_stride;     // int32 elements per warp
+  // window checkpoints (register-window sweeps)
+  int32_t* ckpt;               // pool of CK_SLOT_WORDS-word slots, or nullptr (none written)
+  uint32_t ckpt_cap;           // slots in the pool
+  uint32_t* ckpt_used;         // slot allocator (may run past ckpt_cap: then nothing is written)
+  int32_t ckpt_every;          // write one every ckpt_every anti-diagonals (a power of two) ...
+  int32_t ckpt_recent;         // ... while the best cell is at most this many anti-diagonals back
+  int resume;                  // inspector: continue from the extension's newest checkpoint
+  // executor: work items are segments {position in the executor list, start
+  // checkpoint + 1 (0 = the origin), last anti-diagonal, first anti-diagonal};
+  // list then holds the whole executor list and trace_off is indexed by position
+  const uint4* seg;
 };
 
 // register-window sweep (extend_fast.cu)
@@ -97,6 +108,15 @@ struct EmitArgs {
   int32_t oe;
   int32_t max_sub;
 };
+// executor segments from the checkpoint chains: nseg[pos] = segments of
+// executor item pos (1 + its checkpoints before the best cell's anti-diagonal)
+// for pos < *n_exec, 0 up to n_max; then, with seg_off the exclusive scan of
+// nseg, the segments themselves
+cudaError_t launch_seg_count(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
+                             const int32_t* ckpt, uint64_t* nseg, cudaStream_t st);
+cudaError_t launch_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
+                            const int32_t* ckpt, const uint64_t* seg_off, uint4* seg, cudaStream_t st);
+
 cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st);   // eager, empty, local, not requested
 // executor items [exec_begin, exec_end); items before long_end (the bins of
 // longer alignments) get a warp each, the rest a thread each

@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(WL * 32, 3) k_local(Params p, LocalArgs la) {
       o.d_last = w.m + w.n;
       o.live = (uint64_t)w.m * (uint64_t)w.n;
       o.path = 0; o.flags = FZ_FLAG_DONE; o.npath = 0;
-      o.m = w.m; o.n = w.n; o.width = 0; o.pad = 0;
+      o.m = w.m; o.n = w.n; o.width = 0; o.ckpt = 0;
       *R = o;
       atomicAdd(la.live_total, (unsigned long long)o.live);
     }

@@ -99,6 +99,52 @@ __global__ void k_scatter(PipeArgs a) {
   }
 }
 
+// ---- executor segments ----
+constexpr int CHAIN_MAX = 1 << 22;   // bound on a chain walk (a chain never holds a cycle)
+
+// An executor extension is replayed in segments: from the origin to its first
+// checkpoint, between consecutive checkpoints, and from its last checkpoint
+// before the best cell's anti-diagonal d* to d*.  Checkpoints are linked
+// newest first, so anti-diagonals decrease along a chain.
+__global__ void k_seg_count(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
+                            const int32_t* ck, uint64_t* nseg) {
+  const uint32_t pos = blockIdx.x * blockDim.x + threadIdx.x;
+  if (pos >= n_max) return;
+  if (pos >= *n_exec) { nseg[pos] = 0; return; }
+  const ExtRec r = rec[exec_list[pos]];
+  const int32_t dstar = r.i_end + r.j_end;
+  uint64_t cnt = 1;
+  uint32_t h = ck ? r.ckpt : 0u;
+  for (int guard = 0; h && guard < CHAIN_MAX; ++guard) {
+    const int32_t* c = ck + (uint64_t)(h - 1) * CK_SLOT_WORDS;
+    if (c[CK_D] < dstar) ++cnt;
+    h = (uint32_t)c[CK_PREV];
+  }
+  nseg[pos] = cnt;
+}
+
+// seg = {position, start checkpoint + 1 (0 = origin), last anti-diagonal, first anti-diagonal}
+__global__ void k_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
+                           const int32_t* ck, const uint64_t* seg_off, uint4* seg) {
+  const uint32_t pos = blockIdx.x * blockDim.x + threadIdx.x;
+  if (pos >= n_max || pos >= *n_exec) return;
+  const ExtRec r = rec[exec_list[pos]];
+  const int32_t dstar = r.i_end + r.j_end;
+  uint64_t at = seg_off[pos];
+  int32_t end = dstar;
+  uint32_t h = ck ? r.ckpt : 0u;
+  for (int guard = 0; h && guard < CHAIN_MAX; ++guard) {
+    const int32_t* c = ck + (uint64_t)(h - 1) * CK_SLOT_WORDS;
+    const int32_t dc = c[CK_D];
+    if (dc < dstar) {
+      seg[at++] = make_uint4(pos, h, (uint32_t)end, (uint32_t)dc);
+      end = dc;
+    }
+    h = (uint32_t)c[CK_PREV];
+  }
+  seg[at] = make_uint4(pos, 0u, (uint32_t)end, 0u);
+}
+
 // ---- exclusive scan of uint64 (3 passes, 2048 elements per block) ----
 constexpr int SCAN_T = 1024;
 constexpr int SCAN_E = 2 * SCAN_T;
@@ -434,6 +480,18 @@ cudaError_t launch_scan_u64(uint64_t* data, uint32_t n, uint64_t* block_tmp, uin
   k_scan1<<<nb, SCAN_T, 0, st>>>(data, n, block_tmp);
   k_scan2<<<1, SCAN_T, 0, st>>>(block_tmp, nb, total);
   k_scan3<<<nb, SCAN_T, 0, st>>>(data, n, block_tmp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seg_count(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
+                             const int32_t* ckpt, uint64_t* nseg, cudaStream_t st) {
+  if (n_max) k_seg_count<<<(n_max + TB - 1) / TB, TB, 0, st>>>(rec, exec_list, n_max, n_exec, ckpt, nseg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
+                            const int32_t* ckpt, const uint64_t* seg_off, uint4* seg, cudaStream_t st) {
+  if (n_max) k_seg_fill<<<(n_max + TB - 1) / TB, TB, 0, st>>>(rec, exec_list, n_max, n_exec, ckpt, seg_off, seg);
   return cudaGetLastError();
 }
 

@@ -271,6 +271,37 @@ def test_host_entry_matches_device_entry():
     assert bcig.size == int(b["cigar_len"].sum())
 
 
+def test_checkpoint_settings_give_identical_results(monkeypatch):
+    """Window checkpoints change only where sweeps resume (the 512-row retry,
+    executor segments), never a result: a checkpoint every 32 anti-diagonals
+    (many segments per executor extension), none at all, and a pool that runs
+    out part-way all give the oracle's records."""
+    w = G.workload(2)
+    idx = np.arange(3000)
+    ores, ocig, ooff = G.oracle_run(w, w.seeds[idx])
+    runs = {}
+    for label, env in (("every32", {"FZ_CKPT_EVERY": "32"}), ("none", {"FZ_CKPT_SLOTS": "0"}),
+                       ("pool300", {"FZ_CKPT_SLOTS": "300", "FZ_CKPT_EVERY": "32"})):
+        for k, v in env.items():
+            monkeypatch.setenv(k, v)
+        gres, gcig, st = G.gpu_run(w, w.seeds[idx])
+        for k in env:
+            monkeypatch.delenv(k)
+        G.compare(w, w.seeds[idx], gres, gcig, ores, ocig, ooff, label=f"checkpoints {label}")
+        assert st.live_cells == int(ores["live_cells"].sum()), label
+        runs[label] = st
+    # segments tile each replay (0, d*] exactly: the replayed rows do not depend on them
+    assert runs["every32"].exec_cells == runs["none"].exec_cells == runs["pool300"].exec_cells
+
+
+def test_checkpoints_long_alignments(monkeypatch):
+    """Long alignments (60 kbp windows): many segments per extension."""
+    monkeypatch.setenv("FZ_CKPT_EVERY", "64")
+    w = G.workload(4)
+    idx = G.sample_seeds(w, 12, seed=11)
+    _check(w, w.seeds[idx], label="long-60kbp, checkpoint every 64")
+
+
 def test_chunked_executor(monkeypatch):
     w = G.workload(1)
     a, acig, sa = G.gpu_run(w)
