@@ -727,6 +727,13 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
     top_prev = (prev >> 31) != 0u;                  // conservative: may only add an overflow
     __syncwarp();
   }
+  if (!head) {
+    // sT[d], d <= 32: the best score when it rose at anti-diagonal d (NEG: it
+    // did not); the eager corner's thresholds are rebuilt from these
+    sT[lane] = NEG;
+    if (lane == 0) sT[32] = NEG;
+    __syncwarp();
+  }
   Reservoir qr, tr;
   res_init(qr, p.q2, p.q_len, w.qg0, w.dir, (int64_t)d + 1 - b);   // query columns entering at row b
   res_init(tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + WIN);     // target rows entering at the window top
@@ -743,76 +750,83 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
 
   // The step loop leaves at the end of the sweep, on an overflow, and at every
   // checkpoint boundary; the checkpoint writes stay out of the step loop.
-  int why = 0;   // 0: checkpoint boundary, 1: overflow, 2: the sweep ended
-  for (;;) {
-  for (;;) {
-    const int32_t dn = d + 1;
-    if (dn > mn) { why = 2; break; }
-    const bool shift = !rowb_alive;
-    const int32_t bn = b + (shift ? 1 : 0);
-    if (!shift && (top || top_prev)) { why = 1; break; }   // the live band may grow past the window top
-    const bool edge = bn + WIN - 1 > m || bn < dn - n;
-    int32_t lm;
-    if (!shift) {
-      in.qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-      if (edge) {
-        const int32_t rowbase = bn + lane * KS;
-        in.vhi = m - rowbase;
-        in.vlo = dn - n - rowbase;
-        lm = step<KS, KS, false, false, true>(L, in, lane, cnt, no_codes);
-      } else {
-        lm = step<KS, KS, false, false, false>(L, in, lane, cnt, no_codes);
-      }
-    } else {
-      in.mr_new = s_mrow[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-      if (edge) {
-        const int32_t rowbase = bn + lane * KS;
-        in.vhi = m - rowbase;
-        in.vlo = dn - n - rowbase;
-        lm = step<KS, KS, false, true, true>(L, in, lane, cnt, no_codes);
-      } else {
-        lm = step<KS, KS, false, true, false>(L, in, lane, cnt, no_codes);
-      }
-    }
-    const int32_t wm = __reduce_max_sync(FULL, lm);
-    const bool edge_lane = (lane == 0 && L.H[0] >= in.Th) || (lane == 31 && lm >= in.Th);
-    const uint32_t bits = __ballot_sync(FULL, edge_lane);
-    sT[imin(dn, 2 * EAGER_N + 1)] = in.Th + oe;       // thresholds of anti-diagonals 1..32 (33: scratch)
-    const bool live = wm >= in.Th;
-    if (wm + oe > best) {                                // implies live
-      int rf = KS;
+  // Exits are tested once per step, after it, for the next step: the end of
+  // the sweep (two empty anti-diagonals, or the window's last one), an
+  // overflow (the base stays and the top lane is or was live), and every
+  // checkpoint boundary; the checkpoint writes stay out of the step loop.
+  int why = d + 1 > mn ? 2 : ((rowb_alive && (top || top_prev)) ? 1 : 0);   // 0 boundary, 1 overflow, 2 end
+  if (why == 0) {
+    for (;;) {
+      for (;;) {
+        const int32_t dn = d + 1;
+        const bool shift = !rowb_alive;
+        const int32_t bn = b + (shift ? 1 : 0);
+        const bool edge = bn + WIN - 1 > m || bn < dn - n;
+        int32_t lm;
+        if (!shift) {
+          in.qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
+          if (edge) {
+            const int32_t rowbase = bn + lane * KS;
+            in.vhi = m - rowbase;
+            in.vlo = dn - n - rowbase;
+            lm = step<KS, KS, false, false, true>(L, in, lane, cnt, no_codes);
+          } else {
+            lm = step<KS, KS, false, false, false>(L, in, lane, cnt, no_codes);
+          }
+        } else {
+          in.mr_new = s_mrow[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+          if (edge) {
+            const int32_t rowbase = bn + lane * KS;
+            in.vhi = m - rowbase;
+            in.vlo = dn - n - rowbase;
+            lm = step<KS, KS, false, true, true>(L, in, lane, cnt, no_codes);
+          } else {
+            lm = step<KS, KS, false, true, false>(L, in, lane, cnt, no_codes);
+          }
+        }
+        const int32_t wm = __reduce_max_sync(FULL, lm);
+        const bool edge_lane = (lane == 0 && L.H[0] >= in.Th) || (lane == 31 && lm >= in.Th);
+        const uint32_t bits = __ballot_sync(FULL, edge_lane);
+        const bool live = wm >= in.Th;
+        if (wm + oe > best) {                                // implies live
+          int rf = KS;
 #pragma unroll
-      for (int r = KS - 1; r >= 0; --r) rf = (L.H[r] == wm) ? r : rf;
-      const uint32_t fm = __ballot_sync(FULL, rf < KS);
-      const int Ln = __ffs(fm) - 1;
-      const int rr = __shfl_sync(FULL, rf, Ln);
-      bi = bn + Ln * KS + rr;
-      bj = dn - bi;
-      best = wm + oe;
-      in.Th = threshold(best, p.ydrop) - oe;
-    }
-    d_last = live ? dn : d_last;
-    rowb_alive = bits & 1u;
-    top_prev = top && !shift;      // the old top row is still the top row only if the base stayed
-    top = (bits >> 31) != 0u;
-    b = bn;
-    d = dn;
-    if (!live && !live_prev) { why = 2; break; }
-    live_prev = live;
-    if (((uint32_t)d & ck_mask) == 0u) { why = 0; break; }
-  }
-    if (why == 2) break;
-    if (why == 1) {
-      overflow = true;
-      if (wa.ckpt) {     // the wider window resumes here
+          for (int r = KS - 1; r >= 0; --r) rf = (L.H[r] == wm) ? r : rf;
+          const uint32_t fm = __ballot_sync(FULL, rf < KS);
+          const int Ln = __ffs(fm) - 1;
+          const int rr = __shfl_sync(FULL, rf, Ln);
+          bi = bn + Ln * KS + rr;
+          bj = dn - bi;
+          best = wm + oe;
+          in.Th = threshold(best, p.ydrop) - oe;
+          if (dn <= 2 * EAGER_N && lane == 0) sT[dn] = best;   // eager corner thresholds come from these
+        }
+        d_last = live ? dn : d_last;
+        rowb_alive = bits & 1u;
+        top_prev = top && !shift;      // the old top row is still the top row only if the base stayed
+        top = (bits >> 31) != 0u;
+        b = bn;
+        d = dn;
+        const bool end_ = (!live && !live_prev) || d + 1 > mn;
+        live_prev = live;
+        const bool ovf = rowb_alive && (top || top_prev);
+        if (end_ || ovf || ((uint32_t)d & ck_mask) == 0u) {
+          why = end_ ? 2 : (ovf ? 1 : 0);
+          break;
+        }
+      }
+      if (why != 0) break;
+      // periodic checkpoint while the best cell is recent: executor segments
+      // start from these
+      if (d - (bi + bj) <= wa.ckpt_recent) {
         const CkScalars cs{b, d, best, bi, bj, d_last};
         head = ck_write<KS>(wa, L, lane, head, cs, cnt, cnt_hi_carry, sT);
       }
-      break;
     }
-    // periodic checkpoint while the best cell is recent: executor segments
-    // start from these
-    if (d - (bi + bj) <= wa.ckpt_recent) {
+  }
+  if (why == 1) {
+    overflow = true;   // the live band may grow past the window top
+    if (wa.ckpt) {     // the wider window resumes here
       const CkScalars cs{b, d, best, bi, bj, d_last};
       head = ck_write<KS>(wa, L, lane, head, cs, cnt, cnt_hi_carry, sT);
     }
@@ -842,7 +856,18 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
   if (bi <= EAGER_N && bj <= EAGER_N) {
     flags |= FZ_FLAG_EAGER;
     width = 0;
-    if (bi + bj > 0) eager_corner(p, w, lane, sT, tile, s_sub, bi, bj, path, npath, wa.err);
+    if (bi + bj > 0) {
+      // thresholds of anti-diagonals 1..32: from the best score over the
+      // anti-diagonals before each (the origin scores 0)
+      int32_t v = sT[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) v = imax(v, __shfl_up_sync(FULL, v, o));
+      v = imax(v, 0);                                  // best over anti-diagonals 0 .. lane
+      __syncwarp();
+      sT[lane + 1] = threshold(v, p.ydrop);            // lane 31 writes sT[32]
+      __syncwarp();
+      eager_corner(p, w, lane, sT, tile, s_sub, bi, bj, path, npath, wa.err);
+    }
   }
   if (lane == 0) {
     ExtRec o;
