@@ -53,7 +53,7 @@ struct Counters {
   uint32_t bin_cursor[8];
   uint32_t ckpt_used;          // window checkpoint slots taken (may exceed the pool)
   uint32_t pad_;
-  uint64_t seg_total;          // executor segments
+  uint64_t seg_total[3];       // executor segments per tier (384 rows, 512 rows, wide)
 };
 
 constexpr uint64_t TRACE_CAP_DEFAULT = 1ull << 30;   // smallest executor arena cap before chunking
@@ -129,7 +129,7 @@ fz_status ensure_batch_buffers(fz_ctx* ctx, uint32_t n_ext) {
   CU(ctx->scan_tmp.ensure((size_t)scan_tmp_elems((uint32_t)n) * 8));
   CU(ctx->wide_list.ensure(n * 4));
   CU(ctx->retry_list.ensure(n * 4));
-  CU(ctx->seg_cnt.ensure(n * 8));
+  CU(ctx->seg_cnt.ensure(3 * n * 8));
   CU(ctx->counters.ensure(sizeof(Counters)));
   if (ctx->mode == FZ_EXTEND) {
     const uint64_t per = wide_scratch_elems(ctx->p.max_len) * 4;
@@ -268,8 +268,10 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   CU(launch_scan_u64(pa.trace_sz, n_ext, ctx->scan_tmp.as<uint64_t>(), &dc->trace_total, st));
   // executor segments: count per executor item, then their offsets
   CU(launch_seg_count(pa.rec, pa.exec_list, n_ext, &dc->bin_cursor[0], wa.ckpt, ctx->seg_cnt.as<uint64_t>(), st));
-  CU(launch_scan_u64(ctx->seg_cnt.as<uint64_t>(), n_ext, ctx->scan_tmp.as<uint64_t>(), &dc->seg_total, st));
-  ctx->launches += 3 + 6 + 4;
+  for (int t = 0; t < 3; ++t)
+    CU(launch_scan_u64(ctx->seg_cnt.as<uint64_t>() + (size_t)t * n_ext, n_ext, ctx->scan_tmp.as<uint64_t>(),
+                       &dc->seg_total[t], st));
+  ctx->launches += 3 + 6 + 1 + 9;
   mark(ctx, 3, st);
   CU(cudaMemcpyAsync(ctx->h_cnt, dc, sizeof(Counters), cudaMemcpyDeviceToHost, st));
   CU(cudaStreamSynchronize(st));
@@ -283,30 +285,35 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   CU(ctx->cigar.ensure(std::max<uint64_t>(hc.cig_total, 1) * 4));
   ctx->stats.trace_bytes = hc.trace_total;
   ctx->stats.cigar_runs = hc.cig_total;
-  const uint64_t n_seg = hc.seg_total;
+  const uint64_t seg_base[4] = {0, hc.seg_total[0], hc.seg_total[0] + hc.seg_total[1],
+                                hc.seg_total[0] + hc.seg_total[1] + hc.seg_total[2]};
+  const uint64_t n_seg = seg_base[3];
   if (wa.ckpt && hc.ckpt_used > wa.ckpt_cap)   // checkpoints were dropped: a larger pool next batch
     ctx->ckpt_demand = std::max<uint64_t>(ctx->ckpt_demand, (uint64_t)hc.ckpt_used + hc.ckpt_used / 4);
   if (n_exec) {
     CU(ctx->seg.ensure(std::max<uint64_t>(n_seg, 1) * sizeof(uint4)));
     CU(launch_seg_fill(pa.rec, pa.exec_list, n_ext, &dc->bin_cursor[0], wa.ckpt, ctx->seg_cnt.as<uint64_t>(),
-                       ctx->seg.as<uint4>(), st));
+                       ctx->seg.as<uint4>(), seg_base[1], seg_base[2], st));
     ctx->launches += 1;
   }
 
   // 3. executor + traceback, chunked by the arena cap
   std::vector<std::pair<uint32_t, uint32_t>> chunks;
-  std::vector<uint64_t> toff, soff;          // per position: trace offset, first segment
+  std::vector<uint64_t> toff, soff;          // per position: trace offset; per tier and position: first segment
   if (n_exec) {
     if (hc.trace_total <= ctx->trace_cap) {
       chunks.push_back({0u, n_exec});
       CU(ctx->trace.ensure(std::max<uint64_t>(hc.trace_total, 16)));
     } else {
       toff.resize(n_exec + 1);
-      soff.resize(n_exec + 1);
+      soff.resize(3 * ((size_t)n_exec + 1));
       CU(cudaMemcpy(toff.data(), ctx->trace_sz.p, (size_t)n_exec * 8, cudaMemcpyDeviceToHost));
-      CU(cudaMemcpy(soff.data(), ctx->seg_cnt.p, (size_t)n_exec * 8, cudaMemcpyDeviceToHost));
+      for (int t = 0; t < 3; ++t) {
+        CU(cudaMemcpy(soff.data() + (size_t)t * (n_exec + 1), ctx->seg_cnt.as<uint64_t>() + (size_t)t * n_ext,
+                      (size_t)n_exec * 8, cudaMemcpyDeviceToHost));
+        soff[(size_t)t * (n_exec + 1) + n_exec] = hc.seg_total[t];
+      }
       toff[n_exec] = hc.trace_total;
-      soff[n_exec] = n_seg;
       uint32_t a = 0;
       while (a < n_exec) {
         uint32_t b = a + 1;
@@ -338,27 +345,26 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   bool first_chunk = true;
   for (auto& c : chunks) {
     const uint64_t sub = toff.empty() ? 0 : toff[c.first];
-    const uint64_t s0 = soff.empty() ? 0 : soff[c.first], s1 = soff.empty() ? n_seg : soff[c.second];
     WorkArgs we = wa;
     we.list = ctx->exec_list.as<uint32_t>();    // segments name executor positions
-    we.seg = ctx->seg.as<uint4>() + s0;
-    we.n_work = (uint32_t)(s1 - s0);
     we.n_work_dev = nullptr;
     we.trace = ctx->trace.as<uint8_t>();
     we.trace_off = ctx->trace_sz.as<uint64_t>();
     we.trace_sub = sub;
     if (!first_chunk) CU(cudaMemsetAsync(&dc->work[3], 0, 3 * sizeof(uint32_t), st));
     first_chunk = false;
-    if (ctx->fast_ok) {
-      for (int tier = 0; tier < 2; ++tier) {
-        we.counter = &dc->work[3 + tier];
-        CU(launch_execute_fast(tier, ctx->p, we, ctx->grid_fast_trace[tier], st));
-        ctx->launches += 1;
-      }
+    for (int tier = 0; tier < 3; ++tier) {
+      // this tier's segments of the chunk's positions
+      const uint64_t* so = soff.empty() ? nullptr : soff.data() + (size_t)tier * (n_exec + 1);
+      const uint64_t s0 = so ? so[c.first] : 0, s1 = so ? so[c.second] : hc.seg_total[tier];
+      if (s1 == s0) continue;
+      we.seg = ctx->seg.as<uint4>() + seg_base[tier] + s0;
+      we.n_work = (uint32_t)(s1 - s0);
+      we.counter = &dc->work[3 + tier];
+      if (tier < 2) CU(launch_execute_fast(tier, ctx->p, we, ctx->grid_fast_trace[tier], st));
+      else CU(launch_execute_wide(ctx->p, we, ctx->grid_wide, st));
+      ctx->launches += 1;
     }
-    we.counter = &dc->work[5];
-    CU(launch_execute_wide(ctx->p, we, ctx->grid_wide, st));
-    ctx->launches += 1;
     if (chunks.size() > 1) {
       EmitArgs ex = ea;
       ex.exec_begin = c.first;

@@ -754,7 +754,7 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
   // the sweep (two empty anti-diagonals, or the window's last one), an
   // overflow (the base stays and the top lane is or was live), and every
   // checkpoint boundary; the checkpoint writes stay out of the step loop.
-  int why = d + 1 > mn ? 2 : ((rowb_alive && (top || top_prev)) ? 1 : 0);   // 0 boundary, 1 overflow, 2 end
+  int why = d + 1 > mn ? 2 : ((rowb_alive && (top || top_prev) && b + WIN <= m) ? 1 : 0);   // 0 boundary, 1 overflow, 2 end
   if (why == 0) {
     for (;;) {
       for (;;) {
@@ -809,7 +809,8 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
         d = dn;
         const bool end_ = (!live && !live_prev) || d + 1 > mn;
         live_prev = live;
-        const bool ovf = rowb_alive && (top || top_prev);
+        // (no overflow once the window reaches row m: no row lies beyond it)
+        const bool ovf = rowb_alive && (top || top_prev) && b + WIN <= m;
         if (end_ || ovf || ((uint32_t)d & ck_mask) == 0u) {
           why = end_ ? 2 : (ovf ? 1 : 0);
           break;
@@ -917,7 +918,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_extend(Params p, WorkArgs 
 // Two register windows: 384 rows (K = 12, fitted to 4 blocks of 4 warps per
 // SM) holds the live band of typical y-drop extensions; extensions whose band
 // could outgrow it are retried with 512 rows (K = 16), then the wide path.
-constexpr int KA = 12, KB = 16;
+constexpr int KA = K_TIER0, KB = K_TIER1;
 
 int fast_window_rows(int tier) { return 32 * (tier == 0 ? KA : KB); }
 

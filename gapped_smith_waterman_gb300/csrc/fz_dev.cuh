@@ -11,6 +11,7 @@ constexpr int32_t NEG = -(1 << 30);       // dead / missing score
 constexpr int32_t TFLOOR = -(1 << 29);    // lowest threshold: every reachable cell is above it
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int EAGER_N = 16;               // eager traceback corner: i*, j* <= 16
+constexpr int K_TIER0 = 12, K_TIER1 = 16; // rows per lane of the two register windows (384, 512 rows)
 
 // Per-extension record written by the inspector, read by binning, the
 // executor and the traceback.

@@ -108,14 +108,17 @@ struct EmitArgs {
   int32_t oe;
   int32_t max_sub;
 };
-// executor segments from the checkpoint chains: nseg[pos] = segments of
-// executor item pos (1 + its checkpoints before the best cell's anti-diagonal)
-// for pos < *n_exec, 0 up to n_max; then, with seg_off the exclusive scan of
-// nseg, the segments themselves
+// executor segments from the checkpoint chains, one list per executor tier
+// (0: 384-row window, 1: 512-row window, 2: wide band): nseg holds three
+// arrays of n_max counts; item pos < *n_exec counts 1 + its checkpoints
+// before the best cell's anti-diagonal in its tier's array.  Then, with
+// seg_off the per-tier exclusive scans, the segments themselves (tier t's
+// list starts at seg + base_t, base_0 = 0)
 cudaError_t launch_seg_count(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
                              const int32_t* ckpt, uint64_t* nseg, cudaStream_t st);
 cudaError_t launch_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
-                            const int32_t* ckpt, const uint64_t* seg_off, uint4* seg, cudaStream_t st);
+                            const int32_t* ckpt, const uint64_t* seg_off, uint4* seg, uint64_t base1, uint64_t base2,
+                            cudaStream_t st);
 
 cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st);   // eager, empty, local, not requested
 // executor items [exec_begin, exec_end); items before long_end (the bins of

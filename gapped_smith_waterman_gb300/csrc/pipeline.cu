@@ -106,11 +106,22 @@ constexpr int CHAIN_MAX = 1 << 22;   // bound on a chain walk (a chain never hol
 // checkpoint, between consecutive checkpoints, and from its last checkpoint
 // before the best cell's anti-diagonal d* to d*.  Checkpoints are linked
 // newest first, so anti-diagonals decrease along a chain.
+// Executor tier of an extension: 0 = 384-row window, 1 = 512-row window, 2 = wide band.
+__device__ __forceinline__ int exec_tier(const ExtRec& r) {
+  return (r.flags & FZ_FLAG_WIDE) ? 2 : (r.width == 32u * K_TIER0 ? 0 : 1);
+}
+
+// nseg holds three arrays of n_max counts, one per tier: item pos counts in
+// its tier's array (0 in the others), so that each tier's segments form one
+// list after a scan of its array.
 __global__ void k_seg_count(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
                             const int32_t* ck, uint64_t* nseg) {
   const uint32_t pos = blockIdx.x * blockDim.x + threadIdx.x;
   if (pos >= n_max) return;
-  if (pos >= *n_exec) { nseg[pos] = 0; return; }
+  nseg[pos] = 0;
+  nseg[n_max + pos] = 0;
+  nseg[2ull * n_max + pos] = 0;
+  if (pos >= *n_exec) return;
   const ExtRec r = rec[exec_list[pos]];
   const int32_t dstar = r.i_end + r.j_end;
   uint64_t cnt = 1;
@@ -120,17 +131,19 @@ __global__ void k_seg_count(const ExtRec* rec, const uint32_t* exec_list, uint32
     if (c[CK_D] < dstar) ++cnt;
     h = (uint32_t)c[CK_PREV];
   }
-  nseg[pos] = cnt;
+  nseg[(uint64_t)exec_tier(r) * n_max + pos] = cnt;
 }
 
-// seg = {position, start checkpoint + 1 (0 = origin), last anti-diagonal, first anti-diagonal}
+// seg = {position, start checkpoint + 1 (0 = origin), last anti-diagonal,
+// first anti-diagonal}; tier t's segments start at seg + base[t]
 __global__ void k_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
-                           const int32_t* ck, const uint64_t* seg_off, uint4* seg) {
+                           const int32_t* ck, const uint64_t* seg_off, uint4* seg, uint64_t base1, uint64_t base2) {
   const uint32_t pos = blockIdx.x * blockDim.x + threadIdx.x;
   if (pos >= n_max || pos >= *n_exec) return;
   const ExtRec r = rec[exec_list[pos]];
+  const int tier = exec_tier(r);
   const int32_t dstar = r.i_end + r.j_end;
-  uint64_t at = seg_off[pos];
+  uint64_t at = (tier == 0 ? 0 : (tier == 1 ? base1 : base2)) + seg_off[(uint64_t)tier * n_max + pos];
   int32_t end = dstar;
   uint32_t h = ck ? r.ckpt : 0u;
   for (int guard = 0; h && guard < CHAIN_MAX; ++guard) {
@@ -391,6 +404,16 @@ __device__ void walk_warp(const EmitArgs& a, uint32_t pos, int lane, uint32_t (*
       for (int k = 0; k < SEG_W; ++k) seg[lane][k] = src[k];
       seg_off[lane] = (int32_t)(a0 - row);                  // byte offset of the segment in its row
       seg_lo[lane] = lot;
+      // The next batch starts about 32 anti-diagonals lower and at most 33
+      // rows lower: pull its row origins and, with this row's origin as the
+      // guess, its row segments into L2 while lane 0 walks this batch.
+      const int32_t dq = dt - 32;
+      if (dq >= 0) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(w.lo + dq));
+        int32_t uq = iA - 16 - lane - lot;
+        uq = uq < 0 ? 0 : ((uint32_t)uq >= w.W ? (int32_t)w.W - 1 : uq);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(w.base + (uint64_t)dq * rowb + (uint32_t)(uq >> 1)));
+      }
     }
     __syncwarp();
     if (lane == 0) {
@@ -490,8 +513,10 @@ cudaError_t launch_seg_count(const ExtRec* rec, const uint32_t* exec_list, uint3
 }
 
 cudaError_t launch_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32_t n_max, const uint32_t* n_exec,
-                            const int32_t* ckpt, const uint64_t* seg_off, uint4* seg, cudaStream_t st) {
-  if (n_max) k_seg_fill<<<(n_max + TB - 1) / TB, TB, 0, st>>>(rec, exec_list, n_max, n_exec, ckpt, seg_off, seg);
+                            const int32_t* ckpt, const uint64_t* seg_off, uint4* seg, uint64_t base1, uint64_t base2,
+                            cudaStream_t st) {
+  if (n_max)
+    k_seg_fill<<<(n_max + TB - 1) / TB, TB, 0, st>>>(rec, exec_list, n_max, n_exec, ckpt, seg_off, seg, base1, base2);
   return cudaGetLastError();
 }
 
