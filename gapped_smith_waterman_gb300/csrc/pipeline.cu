@@ -247,6 +247,12 @@ struct RunWriter {
     op = o;
     len = 1;
   }
+  __device__ void push_n(uint32_t o, uint32_t n) {   // n >= 1 ops of one kind
+    if (o == op) { len += n; return; }
+    flush();
+    op = o;
+    len = n;
+  }
   __device__ uint32_t first() const { return (uint32_t)(backwards ? off + cap - nruns : off); }
 };
 
@@ -416,24 +422,70 @@ __device__ void walk_warp(const EmitArgs& a, uint32_t pos, int lane, uint32_t (*
       }
     }
     __syncwarp();
-    if (lane == 0) {
-      for (;;) {
-        if (!(w.i > 0 || w.j > 0)) { run = false; break; }
-        if (--guard <= 0) { run = false; break; }
-        if (w.i < 0 || w.j < 0) { atomicOr(a.err, 1u); run = false; break; }
-        const int32_t d = w.i + w.j, t = dA - d;
-        if (t >= 32) break;                                 // left the loaded anti-diagonals
-        const int32_t u = w.i - seg_lo[t];
-        if (u < 0 || (uint32_t)u >= w.W) { atomicOr(a.err, 1u); run = false; break; }
-        const int32_t b = (u >> 1) - seg_off[t];
-        uint32_t byte;
-        if (b >= 0 && b < 4 * SEG_W) byte = (seg[t][b >> 2] >> (8 * (b & 3))) & 0xffu;
-        else byte = w.base[(uint64_t)d * rowb + (uint32_t)(u >> 1)];
-        const uint32_t c = (byte >> (4 * (u & 1))) & 15u;
-        if (!walk_step(w, c, wr, a.err)) { run = false; break; }
+    // Walk this batch with the whole warp.  The walker's state (i, j, st) is
+    // the same in every lane; lane k looks at the k-th cell of a run in the
+    // current state's direction (diagonal in S, left in I, up in D), and one
+    // ballot gives the run of moves that stays in the state.  Cells outside
+    // the staged segments end a run; the walker's own cell is read from global
+    // memory when it is not staged.
+    for (;;) {
+      if (!(w.i > 0 || w.j > 0)) { run = false; break; }
+      if (--guard <= 0) { run = false; break; }
+      if (w.i < 0 || w.j < 0) { if (lane == 0) atomicOr(a.err, 1u); run = false; break; }
+      const int32_t t = dA - (w.i + w.j);
+      if (t >= 32) break;                                   // left the loaded anti-diagonals
+      int32_t ci, cj, ct;
+      if (w.st == 0) { ci = w.i - lane; cj = w.j - lane; ct = t + 2 * lane; }
+      else if (w.st == 1) { ci = w.i; cj = w.j - lane; ct = t + lane; }
+      else { ci = w.i - lane; cj = w.j; ct = t + lane; }
+      uint32_t c = 0;
+      bool known = false, band = true;
+      if (ct < 32 && ci >= 0 && cj >= 0) {
+        const int32_t u = ci - seg_lo[ct];
+        band = u >= 0 && (uint32_t)u < w.W;
+        if (band) {
+          const int32_t b = (u >> 1) - seg_off[ct];
+          if (b >= 0 && b < 4 * SEG_W) {
+            c = ((seg[ct][b >> 2] >> (8 * (b & 3))) >> (4 * (u & 1))) & 15u;
+            known = true;
+          } else if (lane == 0) {
+            c = (w.base[(uint64_t)(w.i + w.j) * rowb + (uint32_t)(u >> 1)] >> (4 * (u & 1))) & 15u;
+            known = true;
+          }
+        }
+      }
+      if (!__shfl_sync(FULL, band ? 1 : 0, 0)) { if (lane == 0) atomicOr(a.err, 1u); run = false; break; }
+      const uint32_t c0 = __shfl_sync(FULL, c, 0);
+      if (w.st == 0) {
+        const uint32_t diag = __ballot_sync(FULL, known && (c & 3u) == 0u && ci >= 1 && cj >= 1);
+        const int n = __ffs(~diag) - 1;                     // leading diagonal moves (-1: all 32)
+        const int k = n < 0 ? 32 : n;
+        if (k > 0) {
+          if (lane == 0) wr.push_n(0, (uint32_t)k);
+          w.i -= k;
+          w.j -= k;
+          continue;
+        }
+        const uint32_t sc = c0 & 3u;
+        if (sc == 3u || sc == 0u) { if (lane == 0) atomicOr(a.err, sc == 3u ? 2u : 1u); run = false; break; }
+        w.st = (int)sc;
+      } else {
+        // a run of gap moves: every cell pushes the gap op; the cell whose code
+        // says the gap opens there returns the walk to S
+        const uint32_t bit = w.st == 1 ? 4u : 8u;
+        const bool valid = known && (w.st == 1 ? cj >= 1 : ci >= 1);
+        const uint32_t vm = __ballot_sync(FULL, valid);
+        const uint32_t om = __ballot_sync(FULL, valid && (c & bit) != 0u);
+        const int nv = __ffs(~vm) - 1;
+        const int nvalid = nv < 0 ? 32 : nv;                // cells from the walker's that can be used
+        if (nvalid == 0) { if (lane == 0) atomicOr(a.err, 1u); run = false; break; }
+        const int f = __ffs(om) - 1;                         // first opening cell, or -1
+        const int k = (f >= 0 && f < nvalid) ? f + 1 : nvalid;
+        if (lane == 0) wr.push_n((uint32_t)w.st, (uint32_t)k);
+        if (w.st == 1) w.j -= k; else w.i -= k;
+        if (f >= 0 && f < nvalid) w.st = 0;
       }
     }
-    run = __shfl_sync(FULL, run, 0);
     __syncwarp();
   }
   if (lane == 0) emit_done(a, x, r, wr, off, guard);
