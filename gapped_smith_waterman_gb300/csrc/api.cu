@@ -45,6 +45,7 @@ struct Counters {
   uint64_t trace_total;
   uint64_t cig_total;
   uint64_t cig_packed;         // runs actually written (host-copy packing)
+  uint64_t comb_total;         // runs of the combined two-sided CIGARs
   uint32_t work[8];            // dynamic work counters: 0..2 inspectors, 3..5 executors
   uint32_t retry_count;        // extensions retried with the 512-row window
   uint32_t wide_count;
@@ -72,6 +73,7 @@ struct fz_ctx {
   DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, retry_list, counters;
   DevBuf cigar, cigar_packed, trace, scratch, spill;
   DevBuf ckpt, seg_cnt, seg;         // window checkpoints, executor segments
+  DevBuf comb_off, comb_cig;         // two-sided alignments (fz_combine)
   DevBuf in_t, in_q, in_seeds, out_res;
   Counters* h_cnt = nullptr;         // pinned
   cudaStream_t last_stream = nullptr;
@@ -580,6 +582,31 @@ fz_status fz_extend_batch_host(fz_ctx* ctx, const uint8_t* h_target2, uint64_t t
   return FZ_OK;
 }
 
+fz_status fz_combine(fz_ctx* ctx, const fz_seed* d_seeds, uint32_t n_seeds, const fz_result* d_res,
+                     const uint32_t* d_cigar, fz_alignment* d_aln, const uint32_t** d_aln_cigar,
+                     void* cuda_stream) {
+  if (!ctx) return FZ_ERR_ARG;
+  ctx->err.clear();
+  if (n_seeds && (!d_seeds || !d_res || !d_aln || (!d_cigar && ctx->mode == FZ_EXTEND)))
+    return fail(ctx, FZ_ERR_ARG, "null seeds, results, CIGAR arena or output");
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  CU(cudaSetDevice(ctx->device));
+  CU(ctx->counters.ensure(sizeof(Counters)));
+  CU(ctx->comb_off.ensure(std::max<size_t>(n_seeds, 1) * 8));
+  CU(ctx->scan_tmp.ensure((size_t)scan_tmp_elems(std::max<uint32_t>(n_seeds, 1)) * 8));
+  Counters* dc = ctx->counters.as<Counters>();
+  CU(launch_comb_lens(d_res, n_seeds, d_cigar, ctx->comb_off.as<uint64_t>(), st));
+  CU(launch_scan_u64(ctx->comb_off.as<uint64_t>(), n_seeds, ctx->scan_tmp.as<uint64_t>(), &dc->comb_total, st));
+  CU(cudaMemcpyAsync(&ctx->h_cnt->comb_total, &dc->comb_total, sizeof(uint64_t), cudaMemcpyDeviceToHost, st));
+  CU(cudaStreamSynchronize(st));
+  const uint64_t total = ctx->h_cnt->comb_total;
+  CU(ctx->comb_cig.ensure(std::max<uint64_t>(total, 1) * 4));
+  CU(launch_comb(d_seeds, n_seeds, d_res, d_cigar, ctx->comb_off.as<uint64_t>(), ctx->comb_cig.as<uint32_t>(),
+                 d_aln, st));
+  if (d_aln_cigar) *d_aln_cigar = ctx->comb_cig.as<uint32_t>();
+  return FZ_OK;
+}
+
 fz_status fz_get_stats(fz_ctx* ctx, fz_stats* out) {
   if (!ctx || !out) return FZ_ERR_ARG;
   if (!ctx->have_batch) return fail(ctx, FZ_ERR_ARG, "no completed batch");
@@ -629,7 +656,8 @@ void fz_destroy(fz_ctx* ctx) {
   cudaSetDevice(ctx->device);
   DevBuf* bufs[] = {&ctx->rec, &ctx->ext_bin, &ctx->exec_list, &ctx->exec_pos, &ctx->trace_sz, &ctx->cig_cap,
                     &ctx->scan_tmp, &ctx->wide_list, &ctx->retry_list, &ctx->counters, &ctx->cigar, &ctx->trace, &ctx->scratch,
-                    &ctx->spill, &ctx->in_t, &ctx->in_q, &ctx->in_seeds, &ctx->out_res};
+                    &ctx->spill, &ctx->in_t, &ctx->in_q, &ctx->in_seeds, &ctx->out_res, &ctx->cigar_packed,
+                    &ctx->ckpt, &ctx->seg_cnt, &ctx->seg, &ctx->comb_off, &ctx->comb_cig};
   for (DevBuf* b : bufs) b->release();
   if (ctx->h_cnt) cudaFreeHost(ctx->h_cnt);
   for (cudaEvent_t& e : ctx->ev)

@@ -131,6 +131,13 @@ cudaError_t launch_cig_lens(const fz_result* out, uint32_t n, uint64_t* lens, cu
 cudaError_t launch_cig_pack(fz_result* out, uint32_t n, const uint64_t* poff, const uint32_t* src, uint32_t* dst,
                             cudaStream_t st);
 
+// two-sided alignments: lens[k] = runs of seed k's combined CIGAR; then, with
+// off the exclusive scan of lens, the combined records and runs (fz_combine in fz.h)
+cudaError_t launch_comb_lens(const fz_result* res, uint32_t n_seeds, const uint32_t* cig, uint64_t* lens,
+                             cudaStream_t st);
+cudaError_t launch_comb(const fz_seed* seeds, uint32_t n_seeds, const fz_result* res, const uint32_t* cig,
+                        const uint64_t* off, uint32_t* out_cig, fz_alignment* aln, cudaStream_t st);
+
 // integer pipe microbenchmark (microbench.cu)
 cudaError_t bench_int_rates(double rates[4]);
 

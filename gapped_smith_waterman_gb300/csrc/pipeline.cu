@@ -510,6 +510,58 @@ __global__ void k_cig_pack(fz_result* out, uint32_t n, const uint64_t* poff, con
   if (lane == 0) out[x].cigar_off = (uint32_t)to;
 }
 
+// ---- two-sided alignments (fz_combine) ----
+// runs of seed k's combined CIGAR: both sides' runs, one fewer when the two
+// runs meeting at the anchor are the same operation
+__device__ __forceinline__ uint32_t comb_runs(const fz_result& rr, const fz_result& rl, const uint32_t* cig,
+                                              bool& merge) {
+  const uint32_t nl = (rl.flags & FZ_FLAG_DONE) ? rl.cigar_len : 0u;
+  const uint32_t nr = (rr.flags & FZ_FLAG_DONE) ? rr.cigar_len : 0u;
+  merge = nl && nr && (cig[(uint64_t)rl.cigar_off + nl - 1] & 15u) == (cig[rr.cigar_off] & 15u);
+  return nl + nr - (merge ? 1u : 0u);
+}
+
+__global__ void k_comb_lens(const fz_result* res, uint32_t n_seeds, const uint32_t* cig, uint64_t* lens) {
+  const uint32_t k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n_seeds) return;
+  bool merge;
+  lens[k] = comb_runs(res[2 * k], res[2 * k + 1], cig, merge);
+}
+
+// warp per seed: the left runs, then the right runs; the two runs that meet at
+// the anchor become one when they are the same operation
+__global__ void k_comb(const fz_seed* seeds, uint32_t n_seeds, const fz_result* res, const uint32_t* cig,
+                       const uint64_t* off, uint32_t* out_cig, fz_alignment* aln) {
+  const uint32_t k = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (k >= n_seeds) return;
+  const fz_seed sd = seeds[k];
+  const fz_result rr = res[2 * k], rl = res[2 * k + 1];
+  const bool hr = (rr.flags & FZ_FLAG_DONE) != 0u, hl = (rl.flags & FZ_FLAG_DONE) != 0u;
+  const uint32_t nl = hl ? rl.cigar_len : 0u, nr = hr ? rr.cigar_len : 0u;
+  const uint64_t o = off[k];
+  bool merge;
+  const uint32_t total = comb_runs(rr, rl, cig, merge);
+  const uint32_t first_r = nr ? cig[rr.cigar_off] : 0u;
+  for (uint32_t q = lane; q < nl; q += 32) {
+    uint32_t v = cig[(uint64_t)rl.cigar_off + q];
+    if (merge && q == nl - 1) v += first_r & ~15u;     // add the right run's length
+    out_cig[o + q] = v;
+  }
+  const uint32_t skip = merge ? 1u : 0u;
+  for (uint32_t q = lane + skip; q < nr; q += 32) out_cig[o + nl + q - skip] = cig[(uint64_t)rr.cigar_off + q];
+  if (lane == 0) {
+    fz_alignment a;
+    a.score = (hr ? rr.score : 0) + (hl ? rl.score : 0);
+    a.cigar_len = total;
+    a.t_start = sd.t_pos - (uint64_t)(hl ? rl.t_end : 0);
+    a.q_start = sd.q_pos - (uint64_t)(hl ? rl.q_end : 0);
+    a.t_end = sd.t_pos + (uint64_t)(hr ? rr.t_end : 0);
+    a.q_end = sd.q_pos + (uint64_t)(hr ? rr.q_end : 0);
+    a.cigar_off = o;
+    aln[k] = a;
+  }
+}
+
 // Blocks [0, long_blocks): one warp per item of [exec_begin, exec_split), the
 // long walks (the executor list holds the largest bins first).  The other
 // blocks: one thread per item of [exec_split, exec_end).
@@ -587,6 +639,19 @@ cudaError_t launch_cig_pack(fz_result* out, uint32_t n, const uint64_t* poff, co
                             cudaStream_t st) {
   const uint64_t threads = (uint64_t)n * 32;
   if (n) k_cig_pack<<<(uint32_t)((threads + TB - 1) / TB), TB, 0, st>>>(out, n, poff, src, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_comb_lens(const fz_result* res, uint32_t n_seeds, const uint32_t* cig, uint64_t* lens,
+                             cudaStream_t st) {
+  if (n_seeds) k_comb_lens<<<(n_seeds + TB - 1) / TB, TB, 0, st>>>(res, n_seeds, cig, lens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_comb(const fz_seed* seeds, uint32_t n_seeds, const fz_result* res, const uint32_t* cig,
+                        const uint64_t* off, uint32_t* out_cig, fz_alignment* aln, cudaStream_t st) {
+  const uint64_t threads = (uint64_t)n_seeds * 32;
+  if (n_seeds) k_comb<<<(uint32_t)((threads + TB - 1) / TB), TB, 0, st>>>(seeds, n_seeds, res, cig, off, out_cig, aln);
   return cudaGetLastError();
 }
 

@@ -21,11 +21,16 @@ FZ_FLAG_DONE, FZ_FLAG_EAGER, FZ_FLAG_WIDE = 1, 2, 4
 FZ_FLAG_BIN_SHIFT = 4
 
 SYMBOLS = ("fz_create", "fz_extend_batch", "fz_extend_batch_host", "fz_get_stats", "fz_set_profiling",
-           "fz_last_error", "fz_destroy", "fz_bench_int_rates", "fz_local_fill_noalloc")
+           "fz_last_error", "fz_destroy", "fz_bench_int_rates", "fz_local_fill_noalloc", "fz_combine")
 
 RESULT_DTYPE = np.dtype([("score", "<i4"), ("t_end", "<i4"), ("q_end", "<i4"), ("cigar_off", "<u4"),
                          ("cigar_len", "<u4"), ("flags", "<u4")])
 assert RESULT_DTYPE.itemsize == 24
+
+
+ALIGNMENT_DTYPE = np.dtype([("score", "<i4"), ("cigar_len", "<u4"), ("t_start", "<u8"), ("q_start", "<u8"),
+                            ("t_end", "<u8"), ("q_end", "<u8"), ("cigar_off", "<u8")])
+assert ALIGNMENT_DTYPE.itemsize == 48
 
 
 class FzStats(ctypes.Structure):
@@ -77,6 +82,8 @@ def load(path: str | None = None, build_if_missing: bool = False):
     L.fz_local_fill_noalloc.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32,
                                         ctypes.c_int32, u8p, u64p, u8p, u64p, vp, ctypes.c_uint32, vp, vp]
     L.fz_local_fill_noalloc.restype = ctypes.c_int
+    L.fz_combine.argtypes = [vp, vp, ctypes.c_uint32, vp, vp, vp, ctypes.POINTER(ctypes.c_void_p), vp]
+    L.fz_combine.restype = ctypes.c_int
     L.fz_bench_int_rates.argtypes = [ctypes.POINTER(ctypes.c_double)]
     L.fz_bench_int_rates.restype = ctypes.c_int
     _lib = L
@@ -146,6 +153,13 @@ def fz_local_fill_noalloc(sub, gap_open: int, gap_extend: int, max_len: int, d_t
     arr = (ctypes.c_int32 * 16)(*[int(x) for x in np.asarray(sub, np.int64).reshape(16)])
     _check(None, load().fz_local_fill_noalloc(arr, gap_open, gap_extend, max_len, d_target2, t_len, d_query2,
                                               q_len, d_seeds, n_seeds, d_out, stream))
+
+
+def fz_combine(ctx, d_seeds: int, n_seeds: int, d_res: int, d_cigar: int, d_aln: int, stream: int = 0) -> int:
+    """Two-sided alignments; returns the device address of the combined CIGAR arena."""
+    cig = ctypes.c_void_p()
+    _check(ctx, load().fz_combine(ctx, d_seeds, n_seeds, d_res, d_cigar or None, d_aln, ctypes.byref(cig), stream))
+    return cig.value or 0
 
 
 def fz_bench_int_rates():
@@ -234,6 +248,26 @@ class Extender:
         d_out = self.alloc_out(len(seeds))
         cp = self.run(d_t, w.target.size, d_q, w.query.size, d_s, len(seeds), d_out)
         return self.fetch(d_out, len(seeds), cp)
+
+    def extend_and_combine(self, w, seeds=None):
+        """Whole workload, then fz_combine; returns (alignments, combined cigar)."""
+        from .workloads import pack2
+        seeds = w.seeds if seeds is None else seeds
+        t = self.torch
+        d_t, d_q, d_s = self.upload(pack2(w.target), pack2(w.query), seeds)
+        d_out = self.alloc_out(len(seeds))
+        cp = self.run(d_t, w.target.size, d_q, w.query.size, d_s, len(seeds), d_out)
+        d_aln = t.empty(max(1, len(seeds) * ALIGNMENT_DTYPE.itemsize), dtype=t.uint8, device=self.device)
+        st = t.cuda.current_stream(self.device).cuda_stream
+        acp = fz_combine(self.ctx, d_s.data_ptr(), len(seeds), d_out.data_ptr(), cp, d_aln.data_ptr(), st)
+        aln = np.frombuffer(d_aln[:len(seeds) * ALIGNMENT_DTYPE.itemsize].cpu().numpy().tobytes(),
+                            dtype=ALIGNMENT_DTYPE)
+        n = int(aln["cigar_off"][-1] + aln["cigar_len"][-1]) if len(seeds) else 0
+        if n and acp:
+            cig = t.as_tensor(_DevArray(acp, n, "<u4"), device=self.device).cpu().numpy().copy()
+        else:
+            cig = np.zeros(0, np.uint32)
+        return aln, cig
 
     def extend_workload_host(self, w, seeds=None, cigar_cap=None):
         from .workloads import pack2

@@ -145,6 +145,42 @@ fz_status fz_extend_batch_host(fz_ctx* ctx, const uint8_t* h_target2, uint64_t t
                                uint32_t n_seeds, fz_result* h_out, uint32_t* h_cigar,
                                uint64_t cigar_cap, uint64_t* cigar_used, void* cuda_stream);
 
+/* One two-sided alignment per seed (fz_combine). */
+typedef struct {
+    int32_t score;          /* right score + left score */
+    uint32_t cigar_len;     /* runs in the combined CIGAR */
+    uint64_t t_start, q_start;   /* first aligned base: t_pos - left t_end, q_pos - left q_end */
+    uint64_t t_end, q_end;       /* one past the last: t_pos + right t_end, q_pos + right q_end */
+    uint64_t cigar_off;     /* first run in the combined CIGAR arena */
+} fz_alignment;             /* 48 bytes */
+
+/*
+ * Combine the two one-sided results of every seed into one alignment (FastZ,
+ * section 3.1.2: LASTZ joins the left and right extensions of a seed before it
+ * filters the alignments).  The pages give no formula; this is the plain one:
+ *   score = right score + left score (the anchor is a point between the two
+ *           windows and scores nothing);
+ *   span  = [t_pos - left t_end, t_pos + right t_end) and the same on the query;
+ *   CIGAR = the left side's runs, then the right side's, both in forward genomic
+ *           order, with the two runs that meet at the anchor merged into one
+ *           when they are the same operation.
+ * A side that was not requested (or is empty) contributes score 0, no bases and
+ * no runs.
+ * d_seeds: the n_seeds anchors given to fz_extend_batch; d_res: its 2*n_seeds
+ * results; d_cigar: its CIGAR arena (device memory, caller- or context-owned,
+ * unchanged; required for an EXTEND context, may be NULL for a LOCAL one,
+ * whose results have no runs).  d_aln: n_seeds records (device, caller-owned).  *d_aln_cigar
+ * receives the device address of the context-owned combined CIGAR arena,
+ * packed in seed order and valid until the next fz_combine or fz_extend_batch
+ * on this context, or fz_destroy.  Reads 8 bytes back to size that arena (so
+ * it synchronises with cuda_stream once); the rest is asynchronous.
+ * Errors: FZ_ERR_ARG for a NULL context or NULL pointers with n_seeds > 0.
+ * Device memory: the combined arena grows as needed (FZ_ERR_OOM if it cannot).
+ */
+fz_status fz_combine(fz_ctx* ctx, const fz_seed* d_seeds, uint32_t n_seeds, const fz_result* d_res,
+                     const uint32_t* d_cigar, fz_alignment* d_aln, const uint32_t** d_aln_cigar,
+                     void* cuda_stream);
+
 /* Counters of the last completed batch (synchronises the context's last stream). */
 fz_status fz_get_stats(fz_ctx* ctx, fz_stats* out);
 

@@ -166,3 +166,34 @@ def genomic_cigar(runs, left: bool):
     reversed for the left side (its window is read backwards)."""
     runs = np.asarray(runs, np.uint32)
     return runs[::-1].copy() if left else runs.copy()
+
+
+def combine(seeds, res, cigar, cig_off):
+    """Two-sided alignment per seed from the oracle's one-sided results (FastZ,
+    section 3.1.2: LASTZ joins the two extensions of a seed).  Plain definition:
+    score = right score + left score; target span [t_pos - left i*, t_pos +
+    right i*), query span [q_pos - left j*, q_pos + right j*); CIGAR = the left
+    runs then the right runs, both in forward genomic order, the two runs that
+    meet at the anchor merged into one when they are the same operation.  A side
+    that was not requested contributes nothing.
+
+    Returns a list of (score, t_start, q_start, t_end, q_end, runs[np.uint32])."""
+    out = []
+    for k in range(len(seeds)):
+        side = int(seeds["side"][k])
+        tp, qp = int(seeds["t_pos"][k]), int(seeds["q_pos"][k])
+        xr, xl = 2 * k, 2 * k + 1
+        hr, hl = bool(side & 1), bool(side & 2)
+        right = [int(v) for v in cigar[cig_off[xr]:cig_off[xr] + res["n_cigar"][xr]]] if hr else []
+        left = [int(v) for v in genomic_cigar(cigar[cig_off[xl]:cig_off[xl] + res["n_cigar"][xl]], True)] if hl else []
+        runs = list(left)
+        if runs and right and (runs[-1] & 15) == (right[0] & 15):
+            runs[-1] += right[0] & ~15
+            right = right[1:]
+        runs += right
+        score = (int(res["score"][xr]) if hr else 0) + (int(res["score"][xl]) if hl else 0)
+        out.append((score,
+                    tp - (int(res["i_end"][xl]) if hl else 0), qp - (int(res["j_end"][xl]) if hl else 0),
+                    tp + (int(res["i_end"][xr]) if hr else 0), qp + (int(res["j_end"][xr]) if hr else 0),
+                    np.asarray(runs, np.uint32)))
+    return out

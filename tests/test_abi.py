@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     assert {"fz_create", "fz_extend_batch", "fz_destroy", "fz_extend_batch_host", "fz_get_stats",
-            "fz_last_error", "fz_set_profiling", "fz_bench_int_rates", "fz_local_fill_noalloc"} <= set(names)
+            "fz_last_error", "fz_set_profiling", "fz_bench_int_rates", "fz_local_fill_noalloc",
+            "fz_combine"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -44,6 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_layouts_match_header():
     assert W.SEED_DTYPE.itemsize == 24
     assert fz.RESULT_DTYPE.itemsize == 24
+    assert fz.ALIGNMENT_DTYPE.itemsize == 48
     assert ctypes.sizeof(fz.FzStats) == 8 + 8 + 4 + 20 + 4 + 4 + 8 + 8 + 4 + 4 + 24
 
 
@@ -90,3 +92,7 @@ def test_no_cpu_fallback_in_product_path():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_combine_rejects_null_context_without_gpu(lib):
+    assert lib.fz_combine(None, None, 0, None, None, None, None, None) == fz.FZ_ERR_ARG

@@ -302,6 +302,32 @@ def test_checkpoints_long_alignments(monkeypatch):
     _check(w, w.seeds[idx], label="long-60kbp, checkpoint every 64")
 
 
+def test_two_sided_combination():
+    """fz_combine on two-sided anchors of the chromosome workload against the
+    oracle's combination of its one-sided results."""
+    import oracle
+    from gapped_smith_waterman_gb300 import fz
+    w = G.workload(3)
+    idx = G.sample_seeds(w, 300, seed=21)
+    seeds = w.seeds[idx]
+    ext = fz.Extender.for_workload(w)
+    try:
+        aln, cig = ext.extend_and_combine(w, seeds)
+    finally:
+        ext.close()
+    ores, ocig, ooff = G.oracle_run(w, seeds)
+    exp = oracle.combine(seeds, ores, ocig, ooff)
+    assert len(aln) == len(exp)
+    for k, (score, ts, qs, te, qe, runs) in enumerate(exp):
+        a = aln[k]
+        assert (int(a["score"]), int(a["t_start"]), int(a["q_start"]), int(a["t_end"]), int(a["q_end"])) == \
+            (score, ts, qs, te, qe), k
+        got = cig[int(a["cigar_off"]):int(a["cigar_off"]) + int(a["cigar_len"])]
+        assert np.array_equal(got, runs), k
+    # packed in seed order
+    assert np.array_equal(aln["cigar_off"][1:], (aln["cigar_off"] + aln["cigar_len"])[:-1])
+
+
 def test_chunked_executor(monkeypatch):
     w = G.workload(1)
     a, acig, sa = G.gpu_run(w)

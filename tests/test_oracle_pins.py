@@ -306,3 +306,64 @@ def test_end_cell_tie_on_one_antidiagonal(oracle_lib):
     # mirrored: t = CA, q = AC -> cells (1,2) and (2,1) again
     s, i, j, _, _, _ = oracle_lib.extend_one(enc("GAC"), enc("GCA"), sub, 1, 1, -1)
     assert (s, i, j) == (8, 2, 3)
+
+
+# ---- two-sided combination (FastZ, section 3.1.2: LASTZ joins the two sides) ----
+
+def _pair_workload(t, q, seeds, max_len=200):
+    return W.Workload("pair", np.asarray(t, np.uint8), np.asarray(q, np.uint8), seeds,
+                      np.asarray(W.HOXD70, np.int32), 400, 30, 9400, max_len, W.MODE_EXTEND)
+
+
+def _cigar_str(runs):
+    return "".join(f"{int(r) >> 4}{'MID'[int(r) & 15]}" for r in runs)
+
+
+def test_combine_identical_region_is_one_match_run(oracle_lib):
+    """A seed inside an identical region: the two sides meet at the anchor, so
+    the combined alignment is the whole region, one M run, scoring the sum of
+    the diagonal terms."""
+    import oracle
+    rng = np.random.default_rng(11)
+    t = rng.integers(0, 4, 40).astype(np.uint8)
+    sub = np.asarray(W.HOXD70, np.int64).reshape(4, 4)
+    seeds = np.zeros(1, W.SEED_DTYPE)
+    seeds["t_pos"], seeds["q_pos"], seeds["side"] = 15, 15, W.SIDE_BOTH
+    w = _pair_workload(t, t.copy(), seeds)
+    res, cig, off = oracle.extend_batch(w)
+    (score, ts, qs, te, qe, runs), = oracle.combine(seeds, res, cig, off)
+    assert score == int(sum(sub[a, a] for a in t))
+    assert (ts, qs, te, qe) == (0, 0, 40, 40)
+    assert _cigar_str(runs) == "40M"
+
+
+def test_combine_gap_on_the_left_side(oracle_lib):
+    """A 3-base deletion 10 bases left of the anchor: the left side carries it,
+    the right side is all matches, and the runs join as 10M 3D (10+20)M."""
+    import oracle
+    rng = np.random.default_rng(12)
+    q = rng.integers(0, 4, 40).astype(np.uint8)
+    t = np.concatenate([q[:10], rng.integers(0, 4, 3).astype(np.uint8), q[10:]])   # 3 extra target bases
+    sub = np.asarray(W.HOXD70, np.int64).reshape(4, 4)
+    seeds = np.zeros(1, W.SEED_DTYPE)
+    seeds["t_pos"], seeds["q_pos"], seeds["side"] = 23, 20, W.SIDE_BOTH   # anchor after 20 query bases
+    w = _pair_workload(t, q, seeds)
+    res, cig, off = oracle.extend_batch(w)
+    (score, ts, qs, te, qe, runs), = oracle.combine(seeds, res, cig, off)
+    assert _cigar_str(runs) == "10M3D30M"
+    assert (ts, qs, te, qe) == (0, 0, 43, 40)
+    assert score == int(sum(sub[a, a] for a in q)) - (400 + 3 * 30)
+
+
+def test_combine_one_side_only(oracle_lib):
+    import oracle
+    rng = np.random.default_rng(13)
+    t = rng.integers(0, 4, 30).astype(np.uint8)
+    seeds = np.zeros(2, W.SEED_DTYPE)
+    seeds["t_pos"], seeds["q_pos"] = 10, 10
+    seeds["side"] = [W.SIDE_RIGHT, W.SIDE_LEFT]
+    w = _pair_workload(t, t.copy(), seeds)
+    res, cig, off = oracle.extend_batch(w)
+    right, left = oracle.combine(seeds, res, cig, off)
+    assert (right[0], right[1], right[3], _cigar_str(right[5])) == (int(res["score"][0]), 10, 30, "20M")
+    assert (left[0], left[1], left[3], _cigar_str(left[5])) == (int(res["score"][3]), 0, 10, "10M")
