@@ -436,6 +436,17 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     ctx->max_sub = std::max(ctx->max_sub, sub[k]);
   }
   ctx->fast_ok = bytes;
+  {
+    // 16-bit pair sweep: stored values (relative to the threshold - 2048) stay
+    // below ydrop + 2048 + 2 max|sub| and a dead cell must stay below the
+    // threshold after adding o + e + max sub
+    int64_t smax = 0;
+    for (int k = 0; k < 16; ++k) smax = std::max<int64_t>(smax, std::llabs((long long)sub[k]));
+    const int64_t oe = (int64_t)gap_open + gap_extend;
+    const char* nop = getenv("FZ_NO_PAIR");
+    p.pair_ok = (bytes && ydrop != FZ_YDROP_INF && (int64_t)ydrop + 2048 + 4 * (oe + smax) <= 30000 &&
+                 oe + smax + 16 < 2048 && !(nop && *nop && *nop != '0')) ? 1 : 0;
+  }
   for (int t = 0; t < 4; ++t) {
     uint32_t row = 0, col = 0;
     for (int q = 0; q < 4; ++q) {
@@ -443,6 +454,9 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
       col |= (uint32_t)((bytes ? sub[q * 4 + t] : 0) + 128) << (8 * q);
     }
     p.mrow[t] = row;
+    uint32_t row16 = 0;
+    for (int q = 0; q < 4; ++q) row16 |= (uint32_t)((bytes ? sub[t * 4 + q] : 0) & 0xff) << (8 * q);
+    p.mrow16[t] = row16;
     ctx->mcol[t] = col;
   }
   for (int tier = 0; tier < 2; ++tier) {

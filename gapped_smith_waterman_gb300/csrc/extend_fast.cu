@@ -880,6 +880,347 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
   }
 }
 
+// ---- 16-bit pair sweep: the first tier when scores fit (Params::pair_ok) ----
+//
+// The same 384-row window and steps as run_inspect<12>, with two rows in each
+// 32-bit register as 16-bit values, so that every DPX instruction (the s16x2
+// forms) advances two cells.  Values are stored relative to a base
+// B = T - PMG, T being the prune threshold of the anti-diagonal being
+// computed, and clamped at 0 (the relu forms):
+//   * a live cell has S >= T, so its stored h = S - o - e - B >= PMG - o - e;
+//     a pruned cell stores 0;
+//   * any value below T acts like a dead one: a live cell's maximum comes from
+//     a term at or above T, and a term of 0 (or a clamped one) stays below
+//     T - (o + e + max M) > 0, so a dead cell never makes a later one live;
+//   * when the best score rises, T rises by the same amount and every stored
+//     value moves down by it (clamped at 0).
+// Stored values stay below ydrop + PMG + 2 max|M| < 2^15 (checked when the
+// context is created).  Results, live counts and checkpoints are those of the
+// 32-bit sweep: checkpoints are written in its layout, so the 512-row tier and
+// the executor resume from them unchanged.
+constexpr int PK = K_TIER0 / 2;   // register pairs per lane (12 rows)
+constexpr int32_t PMG = 2048;
+
+struct PairState {
+  uint32_t H[PK];     // h = S - o - e, rows 2p (low half) and 2p+1 (high half)
+  uint32_t HP[PK];    // h of the previous anti-diagonal + (o + e): the diagonal source
+  uint32_t I[PK], D[PK];
+  uint32_t MR[2 * PK];  // substitution row of each row's target base (signed bytes)
+  uint32_t SEL[PK];     // byte-permute selector: sign-extended scores of both rows' query bases
+};
+
+// Selector bytes of a row's query base q: as the low row of a pair (bytes q
+// and sign of byte q) and as the high row (bytes 4+q and its sign).
+__device__ __forceinline__ uint32_t sel_lo(uint32_t q) { return 0x80u + 17u * q; }
+__device__ __forceinline__ uint32_t sel_hi(uint32_t q) { return 0xc4u + 17u * q; }
+
+__device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xffffu; }
+__device__ __forceinline__ uint32_t hi16(uint32_t x) { return x >> 16; }
+__device__ __forceinline__ uint32_t dup16(int32_t v) { return ((uint32_t)v & 0xffffu) * 0x10001u; }
+
+// One step of the pair sweep; returns the pair-wise max of the new h (both
+// halves); dead2 accumulates -1 per pruned cell in each half.
+template <bool SHIFT, bool EDGE>
+__device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t noe2, uint32_t oe2, uint32_t th2,
+                                          int lane, uint32_t qb, uint32_t mr_new, int32_t vlo, int32_t vhi,
+                                          uint32_t& dead2) {
+  uint32_t lm2 = 0;
+  if (!SHIFT) {
+    // the row above this lane's row 0 is row 11 of lane l-1 (pair 5, high half)
+    uint32_t hu = __shfl_up_sync(FULL, L.H[PK - 1], 1);
+    uint32_t du = __shfl_up_sync(FULL, L.D[PK - 1], 1);
+    uint32_t pu = __shfl_up_sync(FULL, L.HP[PK - 1], 1);
+    uint32_t su = __shfl_up_sync(FULL, L.SEL[PK - 1], 1);
+    if (lane == 0) { hu = 0u; du = 0u; pu = oe2; su = sel_hi(qb) << 8; }   // above row b: nothing; its new column
+#pragma unroll
+    for (int p = PK - 1; p >= 0; --p) {
+      const uint32_t hs = __funnelshift_r(p ? L.H[p - 1] : hu, L.H[p], 16);    // rows 2p-1, 2p
+      const uint32_t ds = __funnelshift_r(p ? L.D[p - 1] : du, L.D[p], 16);
+      const uint32_t ps = __funnelshift_r(p ? L.HP[p - 1] : pu, L.HP[p], 16);
+      const uint32_t sel = prmt(p ? L.SEL[p - 1] : su, L.SEL[p], 0x0041u) + 0x43bcu;   // queries move down a row
+      const uint32_t ic = __viaddmax_s16x2_relu(L.I[p], ne2, L.H[p]);
+      const uint32_t dc = __viaddmax_s16x2_relu(ds, ne2, hs);
+      const uint32_t g = __vadd2(ps, prmt(L.MR[2 * p], L.MR[2 * p + 1], sel));
+      const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
+      const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
+      uint32_t dead = prmt(__vsub2(hn, th2), 0u, 0xbb99u);                   // 0xffff where h < threshold
+      if (EDGE) {
+        dead |= (2 * p >= vlo && 2 * p <= vhi) ? 0u : 0xffffu;
+        dead |= (2 * p + 1 >= vlo && 2 * p + 1 <= vhi) ? 0u : 0xffff0000u;
+      }
+      const uint32_t h = hn & ~dead;
+      L.HP[p] = __vadd2(L.H[p], oe2);
+      L.H[p] = h;
+      L.I[p] = ic;
+      L.D[p] = dc;
+      L.SEL[p] = sel;
+      dead2 = __vadd2(dead2, dead);
+      lm2 = __vmaxs2(lm2, h);
+    }
+  } else {
+    // the base moves up a row: this lane's row 11 becomes row 0 of lane l+1's old rows
+    uint32_t hd = __shfl_down_sync(FULL, L.H[0], 1);
+    uint32_t id = __shfl_down_sync(FULL, L.I[0], 1);
+    uint32_t md = __shfl_down_sync(FULL, L.MR[0], 1);
+    if (lane == 31) { hd = 0u; id = 0u; md = mr_new; }
+#pragma unroll
+    for (int r = 0; r < 2 * PK - 1; ++r) L.MR[r] = L.MR[r + 1];
+    L.MR[2 * PK - 1] = md;
+#pragma unroll
+    for (int p = 0; p < PK; ++p) {
+      const uint32_t hu = __funnelshift_r(L.H[p], p < PK - 1 ? L.H[p + 1] : hd, 16);   // rows 2p+1, 2p+2 (own rows)
+      const uint32_t iu = __funnelshift_r(L.I[p], p < PK - 1 ? L.I[p + 1] : id, 16);
+      const uint32_t ic = __viaddmax_s16x2_relu(iu, ne2, hu);
+      const uint32_t dc = __viaddmax_s16x2_relu(L.D[p], ne2, L.H[p]);
+      const uint32_t g = __vadd2(L.HP[p], prmt(L.MR[2 * p], L.MR[2 * p + 1], L.SEL[p]));
+      const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
+      const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
+      uint32_t dead = prmt(__vsub2(hn, th2), 0u, 0xbb99u);
+      if (EDGE) {
+        dead |= (2 * p >= vlo && 2 * p <= vhi) ? 0u : 0xffffu;
+        dead |= (2 * p + 1 >= vlo && 2 * p + 1 <= vhi) ? 0u : 0xffff0000u;
+      }
+      const uint32_t h = hn & ~dead;
+      L.HP[p] = __vadd2(hu, oe2);
+      L.H[p] = h;
+      L.I[p] = ic;
+      L.D[p] = dc;
+      dead2 = __vadd2(dead2, dead);
+      lm2 = __vmaxs2(lm2, h);
+    }
+  }
+  return lm2;
+}
+
+// Checkpoint of the pair sweep after anti-diagonal d, in the 32-bit layout
+// (rows u = 12 lane + r): h and I, D back in score space, dead as NEG.
+__device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const PairState& L, int lane, uint32_t head,
+                                                  const CkScalars& cs, int32_t B, int32_t oe, uint32_t cnt,
+                                                  uint32_t cnt_hi, const int32_t* sT) {
+  uint32_t slot = 0;
+  if (lane == 0) slot = atomicAdd(wa.ckpt_used, 1u);
+  slot = __shfl_sync(FULL, slot, 0);
+  if (slot >= wa.ckpt_cap) return head;
+  int32_t* c = wa.ckpt + (uint64_t)slot * CK_SLOT_WORDS;
+  const int32_t c1 = oe - 128;
+#pragma unroll
+  for (int r = 0; r < 2 * PK; ++r) {
+    const uint32_t h = (r & 1) ? hi16(L.H[r >> 1]) : lo16(L.H[r >> 1]);
+    const uint32_t hp = (r & 1) ? hi16(L.HP[r >> 1]) : lo16(L.HP[r >> 1]);
+    const uint32_t iv = (r & 1) ? hi16(L.I[r >> 1]) : lo16(L.I[r >> 1]);
+    const uint32_t dv = (r & 1) ? hi16(L.D[r >> 1]) : lo16(L.D[r >> 1]);
+    c[CK_HDR + r * 32 + lane] = h ? (int32_t)h + B : NEG;
+    c[CK_HDR + CK_WIN_MAX + r * 32 + lane] = ((int32_t)hp > oe ? (int32_t)hp - oe + B : NEG) + c1;
+    c[CK_HDR + 2 * CK_WIN_MAX + r * 32 + lane] = iv ? (int32_t)iv + B : NEG;
+    c[CK_HDR + 3 * CK_WIN_MAX + r * 32 + lane] = dv ? (int32_t)dv + B : NEG;
+  }
+  c[CK_T + lane] = sT[lane];
+  c[CK_CNT + lane] = (int32_t)cnt;
+  if (lane == 0) {
+    c[CK_T + 32] = sT[32];
+    c[CK_D] = cs.d; c[CK_B] = cs.b; c[CK_K] = 2 * PK; c[CK_BEST] = cs.best; c[CK_BI] = cs.bi; c[CK_BJ] = cs.bj;
+    c[CK_DLAST] = cs.d_last; c[CK_FLAGS] = 0; c[CK_PREV] = (int32_t)head;
+    c[CK_CNT_HI] = (int32_t)cnt_hi;
+  }
+  return slot + 1;
+}
+
+__device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t ext, int lane, int32_t* sT,
+                                 uint8_t* tile, const uint32_t* s_mrow16, const int32_t* s_sub) {
+  constexpr int32_t WIN = 64 * PK;
+  const Window w = make_window(p, ext);
+  ExtRec* R = wa.rec + ext;
+  if (!w.requested) {
+    if (lane == 0) {
+      ExtRec z = {};
+      *R = z;
+    }
+    return;
+  }
+  const int32_t m = w.m, n = w.n, oe = p.oe, mn = w.m + w.n;
+  int32_t best = 0, bi = 0, bj = 0, d_last = 0, b = 0, d = 0;
+  int32_t T = threshold(0, p.ydrop);
+  int32_t B = T - PMG;                      // stored value = score-space value - B
+  const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe), th2 = dup16(PMG - oe);
+  PairState L;
+  {
+    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * 2 * PK);
+#pragma unroll
+    for (int r = 0; r < 2 * PK; ++r) L.MR[r] = s_mrow16[(tw >> (2 * r)) & 3u];
+#pragma unroll
+    for (int q = 0; q < PK; ++q) {
+      L.H[q] = 0u; L.HP[q] = oe2; L.I[q] = 0u; L.D[q] = 0u;
+      L.SEL[q] = sel_lo(0) | (sel_hi(0) << 8);
+    }
+    if (lane == 0) L.H[0] = (uint32_t)(-oe - B) & 0xffffu;      // origin: S(0,0) = 0
+  }
+  bool live_prev = true, rowb_alive = true, top = false, top_prev = false;
+  uint32_t dead2 = 0u;                      // pruned cells, per half, since the last flush
+  uint32_t cnt = lane == 0 ? 1u : 0u;       // live cells of this lane (the 32-bit sweep's count)
+  uint32_t head = 0u;
+  sT[lane] = NEG;
+  if (lane == 0) sT[32] = NEG;
+  __syncwarp();
+  Reservoir qr, tr;
+  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);
+  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);
+  const uint32_t ck_mask = wa.ckpt ? (uint32_t)wa.ckpt_every - 1u : 0xffffffffu;
+  int32_t steps = 0;                        // steps since the last count flush
+  bool overflow = false;
+
+  int why = d + 1 > mn ? 2 : 0;
+  if (why == 0) {
+    for (;;) {
+      for (;;) {
+        const int32_t dn = d + 1;
+        const bool shift = !rowb_alive;
+        const int32_t bn = b + (shift ? 1 : 0);
+        const bool edge = bn + WIN - 1 > m || bn < dn - n;
+        const int32_t rowbase = bn + lane * 2 * PK;
+        const int32_t vhi = m - rowbase, vlo = dn - n - rowbase;
+        uint32_t lm2;
+        if (!shift) {
+          const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
+          lm2 = edge ? pstep<false, true>(L, ne2, noe2, oe2, th2, lane, qb, 0u, vlo, vhi, dead2)
+                     : pstep<false, false>(L, ne2, noe2, oe2, th2, lane, qb, 0u, vlo, vhi, dead2);
+        } else {
+          const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+          lm2 = edge ? pstep<true, true>(L, ne2, noe2, oe2, th2, lane, 0u, mr_new, vlo, vhi, dead2)
+                     : pstep<true, false>(L, ne2, noe2, oe2, th2, lane, 0u, mr_new, vlo, vhi, dead2);
+        }
+        const int32_t lm = (int32_t)imax((int32_t)lo16(lm2), (int32_t)hi16(lm2));
+        const int32_t wm = __reduce_max_sync(FULL, lm);           // stored h of the anti-diagonal's best
+        const bool edge_lane = (lane == 0 && lo16(L.H[0]) != 0u) || (lane == 31 && lm != 0);
+        const uint32_t bits = __ballot_sync(FULL, edge_lane);
+        const bool live = wm != 0;
+        ++steps;
+        const int32_t sbest = wm + oe + B;
+        if (live && sbest > best) {
+          int rf = 2 * PK;
+#pragma unroll
+          for (int r = 2 * PK - 1; r >= 0; --r)
+            rf = (int32_t)((r & 1) ? hi16(L.H[r >> 1]) : lo16(L.H[r >> 1])) == wm ? r : rf;
+          const uint32_t fm = __ballot_sync(FULL, rf < 2 * PK);
+          const int Ln = __ffs(fm) - 1;
+          const int rr = __shfl_sync(FULL, rf, Ln);
+          bi = bn + Ln * 2 * PK + rr;
+          bj = dn - bi;
+          best = sbest;
+          if (dn <= 2 * EAGER_N && lane == 0) sT[dn] = best;
+          const int32_t Tn = threshold(best, p.ydrop);
+          const uint32_t dl = dup16(T - Tn);                      // move every value down by the rise
+#pragma unroll
+          for (int q = 0; q < PK; ++q) {
+            L.H[q] = __viaddmax_s16x2_relu(L.H[q], dl, 0u);
+            L.HP[q] = __viaddmax_s16x2_relu(L.HP[q], dl, 0u);
+            L.I[q] = __viaddmax_s16x2_relu(L.I[q], dl, 0u);
+            L.D[q] = __viaddmax_s16x2_relu(L.D[q], dl, 0u);
+          }
+          B += Tn - T;
+          T = Tn;
+        }
+        d_last = live ? dn : d_last;
+        rowb_alive = bits & 1u;
+        top_prev = top && !shift;
+        top = (bits >> 31) != 0u;
+        b = bn;
+        d = dn;
+        if (steps >= 2048) {                                       // fold the 16-bit counters
+          cnt += 2048u * 2 * PK - (uint32_t)(-(int32_t)(int16_t)lo16(dead2) - (int32_t)(int16_t)hi16(dead2));
+          dead2 = 0u;
+          steps = 0;
+        }
+        const bool end_ = (!live && !live_prev) || d + 1 > mn;
+        live_prev = live;
+        const bool ovf = rowb_alive && (top || top_prev) && b + WIN <= m;
+        if (end_ || ovf || ((uint32_t)d & ck_mask) == 0u) {
+          why = end_ ? 2 : (ovf ? 1 : 0);
+          break;
+        }
+      }
+      // bring the live count up to date (checkpoints and the end need it)
+      cnt += (uint32_t)steps * 2 * PK - (uint32_t)(-(int32_t)(int16_t)lo16(dead2) - (int32_t)(int16_t)hi16(dead2));
+      dead2 = 0u;
+      steps = 0;
+      if (why != 0) break;
+      if (d - (bi + bj) <= wa.ckpt_recent) {
+        const CkScalars cs{b, d, best, bi, bj, d_last};
+        head = ck_write_pair(wa, L, lane, head, cs, B, oe, cnt, 0u, sT);
+      }
+    }
+  }
+  if (why == 1) {
+    overflow = true;
+    if (wa.ckpt) {
+      const CkScalars cs{b, d, best, bi, bj, d_last};
+      head = ck_write_pair(wa, L, lane, head, cs, B, oe, cnt, 0u, sT);
+    }
+  }
+
+  uint64_t tot = cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+  if (overflow) {
+    if (lane == 0) {
+      ExtRec z = {};
+      z.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE;
+      z.m = m;
+      z.n = n;
+      z.ckpt = head;
+      *R = z;
+      const uint32_t slot = atomicAdd(wa.ovf_count, 1u);
+      wa.ovf_list[slot] = ext;
+    }
+    return;
+  }
+  uint64_t path = 0;
+  uint32_t npath = 0;
+  uint32_t flags = FZ_FLAG_DONE;
+  uint32_t width = WIN;
+  if (bi <= EAGER_N && bj <= EAGER_N) {
+    flags |= FZ_FLAG_EAGER;
+    width = 0;
+    if (bi + bj > 0) {
+      int32_t v = sT[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) v = imax(v, __shfl_up_sync(FULL, v, o));
+      v = imax(v, 0);
+      __syncwarp();
+      sT[lane + 1] = threshold(v, p.ydrop);
+      __syncwarp();
+      eager_corner(p, w, lane, sT, tile, s_sub, bi, bj, path, npath, wa.err);
+    }
+  }
+  if (lane == 0) {
+    ExtRec o;
+    o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
+    o.live = tot; o.path = path; o.flags = flags; o.npath = npath;
+    o.m = m; o.n = n; o.width = width; o.ckpt = head;
+    *R = o;
+    atomicAdd(wa.live_total, (unsigned long long)tot);
+  }
+}
+
+__global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
+  __shared__ int32_t s_T[WARPS][2 * EAGER_N + 2];
+  __shared__ uint8_t s_tile[WARPS][(EAGER_N + 1) * (EAGER_N + 1)];
+  __shared__ uint32_t s_mrow16[4];
+  __shared__ int32_t s_sub[16];
+  if (threadIdx.x < 4) s_mrow16[threadIdx.x] = p.mrow16[threadIdx.x];
+  if (threadIdx.x < 16) s_sub[threadIdx.x] = p.sub[threadIdx.x];
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (;;) {
+    uint32_t idx = 0;
+    if (lane == 0) idx = atomicAdd(wa.counter, 1u);
+    idx = __shfl_sync(FULL, idx, 0);
+    const uint32_t nw = wa.n_work_dev ? *wa.n_work_dev : wa.n_work;
+    if (idx >= nw) break;
+    const uint32_t ext = wa.list ? wa.list[idx] : idx;
+    run_inspect_pair(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow16, s_sub);
+  }
+}
+
 // MINB: resident blocks per SM the register budget is fitted to.
 template <int K, bool TRACE, int MINB>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_extend(Params p, WorkArgs wa) {
@@ -923,7 +1264,8 @@ constexpr int KA = K_TIER0, KB = K_TIER1;
 int fast_window_rows(int tier) { return 32 * (tier == 0 ? KA : KB); }
 
 cudaError_t launch_inspect_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  if (tier == 0) k_extend<KA, false, 4><<<grid, WARPS * 32, 0, st>>>(p, wa);
+  if (tier == 0 && p.pair_ok) k_pair<<<grid, WARPS * 32, 0, st>>>(p, wa);
+  else if (tier == 0) k_extend<KA, false, 4><<<grid, WARPS * 32, 0, st>>>(p, wa);
   else k_extend<KB, false, 1><<<grid, WARPS * 32, 0, st>>>(p, wa);
   return cudaGetLastError();
 }

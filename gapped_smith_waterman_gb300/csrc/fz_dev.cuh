@@ -38,6 +38,8 @@ struct Params {
   int32_t max_len;
   int32_t one;            // 1, opaque to the compiler (see imad)
   uint32_t mrow[4];       // fast path: byte q of mrow[t] = sub[t][q] + 128
+  uint32_t mrow16[4];     // 16-bit pair path: byte q of mrow16[t] = sub[t][q] (signed)
+  int32_t pair_ok;        // 1: the inspector's first tier keeps two 16-bit rows per register
   int32_t sub[16];
 };
 

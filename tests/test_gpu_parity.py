@@ -302,6 +302,23 @@ def test_checkpoints_long_alignments(monkeypatch):
     _check(w, w.seeds[idx], label="long-60kbp, checkpoint every 64")
 
 
+def test_pair_sweep_equals_32bit_sweep(monkeypatch):
+    """The 16-bit pair sweep (first tier when the y-drop keeps scores within 16
+    bits) and the 32-bit sweep give the same records, CIGARs and live cells;
+    both equal the oracle."""
+    w = G.workload(2)
+    idx = np.arange(2000)
+    a, acig, sa = G.gpu_run(w, w.seeds[idx])
+    monkeypatch.setenv("FZ_NO_PAIR", "1")
+    b, bcig, sb = G.gpu_run(w, w.seeds[idx])
+    monkeypatch.delenv("FZ_NO_PAIR")
+    assert np.array_equal(a, b) and np.array_equal(acig, bcig)
+    assert sa.live_cells == sb.live_cells and sa.exec_cells == sb.exec_cells
+    ores, ocig, ooff = G.oracle_run(w, w.seeds[idx])
+    G.compare(w, w.seeds[idx], a, acig, ores, ocig, ooff, label="pair sweep")
+    assert sa.live_cells == int(ores["live_cells"].sum())
+
+
 def test_two_sided_combination():
     """fz_combine on two-sided anchors of the chromosome workload against the
     oracle's combination of its one-sided results."""
