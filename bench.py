@@ -42,7 +42,8 @@ SMS, SM_MAX_GHZ, CELLS_PER_CLK_SM = 152, 2.07, 16.0
 PEAK_GCUPS = SMS * SM_MAX_GHZ * CELLS_PER_CLK_SM
 # Dominant kernel per mode: (name, source file, committed DRAM-traffic summary).
 DOMINANT = {
-    "extend": ("inspector (register-window sweep)", "extend_fast.cu", "inspector_traffic.json"),
+    "extend": ("inspector (register-window sweep; first tier two 16-bit rows per register)", "extend_fast.cu",
+               "inspector_traffic.json"),
     "local": ("local fill (k_local)", "local.cu", "local_traffic.json"),
 }
 
