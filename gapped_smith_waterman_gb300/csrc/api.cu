@@ -446,6 +446,7 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     const char* nop = getenv("FZ_NO_PAIR");
     p.pair_ok = (bytes && ydrop != FZ_YDROP_INF && (int64_t)ydrop + 2048 + 4 * (oe + smax) <= 30000 &&
                  oe + smax + 16 < 2048 && !(nop && *nop && *nop != '0')) ? 1 : 0;
+    p.pair_slack = p.pair_ok ? (int32_t)std::min<int64_t>(8192, 30000 - ((int64_t)ydrop + 2048 + 4 * (oe + smax))) : 0;
   }
   for (int t = 0; t < 4; ++t) {
     uint32_t row = 0, col = 0;

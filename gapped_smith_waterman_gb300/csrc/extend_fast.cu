@@ -892,10 +892,11 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
 //   * any value below T acts like a dead one: a live cell's maximum comes from
 //     a term at or above T, and a term of 0 (or a clamped one) stays below
 //     T - (o + e + max M) > 0, so a dead cell never makes a later one live;
-//   * when the best score rises, T rises by the same amount and every stored
-//     value moves down by it (clamped at 0).
-// Stored values stay below ydrop + PMG + 2 max|M| < 2^15 (checked when the
-// context is created).  Results, live counts and checkpoints are those of the
+//   * when the best score rises, T rises by the same amount; the rise is kept
+//     in the stored threshold until it passes the slack of the 16-bit range,
+//     then every stored value moves down by it (clamped at 0).
+// Stored values stay below ydrop + PMG + slack + 2 max|M| < 2^15 (checked when
+// the context is created).  Results, live counts and checkpoints are those of the
 // 32-bit sweep: checkpoints are written in its layout, so the 512-row tier and
 // the executor resume from them unchanged.
 constexpr int PK = K_TIER0 / 2;   // register pairs per lane (12 rows)
@@ -1041,7 +1042,12 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   int32_t best = 0, bi = 0, bj = 0, d_last = 0, b = 0, d = 0;
   int32_t T = threshold(0, p.ydrop);
   int32_t B = T - PMG;                      // stored value = score-space value - B
-  const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe), th2 = dup16(PMG - oe);
+  const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe);
+  // A rise of the threshold is first only added to the stored threshold
+  // (pend); the values move down once pend passes the slack that the 16-bit
+  // range leaves (Params::pair_slack).
+  int32_t pend = 0;
+  uint32_t th2 = dup16(PMG - oe);
   PairState L;
   {
     const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * 2 * PK);
@@ -1055,7 +1061,8 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     if (lane == 0) L.H[0] = (uint32_t)(-oe - B) & 0xffffu;      // origin: S(0,0) = 0
   }
   bool live_prev = true, rowb_alive = true, top = false, top_prev = false;
-  uint32_t dead2 = 0u;                      // pruned cells, per half, since the last flush
+  uint32_t dead2 = 0u;                      // pruned cells, per half, since d_fold
+  int32_t d_fold = 0;
   uint32_t cnt = lane == 0 ? 1u : 0u;       // live cells of this lane (the 32-bit sweep's count)
   uint32_t head = 0u;
   sT[lane] = NEG;
@@ -1064,8 +1071,11 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   Reservoir qr, tr;
   res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);
   res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);
+  // the step loop leaves every ex_mask + 1 anti-diagonals (at most 2048, so
+  // that the 16-bit dead counts cannot wrap) to fold the live count and to
+  // write the checkpoints
   const uint32_t ck_mask = wa.ckpt ? (uint32_t)wa.ckpt_every - 1u : 0xffffffffu;
-  int32_t steps = 0;                        // steps since the last count flush
+  const uint32_t ex_mask = (wa.ckpt && wa.ckpt_every <= 2048) ? (uint32_t)wa.ckpt_every - 1u : 2047u;
   bool overflow = false;
 
   int why = d + 1 > mn ? 2 : 0;
@@ -1076,8 +1086,12 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
         const bool shift = !rowb_alive;
         const int32_t bn = b + (shift ? 1 : 0);
         const bool edge = bn + WIN - 1 > m || bn < dn - n;
-        const int32_t rowbase = bn + lane * 2 * PK;
-        const int32_t vhi = m - rowbase, vlo = dn - n - rowbase;
+        int32_t vhi = 0, vlo = 0;
+        if (edge) {
+          const int32_t rowbase = bn + lane * 2 * PK;
+          vhi = m - rowbase;
+          vlo = dn - n - rowbase;
+        }
         uint32_t lm2;
         if (!shift) {
           const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
@@ -1093,7 +1107,6 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
         const bool edge_lane = (lane == 0 && lo16(L.H[0]) != 0u) || (lane == 31 && lm != 0);
         const uint32_t bits = __ballot_sync(FULL, edge_lane);
         const bool live = wm != 0;
-        ++steps;
         const int32_t sbest = wm + oe + B;
         if (live && sbest > best) {
           int rf = 2 * PK;
@@ -1108,16 +1121,21 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
           best = sbest;
           if (dn <= 2 * EAGER_N && lane == 0) sT[dn] = best;
           const int32_t Tn = threshold(best, p.ydrop);
-          const uint32_t dl = dup16(T - Tn);                      // move every value down by the rise
-#pragma unroll
-          for (int q = 0; q < PK; ++q) {
-            L.H[q] = __viaddmax_s16x2_relu(L.H[q], dl, 0u);
-            L.HP[q] = __viaddmax_s16x2_relu(L.HP[q], dl, 0u);
-            L.I[q] = __viaddmax_s16x2_relu(L.I[q], dl, 0u);
-            L.D[q] = __viaddmax_s16x2_relu(L.D[q], dl, 0u);
-          }
-          B += Tn - T;
+          pend += Tn - T;
           T = Tn;
+          if (pend > p.pair_slack) {
+            const uint32_t dl = dup16(-pend);                     // move every value down by the rise
+#pragma unroll
+            for (int q = 0; q < PK; ++q) {
+              L.H[q] = __viaddmax_s16x2_relu(L.H[q], dl, 0u);
+              L.HP[q] = __viaddmax_s16x2_relu(L.HP[q], dl, 0u);
+              L.I[q] = __viaddmax_s16x2_relu(L.I[q], dl, 0u);
+              L.D[q] = __viaddmax_s16x2_relu(L.D[q], dl, 0u);
+            }
+            B += pend;
+            pend = 0;
+          }
+          th2 = dup16(PMG - oe + pend);
         }
         d_last = live ? dn : d_last;
         rowb_alive = bits & 1u;
@@ -1125,25 +1143,20 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
         top = (bits >> 31) != 0u;
         b = bn;
         d = dn;
-        if (steps >= 2048) {                                       // fold the 16-bit counters
-          cnt += 2048u * 2 * PK - (uint32_t)(-(int32_t)(int16_t)lo16(dead2) - (int32_t)(int16_t)hi16(dead2));
-          dead2 = 0u;
-          steps = 0;
-        }
         const bool end_ = (!live && !live_prev) || d + 1 > mn;
         live_prev = live;
         const bool ovf = rowb_alive && (top || top_prev) && b + WIN <= m;
-        if (end_ || ovf || ((uint32_t)d & ck_mask) == 0u) {
+        if (end_ || ovf || ((uint32_t)d & ex_mask) == 0u) {
           why = end_ ? 2 : (ovf ? 1 : 0);
           break;
         }
       }
       // bring the live count up to date (checkpoints and the end need it)
-      cnt += (uint32_t)steps * 2 * PK - (uint32_t)(-(int32_t)(int16_t)lo16(dead2) - (int32_t)(int16_t)hi16(dead2));
+      cnt += (uint32_t)(d - d_fold) * 2 * PK - (uint32_t)(-(int32_t)(int16_t)lo16(dead2) - (int32_t)(int16_t)hi16(dead2));
       dead2 = 0u;
-      steps = 0;
+      d_fold = d;
       if (why != 0) break;
-      if (d - (bi + bj) <= wa.ckpt_recent) {
+      if (((uint32_t)d & ck_mask) == 0u && d - (bi + bj) <= wa.ckpt_recent) {
         const CkScalars cs{b, d, best, bi, bj, d_last};
         head = ck_write_pair(wa, L, lane, head, cs, B, oe, cnt, 0u, sT);
       }

@@ -40,6 +40,7 @@ struct Params {
   uint32_t mrow[4];       // fast path: byte q of mrow[t] = sub[t][q] + 128
   uint32_t mrow16[4];     // 16-bit pair path: byte q of mrow16[t] = sub[t][q] (signed)
   int32_t pair_ok;        // 1: the inspector's first tier keeps two 16-bit rows per register
+  int32_t pair_slack;     // pair sweep: threshold rise kept before the stored values move
   int32_t sub[16];
 };
 
