@@ -319,6 +319,27 @@ def test_pair_sweep_equals_32bit_sweep(monkeypatch):
     assert sa.live_cells == int(ores["live_cells"].sum())
 
 
+@pytest.mark.parametrize("ydrop", [20000, 20252])
+def test_pair_sweep_at_its_range_limit(ydrop, monkeypatch):
+    """The 16-bit pair sweep at the largest y-drops it takes with HOXD70 and
+    o = 1500, e = 300 (ydrop + 2048 + 4 (o + e + max|M|) <= 30000; steep gaps keep
+    the band inside the 384-row window): little or no slack, so the stored
+    values move at nearly every rise of the best score, and live values reach
+    the top of the 16-bit range.  Long high-identity pairs drive scores far
+    from 0; both sweeps and the oracle must agree."""
+    rng = np.random.default_rng(41)
+    pairs = []
+    for _ in range(40):
+        t = rng.integers(0, 4, int(rng.integers(500, 3000))).astype(np.uint8)
+        q = W.mutate(rng, t, rng.uniform(0.0, 0.15), rng.uniform(0.0, 0.02), 3.0)
+        pairs.append((t, q))
+    w, _ = _batch_from_pairs(pairs, o=1500, e=300, ydrop=ydrop)
+    a, acig, st, ores = _check(w, label=f"pair range limit ydrop={ydrop}")
+    monkeypatch.setenv("FZ_NO_PAIR", "1")
+    b, bcig, sb = G.gpu_run(w)
+    assert np.array_equal(a, b) and np.array_equal(acig, bcig) and st.live_cells == sb.live_cells
+
+
 def test_two_sided_combination():
     """fz_combine on two-sided anchors of the chromosome workload against the
     oracle's combination of its one-sided results."""
