@@ -461,8 +461,8 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     ctx->mcol[t] = col;
   }
   for (int tier = 0; tier < 2; ++tier) {
-    ctx->grid_fast[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, false);
-    ctx->grid_fast_trace[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, true);
+    ctx->grid_fast[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, false, p.pair_ok != 0);
+    ctx->grid_fast_trace[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, true, false);
   }
   ctx->grid_wide = ctx->sms;
   ctx->local_smem = local_smem_bytes(max_len);

@@ -1289,9 +1289,11 @@ cudaError_t launch_execute_fast(int tier, const Params& p, const WorkArgs& wa, i
   return cudaGetLastError();
 }
 
-int extend_fast_blocks_per_sm(int tier, bool trace) {
+int extend_fast_blocks_per_sm(int tier, bool trace, bool pair) {
   int nb = 0;
-  if (tier == 0) {
+  if (tier == 0 && !trace && pair) {
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_pair, WARPS * 32, 0);
+  } else if (tier == 0) {
     if (trace) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KA, true, 4>, WARPS * 32, 0);
     else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KA, false, 4>, WARPS * 32, 0);
   } else {

@@ -43,7 +43,7 @@ struct WorkArgs {
 int fast_window_rows(int tier);
 cudaError_t launch_inspect_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
 cudaError_t launch_execute_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
-int extend_fast_blocks_per_sm(int tier, bool trace);
+int extend_fast_blocks_per_sm(int tier, bool trace, bool pair);  // pair: the 16-bit first tier
 
 // general band sweep (extend_wide.cu)
 uint64_t wide_scratch_elems(int32_t max_len);   // per warp
