@@ -432,245 +432,154 @@ __device__ __forceinline__ int ck_stage(Relay<KS>* rb, const int32_t* c, int lan
   return rows;
 }
 
-// Runs one step with ka active slots (ka even, 4 <= ka <= KS) and stores the
-// direction codes of the anti-diagonal in TRACE mode.
-template <int KS, bool TRACE, bool SHIFT, bool EDGE>
-__device__ __forceinline__ int32_t step_any(int ka, LaneState<KS>& L, const StepIn& in, int lane, uint32_t& cnt,
-                                            uint8_t* row) {
-  uint64_t packed = 0;
-  int32_t lm = NEG;
-#define FZ_STEP_CASE(KA_)                                                   \
-  case KA_:                                                                 \
-    if constexpr (KA_ <= KS) {                                              \
-      lm = step<KS, KA_, TRACE, SHIFT, EDGE>(L, in, lane, cnt, packed);     \
-      if (TRACE) store_codes<KA_>(row, lane, packed);                       \
-    }                                                                       \
-    break;
-  switch (ka) {
-    FZ_STEP_CASE(4)
-    FZ_STEP_CASE(6)
-    FZ_STEP_CASE(8)
-    FZ_STEP_CASE(10)
-    FZ_STEP_CASE(12)
-    FZ_STEP_CASE(14)
-    default:
-      if constexpr (KS >= 16) {
-        lm = step<KS, 16, TRACE, SHIFT, EDGE>(L, in, lane, cnt, packed);
-        if (TRACE) store_codes<16>(row, lane, packed);
+// ---- executor: the replay with a lean step loop per window size ----
+//
+// A segment replays the inspector's sweep from the origin or from a
+// checkpoint up to d_stop with KA active rows per lane.  The step loop for one
+// KA carries only what the replay needs: the threshold (from the best score),
+// row b's liveness (shift test) and the top lane's (growth test); it leaves
+// when the segment ends or when the band may reach past the top of the
+// KA-row window, and the caller re-lays the window out two rows per lane
+// wider.  A window of KS rows per lane never needs to grow: the inspector of
+// this tier swept the extension in it without an overflow, with the same
+// base rows (the shift decisions are the same).
+struct ExecState {
+  int32_t b, d, best, T;
+  bool rowb_alive, top, top_prev;
+  Reservoir qr, tr;
+};
+
+template <int KS, int KA>
+__device__ __forceinline__ bool exec_loop(LaneState<KS>& L, ExecState& s, StepIn& in, const Params& p,
+                                          const Window& w, int lane, const uint32_t* s_mrow, uint8_t* tbase,
+                                          int32_t* lo_arr, int32_t d_stop) {
+  constexpr int32_t WIN = 32 * KA, WMAX = 32 * KS;
+  const int32_t m = w.m, n = w.n;
+  uint32_t no_cnt = 0;
+  for (;;) {
+    if (s.d >= d_stop) return false;
+    const int32_t dn = s.d + 1;
+    const bool shift = !s.rowb_alive;
+    const int32_t bn = s.b + (shift ? 1 : 0);
+    if (KA < KS && !shift && (s.top || s.top_prev) && s.b + WIN <= m) return true;   // grow
+    in.Th = s.T - in.oe;
+    const bool edge = bn + WIN - 1 > m || bn < dn - n;
+    uint64_t packed = 0;
+    int32_t lm;
+    if (!shift) {
+      in.qb = res_take(s.qr, p.q2, p.q_len, w.qg0, w.dir);
+      if (edge) {
+        const int32_t rowbase = bn + lane * KA;
+        in.vhi = m - rowbase;
+        in.vlo = dn - n - rowbase;
+        lm = step<KS, KA, true, false, true>(L, in, lane, no_cnt, packed);
+      } else {
+        lm = step<KS, KA, true, false, false>(L, in, lane, no_cnt, packed);
       }
-      break;
+    } else {
+      in.mr_new = s_mrow[res_take(s.tr, p.t2, p.t_len, w.tg0, w.dir)];
+      if (edge) {
+        const int32_t rowbase = bn + lane * KA;
+        in.vhi = m - rowbase;
+        in.vlo = dn - n - rowbase;
+        lm = step<KS, KA, true, true, true>(L, in, lane, no_cnt, packed);
+      } else {
+        lm = step<KS, KA, true, true, false>(L, in, lane, no_cnt, packed);
+      }
+    }
+    store_codes<KA>(tbase + (uint64_t)dn * (WMAX / 2), lane, packed);
+    const int32_t wm = __reduce_max_sync(FULL, lm);
+    const bool edge_lane = (lane == 0 && L.H[0] >= in.Th) || (lane == 31 && lm >= in.Th);
+    const uint32_t bits = __ballot_sync(FULL, edge_lane);
+    if (wm + in.oe > s.best) {                       // the replay needs only the threshold
+      s.best = wm + in.oe;
+      s.T = threshold(s.best, p.ydrop);
+    }
+    if (lane == 0) lo_arr[dn] = bn;
+    s.rowb_alive = bits & 1u;
+    s.top_prev = s.top && !shift;
+    s.top = (bits >> 31) != 0u;
+    s.b = bn;
+    s.d = dn;
   }
-#undef FZ_STEP_CASE
-  return lm;
 }
 
-// ADAPT: resize the window to the live band (the executor, whose replays are
-// short and spend most steps on a narrow band); without it the window stays at
-// KS rows per lane (the inspector: one step variant keeps its loop small).
-template <int KS, bool TRACE, bool ADAPT>
-__device__ void run_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint4 sg, int lane,
-                        int32_t* sT, uint8_t* tile, const uint32_t* s_mrow, const int32_t* s_sub, Relay<KS>* rb) {
+template <int KS>
+__device__ void run_exec(const Params& p, const WorkArgs& wa, uint32_t ext, uint4 sg, int lane,
+                         const uint32_t* s_mrow, Relay<KS>* rb) {
   static_assert(KS % 2 == 0 && KS <= 16, "one 16-base fetch per lane");
-  constexpr int32_t WMAX = 32 * KS;          // trace row width: the widest window
-  constexpr int32_t NOROW_HI = -0x3fffffff, NOROW_LO = 0x3fffffff;
+  constexpr int32_t WMAX = 32 * KS;
   const Window w = make_window(p, ext);
-  ExtRec* R = wa.rec + ext;
-  if (!w.requested) {
-    if (!TRACE && lane == 0) {
-      ExtRec z = {};
-      *R = z;
-    }
-    return;
-  }
-  const int32_t m = w.m, n = w.n, oe = p.oe;
-  int32_t d_stop = 0x7fffffff;
-  uint8_t* tbase = nullptr;
-  int32_t* lo_arr = nullptr;
-  if (TRACE) {
-    // segment sg: replay from anti-diagonal sg.w (the origin, or checkpoint
-    // sg.y - 1) to sg.z; the rows are laid out for the whole extension
-    const int32_t dstar = R->i_end + R->j_end;
-    d_stop = (int32_t)sg.z;
-    tbase = wa.trace + (wa.trace_off[sg.x] - wa.trace_sub);
-    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(WMAX, dstar));
-    if (lane == 0 && sg.y == 0u) lo_arr[0] = 0;
-  }
-
-  // The window starts with 4 rows per lane (128 rows) and is re-laid out as
-  // the live band grows and shrinks (always an even number of rows per lane).
-  int kact = ADAPT ? 4 : KS;
+  const ExtRec* R = wa.rec + ext;
+  if (!w.requested) return;
+  const int32_t dstar = R->i_end + R->j_end;
+  const int32_t d_stop = (int32_t)sg.z;
+  uint8_t* tbase = wa.trace + (wa.trace_off[sg.x] - wa.trace_sub);
+  int32_t* lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(WMAX, dstar));
+  StepIn in;
+  in.oe = p.oe;
+  in.ne = -p.e;
+  in.c1 = p.oe - 128;
+  in.one = p.one;
+  ExecState s;
   LaneState<KS> L;
-  {
-    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * kact);
+  int ka = 4;
+  if (sg.y == 0u) {
+    // origin: 4 rows per lane to start with
+    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * 4);
 #pragma unroll
     for (int r = 0; r < KS; ++r) {
-      L.MR[r] = s_mrow[r < kact ? (tw >> (2 * r)) & 3u : 0u];
+      L.MR[r] = s_mrow[r < 4 ? (tw >> (2 * r)) & 3u : 0u];
       L.H[r] = NEG; L.HP[r] = NEG; L.I[r] = NEG; L.D[r] = NEG;
     }
 #pragma unroll
     for (int k = 0; k < KS / 2; ++k) L.QP[k] = 0x44404440u;
-    if (lane == 0) L.H[0] = -oe;                       // origin: S(0,0) = 0
-  }
-  Reservoir qr, tr;
-  res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);        // query columns 1, 2, ... entering at row b
-  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, 32 * kact);   // target rows entering at the window top
-
-  StepIn in;
-  in.oe = oe;
-  in.ne = -p.e;
-  in.c1 = oe - 128;
-  in.one = p.one;
-  int32_t T = threshold(0, p.ydrop);
-  int32_t b = 0, d = 0, best = 0, bi = 0, bj = 0, d_last = 0;
-  int32_t hi_c = 0, lo_c = 0, hi_p = NOROW_HI, lo_p = NOROW_LO;   // live row bounds at d and d-1
-  bool live = true, live_prev = false, rowb_alive = true;
-  uint32_t cnt = lane == 0 ? 1u : 0u;
-  bool overflow = false;
-  int cool = 0;
-  // a segment that starts at a checkpoint: its rows go to the relay buffer and
-  // the first step's window sizing loads them (staged)
-  bool staged = false;
-  int rows_staged = 0;
-  if (TRACE && ADAPT && sg.y != 0u) {
+    if (lane == 0) L.H[0] = -p.oe;                   // origin: S(0,0) = 0
+    if (lane == 0) lo_arr[0] = 0;
+    s.b = 0; s.d = 0; s.best = 0;
+    s.rowb_alive = true;
+  } else {
+    // checkpoint: the smallest window (even rows per lane, at least 4) whose
+    // top lane holds no live cell of the last two anti-diagonals
     const int32_t* c = wa.ckpt + (uint64_t)(sg.y - 1u) * CK_SLOT_WORDS;
-    b = c[CK_B]; d = c[CK_D]; best = c[CK_BEST]; d_last = c[CK_DLAST];
-    T = threshold(best, p.ydrop);
-    rows_staged = ck_stage<KS>(rb, c, lane, p, w, hi_c, lo_c, hi_p, lo_p);
-    live = hi_c != NOROW_HI;
-    live_prev = hi_p != NOROW_HI;
-    rowb_alive = lo_c == b;
-    staged = true;
-    cool = 0;
-    res_init(qr, p.q2, p.q_len, w.qg0, w.dir, (int64_t)d + 1 - b);
+    int32_t hi_c, lo_c, hi_p, lo_p;
+    const int rows = ck_stage<KS>(rb, c, lane, p, w, hi_c, lo_c, hi_p, lo_p);
+    s.b = c[CK_B]; s.d = c[CK_D]; s.best = c[CK_BEST];
+    const int32_t span = imax(hi_c, hi_p) - s.b;     // highest live row above the base
+    while (ka < KS && 31 * ka <= span) ka += 2;
+    relay_load<KS>(L, rows, ka, s.b, s.d, lane, rb, p, w, s_mrow);
+    s.rowb_alive = lo_c == s.b;
   }
-
+  s.T = threshold(s.best, p.ydrop);
+  s.top = false;
+  s.top_prev = false;
+  res_init(s.qr, p.q2, p.q_len, w.qg0, w.dir, (int64_t)s.d + 1 - s.b);   // query columns entering at row b
+  res_init(s.tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)s.b + 32 * ka);  // target rows entering at the top
   for (;;) {
-    const int32_t dn = d + 1;
-    if (dn > m + n) break;
-    if (TRACE && d >= d_stop) break;
-    const bool shift = !rowb_alive;
-    const int32_t bn = b + (shift ? 1 : 0);
-    const int32_t hi_max = imax(hi_c, hi_p);
-    // rows from the next base to the highest row that may be live
-    const int32_t need = hi_max - bn + 1;
-    if (ADAPT) {
-      int kt = kact;
-      if (need > 29 * kact) {
-        kt = imin(KS, imax(kact + 2, (((need + 64 + 31) >> 5) + 1) & ~1));
-      } else if (cool <= 0 && need + 96 <= 32 * (kact - 2)) {
-        kt = imax(4, (((need + 64 + 31) >> 5) + 1) & ~1);
-      }
-      if (kt != kact || staged) {
-        if (!staged) relay_store<KS>(L, kact, lane, rb, s_mrow);
-        relay_load<KS>(L, staged ? rows_staged : 32 * kact, kt, b, d, lane, rb, p, w, s_mrow);
-        staged = false;
-        kact = kt;
-        res_init(tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)b + 32 * kact);
-        cool = 32;
-      }
-      --cool;
+    bool grow;
+    switch (ka) {
+      case 4: grow = exec_loop<KS, 4>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr, d_stop); break;
+      case 6: grow = exec_loop<KS, 6>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr, d_stop); break;
+      case 8: grow = exec_loop<KS, 8>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr, d_stop); break;
+      case 10: grow = exec_loop<KS, 10>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr, d_stop); break;
+      case 12: grow = exec_loop<KS, (KS >= 12 ? 12 : KS)>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr, d_stop); break;
+      case 14: grow = exec_loop<KS, (KS >= 14 ? 14 : KS)>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr, d_stop); break;
+      default: grow = exec_loop<KS, KS>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr, d_stop); break;
     }
-    const int32_t WIN = 32 * kact;
-    if (!TRACE && hi_max >= bn + WIN - 1) {
-      overflow = true;   // the live band may grow past the widest window
-      break;
-    }
-    in.Th = T - oe;
-    const bool edge = (bn + WIN - 1 > m && hi_max >= m) || lo_c <= d - n || lo_p <= d - 1 - n;
-    const int32_t rowbase = bn + lane * kact;
-    in.vhi = m - rowbase;
-    in.vlo = dn - n - rowbase;
-    uint8_t* row = TRACE ? tbase + (uint64_t)dn * (WMAX / 2) : nullptr;
-    int32_t lm;
-    if (!shift) {
-      in.qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-      lm = edge ? step_any<KS, TRACE, false, true>(kact, L, in, lane, cnt, row)
-                : step_any<KS, TRACE, false, false>(kact, L, in, lane, cnt, row);
-    } else {
-      in.mr_new = s_mrow[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-      lm = edge ? step_any<KS, TRACE, true, true>(kact, L, in, lane, cnt, row)
-                : step_any<KS, TRACE, true, false>(kact, L, in, lane, cnt, row);
-    }
-
-    const int32_t wm = __reduce_max_sync(FULL, lm);
-    const uint32_t mask = __ballot_sync(FULL, lm >= in.Th);
-    const uint32_t rbit = __ballot_sync(FULL, L.H[0] >= in.Th) & 1u;
-    const bool any = mask != 0u;
-    if (any) {
-      d_last = dn;
-      const int32_t sbest = wm + oe;
-      if (sbest > best) {
-        if (!TRACE) {                       // the replay needs only the threshold
-          int rf = KS;
-#pragma unroll
-          for (int r = KS - 1; r >= 0; --r) rf = (r < kact && L.H[r] == wm) ? r : rf;
-          const uint32_t fm = __ballot_sync(FULL, rf < KS);
-          const int Ln = __ffs(fm) - 1;
-          const int rr = __shfl_sync(FULL, rf, Ln);
-          bi = bn + Ln * kact + rr;
-          bj = dn - bi;
-        }
-        best = sbest;
-        T = threshold(best, p.ydrop);
-      }
-    }
-    if (!TRACE && dn <= 2 * EAGER_N && lane == 0) sT[dn] = in.Th + oe;
-    if (TRACE && lane == 0) lo_arr[dn] = bn;
-    hi_p = hi_c;
-    lo_p = lo_c;
-    hi_c = any ? bn + (32 - __clz(mask)) * kact - 1 : NOROW_HI;
-    lo_c = any ? bn + (__ffs(mask) - 1) * kact : NOROW_LO;
-    b = bn;
-    live_prev = live;
-    live = any;
-    rowb_alive = rbit != 0u;
-    d = dn;
-    if (!live && !live_prev) break;
+    if (!grow) break;
+    // two more rows per lane: the old top lane's rows move down, lane 31's are new and dead
+    relay_store<KS>(L, ka, lane, rb, s_mrow);
+    relay_load<KS>(L, 32 * ka, ka + 2, s.b, s.d, lane, rb, p, w, s_mrow);
+    ka += 2;
+    res_init(s.tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)s.b + 32 * ka);
+    s.top = false;
+    s.top_prev = false;
   }
-
-  // live-cell count of this sweep
-  uint64_t tot = cnt;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
-
-  if (TRACE) {
-    if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)(d_stop - (int32_t)sg.w) * (unsigned long long)WMAX);
-    return;
-  }
-  if (overflow) {
-    if (lane == 0) {
-      ExtRec z = {};
-      z.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE;
-      z.m = m;
-      z.n = n;
-      *R = z;
-      const uint32_t slot = atomicAdd(wa.ovf_count, 1u);   // retried with a wider window
-      wa.ovf_list[slot] = ext;
-    }
-    return;
-  }
-  uint64_t path = 0;
-  uint32_t npath = 0;
-  uint32_t flags = FZ_FLAG_DONE;
-  uint32_t width = WMAX;
-  if (bi <= EAGER_N && bj <= EAGER_N) {
-    flags |= FZ_FLAG_EAGER;
-    width = 0;
-    if (bi + bj > 0) eager_corner(p, w, lane, sT, tile, s_sub, bi, bj, path, npath, wa.err);
-  }
-  if (lane == 0) {
-    ExtRec o;
-    o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
-    o.live = tot; o.path = path; o.flags = flags; o.npath = npath;
-    o.m = m; o.n = n; o.width = width; o.ckpt = 0;
-    *R = o;
-    atomicAdd(wa.live_total, (unsigned long long)tot);
-  }
+  if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)(d_stop - (int32_t)sg.w) * (unsigned long long)WMAX);
 }
 
-// Inspector sweep with a fixed window of KS rows per lane.  The executor's
-// run_ext keeps the general bookkeeping (window resizing, exact row bounds);
-// this loop keeps only what the inspector needs per step:
+// Inspector sweep with a fixed window of KS rows per lane.  The loop keeps
+// only what the inspector needs per step:
 //   * overflow: the top lane held a live cell at d or d-1 and the base stays;
 //   * edge mode whenever rows beyond m or columns beyond n exist inside the
 //     window (then every cell checks its bounds);
@@ -1258,8 +1167,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_extend(Params p, WorkArgs 
       const uint32_t ext = wa.list[sg.x];
       const ExtRec& r = wa.rec[ext];
       if ((r.flags & FZ_FLAG_WIDE) || r.width != (uint32_t)(32 * K)) continue;
-      run_ext<K, true, true>(p, wa, ext, sg, lane, s_T[warp], s_tile[warp], s_mrow, s_sub,
-                             reinterpret_cast<Relay<K>*>(&s_relay[warp]));
+      run_exec<K>(p, wa, ext, sg, lane, s_mrow, reinterpret_cast<Relay<K>*>(&s_relay[warp]));
     } else {
       const uint32_t ext = wa.list ? wa.list[idx] : idx;
       run_inspect<K>(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow, s_sub);
