@@ -811,91 +811,119 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
 constexpr int PK = K_TIER0 / 2;   // register pairs per lane (12 rows)
 constexpr int32_t PMG = 2048;
 
+// Register p of a lane holds its rows p (low half) and p + PK (high half).
+// The row above a pair is then the previous pair (both halves), so a step
+// reads its neighbours without moving halves; only pair 0 combines the row
+// above the lane (lane l-1's row 11) with the lane's own row 5.
 struct PairState {
-  uint32_t H[PK];     // h = S - o - e, rows 2p (low half) and 2p+1 (high half)
+  uint32_t H[PK];     // h = S - o - e
   uint32_t HP[PK];    // h of the previous anti-diagonal + (o + e): the diagonal source
   uint32_t I[PK], D[PK];
-  uint32_t MR[2 * PK];  // substitution row of each row's target base (signed bytes)
+  uint32_t MR[2 * PK];  // substitution row of each row's target base (signed bytes), by row
   uint32_t SEL[PK];     // byte-permute selector: sign-extended scores of both rows' query bases
 };
 
 // Selector bytes of a row's query base q: as the low row of a pair (bytes q
-// and sign of byte q) and as the high row (bytes 4+q and its sign).
+// and sign of byte q of the first operand) and as the high row (bytes 4+q and
+// its sign, second operand).
 __device__ __forceinline__ uint32_t sel_lo(uint32_t q) { return 0x80u + 17u * q; }
 __device__ __forceinline__ uint32_t sel_hi(uint32_t q) { return 0xc4u + 17u * q; }
 
 __device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xffffu; }
 __device__ __forceinline__ uint32_t hi16(uint32_t x) { return x >> 16; }
 __device__ __forceinline__ uint32_t dup16(int32_t v) { return ((uint32_t)v & 0xffffu) * 0x10001u; }
+__device__ __forceinline__ uint32_t prow(const uint32_t (&X)[PK], int r) {
+  return r < PK ? lo16(X[r]) : hi16(X[r - PK]);
+}
+
+// Live mask of a pair of stored h values: hn + lb2 (lb2 = 0x8000 - threshold
+// in both halves) sets bit 15 of a half exactly when h >= threshold, without
+// a carry between the halves (0 <= h < 2^15, 0 < threshold <= 2^15); the
+// sign-replicating byte permute spreads that bit over the half.
+__device__ __forceinline__ uint32_t live_mask(uint32_t hn, uint32_t lb2) { return prmt(hn + lb2, 0u, 0xbb99u); }
+
+// Live cells from a sum of live masks (0xffff per live low half, 0xffff0000
+// per live high half, mod 2^32): with n_lo, n_hi < 2^15 the low 16 bits give
+// -n_lo and the rest n_lo - n_hi.
+__device__ __forceinline__ uint32_t live_count(uint32_t s) {
+  const uint32_t nlo = (0x10000u - (s & 0xffffu)) & 0xffffu;
+  const int32_t diff = (int32_t)(int16_t)(uint16_t)((s + nlo) >> 16);
+  return 2u * nlo - (uint32_t)diff;
+}
 
 // One step of the pair sweep; returns the pair-wise max of the new h (both
-// halves); dead2 accumulates -1 per pruned cell in each half.
+// halves); live2 accumulates the live masks.
 template <bool SHIFT, bool EDGE>
-__device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t noe2, uint32_t oe2, uint32_t th2,
+__device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t noe2, uint32_t oe2, uint32_t lb2,
                                           int lane, uint32_t qb, uint32_t mr_new, int32_t vlo, int32_t vhi,
-                                          uint32_t& dead2) {
+                                          uint32_t& live2) {
   uint32_t lm2 = 0;
   if (!SHIFT) {
-    // the row above this lane's row 0 is row 11 of lane l-1 (pair 5, high half)
+    // above pair 0 (rows -1 and 5): lane l-1's row 11 (high half of its pair 5) and own row 5
     uint32_t hu = __shfl_up_sync(FULL, L.H[PK - 1], 1);
     uint32_t du = __shfl_up_sync(FULL, L.D[PK - 1], 1);
     uint32_t pu = __shfl_up_sync(FULL, L.HP[PK - 1], 1);
     uint32_t su = __shfl_up_sync(FULL, L.SEL[PK - 1], 1);
     if (lane == 0) { hu = 0u; du = 0u; pu = oe2; su = sel_hi(qb) << 8; }   // above row b: nothing; its new column
+    const uint32_t ha0 = __funnelshift_r(hu, L.H[PK - 1], 16);
+    const uint32_t da0 = __funnelshift_r(du, L.D[PK - 1], 16);
+    const uint32_t pa0 = __funnelshift_r(pu, L.HP[PK - 1], 16);
+    const uint32_t sel0 = prmt(su, L.SEL[PK - 1], 0x0041u) + 0x43bcu;   // query roles swap halves
 #pragma unroll
     for (int p = PK - 1; p >= 0; --p) {
-      const uint32_t hs = __funnelshift_r(p ? L.H[p - 1] : hu, L.H[p], 16);    // rows 2p-1, 2p
-      const uint32_t ds = __funnelshift_r(p ? L.D[p - 1] : du, L.D[p], 16);
-      const uint32_t ps = __funnelshift_r(p ? L.HP[p - 1] : pu, L.HP[p], 16);
-      const uint32_t sel = prmt(p ? L.SEL[p - 1] : su, L.SEL[p], 0x0041u) + 0x43bcu;   // queries move down a row
+      const uint32_t ha = p ? L.H[p - 1] : ha0;
+      const uint32_t da = p ? L.D[p - 1] : da0;
+      const uint32_t pa = p ? L.HP[p - 1] : pa0;
+      const uint32_t sel = p ? L.SEL[p - 1] : sel0;               // each row takes the next query base
       const uint32_t ic = __viaddmax_s16x2_relu(L.I[p], ne2, L.H[p]);
-      const uint32_t dc = __viaddmax_s16x2_relu(ds, ne2, hs);
-      const uint32_t g = __vadd2(ps, prmt(L.MR[2 * p], L.MR[2 * p + 1], sel));
+      const uint32_t dc = __viaddmax_s16x2_relu(da, ne2, ha);
+      const uint32_t g = __vadd2(pa, prmt(L.MR[p], L.MR[p + PK], sel));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
       const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
-      uint32_t dead = prmt(__vsub2(hn, th2), 0u, 0xbb99u);                   // 0xffff where h < threshold
+      uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
-        dead |= (2 * p >= vlo && 2 * p <= vhi) ? 0u : 0xffffu;
-        dead |= (2 * p + 1 >= vlo && 2 * p + 1 <= vhi) ? 0u : 0xffff0000u;
+        live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + PK >= vlo && p + PK <= vhi) ? 0xffff0000u : 0u);
       }
-      const uint32_t h = hn & ~dead;
-      L.HP[p] = __vadd2(L.H[p], oe2);
+      const uint32_t h = hn & live;
+      L.HP[p] = L.H[p] + oe2;                                       // no carry: h + o + e < 2^16
       L.H[p] = h;
       L.I[p] = ic;
       L.D[p] = dc;
       L.SEL[p] = sel;
-      dead2 = __vadd2(dead2, dead);
+      live2 += live;
       lm2 = __vmaxs2(lm2, h);
     }
   } else {
-    // the base moves up a row: this lane's row 11 becomes row 0 of lane l+1's old rows
+    // the base moves up a row: new row r is old row r + 1; new row 11 is lane
+    // l+1's old row 0 (low half of its pair 0)
     uint32_t hd = __shfl_down_sync(FULL, L.H[0], 1);
     uint32_t id = __shfl_down_sync(FULL, L.I[0], 1);
     uint32_t md = __shfl_down_sync(FULL, L.MR[0], 1);
     if (lane == 31) { hd = 0u; id = 0u; md = mr_new; }
+    const uint32_t ho5 = __funnelshift_r(L.H[0], hd, 16);          // old rows 6 and 12
+    const uint32_t io5 = __funnelshift_r(L.I[0], id, 16);
 #pragma unroll
     for (int r = 0; r < 2 * PK - 1; ++r) L.MR[r] = L.MR[r + 1];
     L.MR[2 * PK - 1] = md;
 #pragma unroll
     for (int p = 0; p < PK; ++p) {
-      const uint32_t hu = __funnelshift_r(L.H[p], p < PK - 1 ? L.H[p + 1] : hd, 16);   // rows 2p+1, 2p+2 (own rows)
-      const uint32_t iu = __funnelshift_r(L.I[p], p < PK - 1 ? L.I[p + 1] : id, 16);
-      const uint32_t ic = __viaddmax_s16x2_relu(iu, ne2, hu);
+      const uint32_t ho = p < PK - 1 ? L.H[p + 1] : ho5;            // the row itself, one step back
+      const uint32_t io = p < PK - 1 ? L.I[p + 1] : io5;
+      const uint32_t ic = __viaddmax_s16x2_relu(io, ne2, ho);
       const uint32_t dc = __viaddmax_s16x2_relu(L.D[p], ne2, L.H[p]);
-      const uint32_t g = __vadd2(L.HP[p], prmt(L.MR[2 * p], L.MR[2 * p + 1], L.SEL[p]));
+      const uint32_t g = __vadd2(L.HP[p], prmt(L.MR[p], L.MR[p + PK], L.SEL[p]));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
       const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
-      uint32_t dead = prmt(__vsub2(hn, th2), 0u, 0xbb99u);
+      uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
-        dead |= (2 * p >= vlo && 2 * p <= vhi) ? 0u : 0xffffu;
-        dead |= (2 * p + 1 >= vlo && 2 * p + 1 <= vhi) ? 0u : 0xffff0000u;
+        live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + PK >= vlo && p + PK <= vhi) ? 0xffff0000u : 0u);
       }
-      const uint32_t h = hn & ~dead;
-      L.HP[p] = __vadd2(hu, oe2);
+      const uint32_t h = hn & live;
+      L.HP[p] = ho + oe2;
       L.H[p] = h;
       L.I[p] = ic;
       L.D[p] = dc;
-      dead2 = __vadd2(dead2, dead);
+      live2 += live;
       lm2 = __vmaxs2(lm2, h);
     }
   }
@@ -915,10 +943,10 @@ __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const Pair
   const int32_t c1 = oe - 128;
 #pragma unroll
   for (int r = 0; r < 2 * PK; ++r) {
-    const uint32_t h = (r & 1) ? hi16(L.H[r >> 1]) : lo16(L.H[r >> 1]);
-    const uint32_t hp = (r & 1) ? hi16(L.HP[r >> 1]) : lo16(L.HP[r >> 1]);
-    const uint32_t iv = (r & 1) ? hi16(L.I[r >> 1]) : lo16(L.I[r >> 1]);
-    const uint32_t dv = (r & 1) ? hi16(L.D[r >> 1]) : lo16(L.D[r >> 1]);
+    const uint32_t h = prow(L.H, r);
+    const uint32_t hp = prow(L.HP, r);
+    const uint32_t iv = prow(L.I, r);
+    const uint32_t dv = prow(L.D, r);
     c[CK_HDR + r * 32 + lane] = h ? (int32_t)h + B : NEG;
     c[CK_HDR + CK_WIN_MAX + r * 32 + lane] = ((int32_t)hp > oe ? (int32_t)hp - oe + B : NEG) + c1;
     c[CK_HDR + 2 * CK_WIN_MAX + r * 32 + lane] = iv ? (int32_t)iv + B : NEG;
@@ -956,7 +984,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   // (pend); the values move down once pend passes the slack that the 16-bit
   // range leaves (Params::pair_slack).
   int32_t pend = 0;
-  uint32_t th2 = dup16(PMG - oe);
+  uint32_t lb2 = dup16(0x8000 - (PMG - oe));   // live_mask bias: 0x8000 - the stored threshold
   PairState L;
   {
     const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * 2 * PK);
@@ -970,8 +998,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     if (lane == 0) L.H[0] = (uint32_t)(-oe - B) & 0xffffu;      // origin: S(0,0) = 0
   }
   bool live_prev = true, rowb_alive = true, top = false, top_prev = false;
-  uint32_t dead2 = 0u;                      // pruned cells, per half, since d_fold
-  int32_t d_fold = 0;
+  uint32_t live2 = 0u;                      // live masks summed since the last fold (live_count)
   uint32_t cnt = lane == 0 ? 1u : 0u;       // live cells of this lane (the 32-bit sweep's count)
   uint32_t head = 0u;
   sT[lane] = NEG;
@@ -981,8 +1008,8 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);
   res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);
   // the step loop leaves every ex_mask + 1 anti-diagonals (at most 2048, so
-  // that the 16-bit dead counts cannot wrap) to fold the live count and to
-  // write the checkpoints
+  // that each half's live count stays below 2^15 for live_count) to fold the
+  // live count and to write the checkpoints
   const uint32_t ck_mask = wa.ckpt ? (uint32_t)wa.ckpt_every - 1u : 0xffffffffu;
   const uint32_t ex_mask = (wa.ckpt && wa.ckpt_every <= 2048) ? (uint32_t)wa.ckpt_every - 1u : 2047u;
   bool overflow = false;
@@ -1004,12 +1031,12 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
         uint32_t lm2;
         if (!shift) {
           const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-          lm2 = edge ? pstep<false, true>(L, ne2, noe2, oe2, th2, lane, qb, 0u, vlo, vhi, dead2)
-                     : pstep<false, false>(L, ne2, noe2, oe2, th2, lane, qb, 0u, vlo, vhi, dead2);
+          lm2 = edge ? pstep<false, true>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, vlo, vhi, live2)
+                     : pstep<false, false>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, vlo, vhi, live2);
         } else {
           const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-          lm2 = edge ? pstep<true, true>(L, ne2, noe2, oe2, th2, lane, 0u, mr_new, vlo, vhi, dead2)
-                     : pstep<true, false>(L, ne2, noe2, oe2, th2, lane, 0u, mr_new, vlo, vhi, dead2);
+          lm2 = edge ? pstep<true, true>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, vlo, vhi, live2)
+                     : pstep<true, false>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, vlo, vhi, live2);
         }
         const int32_t lm = (int32_t)imax((int32_t)lo16(lm2), (int32_t)hi16(lm2));
         const int32_t wm = __reduce_max_sync(FULL, lm);           // stored h of the anti-diagonal's best
@@ -1021,7 +1048,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
           int rf = 2 * PK;
 #pragma unroll
           for (int r = 2 * PK - 1; r >= 0; --r)
-            rf = (int32_t)((r & 1) ? hi16(L.H[r >> 1]) : lo16(L.H[r >> 1])) == wm ? r : rf;
+            rf = (int32_t)prow(L.H, r) == wm ? r : rf;
           const uint32_t fm = __ballot_sync(FULL, rf < 2 * PK);
           const int Ln = __ffs(fm) - 1;
           const int rr = __shfl_sync(FULL, rf, Ln);
@@ -1044,7 +1071,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
             B += pend;
             pend = 0;
           }
-          th2 = dup16(PMG - oe + pend);
+          lb2 = dup16(0x8000 - (PMG - oe + pend));
         }
         d_last = live ? dn : d_last;
         rowb_alive = bits & 1u;
@@ -1061,9 +1088,8 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
         }
       }
       // bring the live count up to date (checkpoints and the end need it)
-      cnt += (uint32_t)(d - d_fold) * 2 * PK - (uint32_t)(-(int32_t)(int16_t)lo16(dead2) - (int32_t)(int16_t)hi16(dead2));
-      dead2 = 0u;
-      d_fold = d;
+      cnt += live_count(live2);
+      live2 = 0u;
       if (why != 0) break;
       if (((uint32_t)d & ck_mask) == 0u && d - (bi + bj) <= wa.ckpt_recent) {
         const CkScalars cs{b, d, best, bi, bj, d_last};
