@@ -997,104 +997,127 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     }
     if (lane == 0) L.H[0] = (uint32_t)(-oe - B) & 0xffffu;      // origin: S(0,0) = 0
   }
-  bool live_prev = true, rowb_alive = true, top = false, top_prev = false;
+  bool rowb_alive = true;
   uint32_t live2 = 0u;                      // live masks summed since the last fold (live_count)
   uint32_t cnt = lane == 0 ? 1u : 0u;       // live cells of this lane (the 32-bit sweep's count)
   uint32_t head = 0u;
+  int32_t wbest = best - oe - B;            // stored h of a cell scoring best: a rise is wm > wbest
+  const uint32_t m0 = lane == 0 ? 0xffffu : 0u;          // lane 0 reports row b,
+  const uint32_t m31 = lane == 31 ? 0xffffffffu : 0u;    // lane 31 its rows (the window's top lane)
   sT[lane] = NEG;
   if (lane == 0) sT[32] = NEG;
   __syncwarp();
   Reservoir qr, tr;
   res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);
   res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);
-  // the step loop leaves every ex_mask + 1 anti-diagonals (at most 2048, so
-  // that each half's live count stays below 2^15 for live_count) to fold the
-  // live count and to write the checkpoints
+  // the sweep stops every ex_mask + 1 anti-diagonals (at most 2048, so that
+  // each half's live count stays below 2^15 for live_count) to fold the live
+  // count and to write the checkpoints
   const uint32_t ck_mask = wa.ckpt ? (uint32_t)wa.ckpt_every - 1u : 0xffffffffu;
   const uint32_t ex_mask = (wa.ckpt && wa.ckpt_every <= 2048) ? (uint32_t)wa.ckpt_every - 1u : 2047u;
   bool overflow = false;
 
-  int why = d + 1 > mn ? 2 : 0;
-  if (why == 0) {
-    for (;;) {
-      for (;;) {
-        const int32_t dn = d + 1;
-        const bool shift = !rowb_alive;
-        const int32_t bn = b + (shift ? 1 : 0);
-        const bool edge = bn + WIN - 1 > m || bn < dn - n;
-        int32_t vhi = 0, vlo = 0;
-        if (edge) {
-          const int32_t rowbase = bn + lane * 2 * PK;
-          vhi = m - rowbase;
-          vlo = dn - n - rowbase;
+  // After each step: the anti-diagonal's best (warp max of the stored h), a
+  // rise of the best score, the last live anti-diagonal, and one ballot with
+  // row b's liveness (bit 0) and the top lane's (bit 31).
+  auto after_step = [&](uint32_t lm2) -> uint32_t {
+    const int32_t lm = imax((int32_t)lo16(lm2), (int32_t)hi16(lm2));
+    const int32_t wm = __reduce_max_sync(FULL, lm);
+    const uint32_t bits = __ballot_sync(FULL, ((L.H[0] & m0) | ((uint32_t)lm & m31)) != 0u);
+    if (wm > wbest) {                         // implies a live cell (wbest > 0)
+      int rf = 2 * PK;
+#pragma unroll
+      for (int r = 2 * PK - 1; r >= 0; --r) rf = (int32_t)prow(L.H, r) == wm ? r : rf;
+      const uint32_t fm = __ballot_sync(FULL, rf < 2 * PK);
+      const int Ln = __ffs(fm) - 1;
+      const int rr = __shfl_sync(FULL, rf, Ln);
+      bi = b + Ln * 2 * PK + rr;
+      bj = d - bi;
+      best = wm + oe + B;
+      if (d <= 2 * EAGER_N && lane == 0) sT[d] = best;
+      const int32_t Tn = threshold(best, p.ydrop);
+      pend += Tn - T;
+      T = Tn;
+      if (pend > p.pair_slack) {
+        const uint32_t dl = dup16(-pend);     // move every value down by the rise
+#pragma unroll
+        for (int q = 0; q < PK; ++q) {
+          L.H[q] = __viaddmax_s16x2_relu(L.H[q], dl, 0u);
+          L.HP[q] = __viaddmax_s16x2_relu(L.HP[q], dl, 0u);
+          L.I[q] = __viaddmax_s16x2_relu(L.I[q], dl, 0u);
+          L.D[q] = __viaddmax_s16x2_relu(L.D[q], dl, 0u);
         }
+        B += pend;
+        pend = 0;
+      }
+      lb2 = dup16(0x8000 - (PMG - oe + pend));
+      wbest = best - oe - B;
+    }
+    d_last = wm != 0 ? d : d_last;
+    return bits;
+  };
+
+  // Exits after a step: the end of the sweep (two anti-diagonals without a
+  // live cell, or the window's last one), an overflow (row b is live, so the
+  // base stays, and the top lane is live) and every fold boundary.  The
+  // overflow test of one step suffices: a cell beyond the window's top row at
+  // d needs that row live at d-1 (gap) or d-2 (diagonal) with the base kept
+  // since, which the test of that step saw.
+  int why = d + 1 > mn ? 2 : 0;   // 0 boundary, 1 overflow, 2 end
+  while (why == 0) {
+    // steps that cannot touch the window's edges: the base grows by at most
+    // one per step, so b + WIN <= m and b >= d - n hold for this many steps
+    const int32_t d_fold = (int32_t)(((uint32_t)d | ex_mask) + 1u);
+    const int32_t d_fast = imin(d_fold, d + imin(m - WIN - b, b - d + n));
+    bool ovf;
+    if (d_fast > d) {
+      do {
+        const bool shift = !rowb_alive;
         uint32_t lm2;
         if (!shift) {
           const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-          lm2 = edge ? pstep<false, true>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, vlo, vhi, live2)
-                     : pstep<false, false>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, vlo, vhi, live2);
+          lm2 = pstep<false, false>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, 0, 0, live2);
         } else {
           const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-          lm2 = edge ? pstep<true, true>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, vlo, vhi, live2)
-                     : pstep<true, false>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, vlo, vhi, live2);
+          lm2 = pstep<true, false>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, 0, 0, live2);
+          ++b;
         }
-        const int32_t lm = (int32_t)imax((int32_t)lo16(lm2), (int32_t)hi16(lm2));
-        const int32_t wm = __reduce_max_sync(FULL, lm);           // stored h of the anti-diagonal's best
-        const bool edge_lane = (lane == 0 && lo16(L.H[0]) != 0u) || (lane == 31 && lm != 0);
-        const uint32_t bits = __ballot_sync(FULL, edge_lane);
-        const bool live = wm != 0;
-        const int32_t sbest = wm + oe + B;
-        if (live && sbest > best) {
-          int rf = 2 * PK;
-#pragma unroll
-          for (int r = 2 * PK - 1; r >= 0; --r)
-            rf = (int32_t)prow(L.H, r) == wm ? r : rf;
-          const uint32_t fm = __ballot_sync(FULL, rf < 2 * PK);
-          const int Ln = __ffs(fm) - 1;
-          const int rr = __shfl_sync(FULL, rf, Ln);
-          bi = bn + Ln * 2 * PK + rr;
-          bj = dn - bi;
-          best = sbest;
-          if (dn <= 2 * EAGER_N && lane == 0) sT[dn] = best;
-          const int32_t Tn = threshold(best, p.ydrop);
-          pend += Tn - T;
-          T = Tn;
-          if (pend > p.pair_slack) {
-            const uint32_t dl = dup16(-pend);                     // move every value down by the rise
-#pragma unroll
-            for (int q = 0; q < PK; ++q) {
-              L.H[q] = __viaddmax_s16x2_relu(L.H[q], dl, 0u);
-              L.HP[q] = __viaddmax_s16x2_relu(L.HP[q], dl, 0u);
-              L.I[q] = __viaddmax_s16x2_relu(L.I[q], dl, 0u);
-              L.D[q] = __viaddmax_s16x2_relu(L.D[q], dl, 0u);
-            }
-            B += pend;
-            pend = 0;
-          }
-          lb2 = dup16(0x8000 - (PMG - oe + pend));
-        }
-        d_last = live ? dn : d_last;
+        ++d;
+        const uint32_t bits = after_step(lm2);
         rowb_alive = bits & 1u;
-        top_prev = top && !shift;
-        top = (bits >> 31) != 0u;
-        b = bn;
-        d = dn;
-        const bool end_ = (!live && !live_prev) || d + 1 > mn;
-        live_prev = live;
-        const bool ovf = rowb_alive && (top || top_prev) && b + WIN <= m;
-        if (end_ || ovf || ((uint32_t)d & ex_mask) == 0u) {
-          why = end_ ? 2 : (ovf ? 1 : 0);
-          break;
-        }
+        ovf = (bits & 0x80000001u) == 0x80000001u;
+      } while (d != d_fast && d - d_last < 2 && !ovf);
+    } else {
+      // one step at the window's edges: rows beyond m or columns beyond n are dead
+      const bool shift = !rowb_alive;
+      const int32_t bn = b + (shift ? 1 : 0), dn = d + 1;
+      const int32_t rowbase = bn + lane * 2 * PK;
+      const int32_t vhi = m - rowbase, vlo = dn - n - rowbase;
+      uint32_t lm2;
+      if (!shift) {
+        const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
+        lm2 = pstep<false, true>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, vlo, vhi, live2);
+      } else {
+        const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+        lm2 = pstep<true, true>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, vlo, vhi, live2);
       }
+      b = bn;
+      d = dn;
+      const uint32_t bits = after_step(lm2);
+      rowb_alive = bits & 1u;
+      // (no overflow once the window reaches row m: no row lies beyond it)
+      ovf = (bits & 0x80000001u) == 0x80000001u && b + WIN <= m;
+    }
+    const bool end_ = d - d_last >= 2 || d + 1 > mn;
+    why = end_ ? 2 : (ovf ? 1 : 0);
+    if (why != 0 || ((uint32_t)d & ex_mask) == 0u) {
       // bring the live count up to date (checkpoints and the end need it)
       cnt += live_count(live2);
       live2 = 0u;
-      if (why != 0) break;
-      if (((uint32_t)d & ck_mask) == 0u && d - (bi + bj) <= wa.ckpt_recent) {
-        const CkScalars cs{b, d, best, bi, bj, d_last};
-        head = ck_write_pair(wa, L, lane, head, cs, B, oe, cnt, 0u, sT);
-      }
+    }
+    if (why == 0 && ((uint32_t)d & ck_mask) == 0u && d - (bi + bj) <= wa.ckpt_recent) {
+      const CkScalars cs{b, d, best, bi, bj, d_last};
+      head = ck_write_pair(wa, L, lane, head, cs, B, oe, cnt, 0u, sT);
     }
   }
   if (why == 1) {
