@@ -35,28 +35,27 @@ namespace {
 constexpr int WARPS = 4;
 
 struct Reservoir {          // warp-uniform stream of bases
-  uint64_t res;
-  uint32_t pend;
-  int32_t cnt;
-  int64_t next;
+  uint32_t cur;             // the next bases, 2 bits each, below a marker bit
+  uint32_t nxt;             // the 16 bases after them (prefetched)
+  int64_t next;             // window index of the first base after nxt's 15
 };
 
+// cur holds 15 bases and a marker bit above them; when only the marker is
+// left the next 15 come from nxt, and nxt is fetched again.
 __device__ __forceinline__ void res_init(Reservoir& r, const uint8_t* s, uint64_t len, int64_t g0, int dir,
                                          int64_t first) {
-  r.res = fetch16(s, len, g0, dir, first);
-  r.pend = fetch16(s, len, g0, dir, first + 16);
-  r.cnt = 16;
-  r.next = first + 32;
+  r.cur = (fetch16(s, len, g0, dir, first) & 0x3fffffffu) | 0x40000000u;
+  r.nxt = fetch16(s, len, g0, dir, first + 15);
+  r.next = first + 30;
 }
 
 __device__ __forceinline__ uint32_t res_take(Reservoir& r, const uint8_t* s, uint64_t len, int64_t g0, int dir) {
-  const uint32_t b = (uint32_t)r.res & 3u;
-  r.res >>= 2;
-  if (--r.cnt < 16) {
-    r.res |= (uint64_t)r.pend << (2 * r.cnt);
-    r.cnt += 16;
-    r.pend = fetch16(s, len, g0, dir, r.next);
-    r.next += 16;
+  const uint32_t b = r.cur & 3u;
+  r.cur >>= 2;
+  if (r.cur == 1u) {
+    r.cur = (r.nxt & 0x3fffffffu) | 0x40000000u;
+    r.nxt = fetch16(s, len, g0, dir, r.next);
+    r.next += 15;
   }
   return b;
 }
@@ -851,13 +850,27 @@ __device__ __forceinline__ uint32_t live_count(uint32_t s) {
   return 2u * nlo - (uint32_t)diff;
 }
 
+// Lane max and live-mask sum over the pairs of a step, two pairs at a time
+// (a 3-way max and a 3-input add): `keep` holds a pair's values back for the
+// next one, `first` starts the max.
+__device__ __forceinline__ void fold2(bool keep, bool first, uint32_t h, uint32_t live, uint32_t& hk,
+                                      uint32_t& lk, uint32_t& lm2, uint32_t& live2) {
+  if (keep) {
+    hk = h;
+    lk = live;
+  } else {
+    live2 = live2 + lk + live;
+    lm2 = first ? __vmaxs2(hk, h) : __vimax3_s16x2(lm2, hk, h);
+  }
+}
+
 // One step of the pair sweep; returns the pair-wise max of the new h (both
 // halves); live2 accumulates the live masks.
 template <bool SHIFT, bool EDGE>
 __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t noe2, uint32_t oe2, uint32_t lb2,
                                           int lane, uint32_t qb, uint32_t mr_new, int32_t vlo, int32_t vhi,
                                           uint32_t& live2) {
-  uint32_t lm2 = 0;
+  uint32_t lm2 = 0, hk = 0, lk = 0;
   if (!SHIFT) {
     // above pair 0 (rows -1 and 5): lane l-1's row 11 (high half of its pair 5) and own row 5
     uint32_t hu = __shfl_up_sync(FULL, L.H[PK - 1], 1);
@@ -890,8 +903,7 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
       L.I[p] = ic;
       L.D[p] = dc;
       L.SEL[p] = sel;
-      live2 += live;
-      lm2 = __vmaxs2(lm2, h);
+      fold2(p & 1, p == PK - 2, h, live, hk, lk, lm2, live2);
     }
   } else {
     // the base moves up a row: new row r is old row r + 1; new row 11 is lane
@@ -923,8 +935,7 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
       L.H[p] = h;
       L.I[p] = ic;
       L.D[p] = dc;
-      live2 += live;
-      lm2 = __vmaxs2(lm2, h);
+      fold2(!(p & 1), p == 1, h, live, hk, lk, lm2, live2);
     }
   }
   return lm2;
