@@ -139,15 +139,16 @@ def cpu_baseline(w, seconds: float):
                                     np.count_nonzero(w.seeds[idx]["side"] & 2)) / dt}
 
 
-def traffic_for_current_kernel(mode):
+def traffic_for_current_kernel(mode, config):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, if its source has not changed since the capture; else None."""
+    summary, if it was taken on this workload and its source has not changed
+    since the capture; else None."""
     import hashlib
     _, src_name, prof_name = DOMINANT[mode]
     try:
         prof = json.load(open(os.path.join(ROOT, "profiles", prof_name)))
         src = open(os.path.join(ROOT, "gapped_smith_waterman_gb300", "csrc", src_name), "rb").read()
-        if prof.get("source_sha1") == hashlib.sha1(src).hexdigest():
+        if prof.get("config") == config and prof.get("source_sha1") == hashlib.sha1(src).hexdigest():
             return prof.get("dram_bytes_per_launch_full_batch")
     except Exception:
         pass
@@ -300,7 +301,7 @@ def main():
                                    "2 IADD at 128/clk per cell)",
                      "peak_measured_int_pipes": measured_peak,
                      "int_rates_gops": {k: v / 1e9 for k, v in (rates or {}).items()},
-                     "traffic": traffic_for_current_kernel(mode),
+                     "traffic": traffic_for_current_kernel(mode, args.config),
                      "kernel_ms_per_step": sum(insp_ms) / args.steps},
         "phase_ms_last_step": [round(x, 4) for x in st.phase_ms],
         "phases": "inspector, wide inspector, bins+scans, executors, traceback+records, whole batch",
