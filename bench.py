@@ -305,7 +305,7 @@ def main():
                      "kernel_ms_per_step": sum(insp_ms) / args.steps},
         "phase_ms_last_step": [round(x, 4) for x in st.phase_ms],
         "phases": "inspector, wide inspector, bins+scans, executors, traceback+records, whole batch",
-        "batch_stats": {"eager": int(st.eager), "bins": [int(b) for b in st.bin], "wide": int(st.wide),
+        "batch_stats": {"eager": int(st.eager), "bins": [int(b) for b in st.bin], "wide": int(st.wide), "retried_512": int(st.retried),
                         "executor_window_cells": int(st.exec_cells), "trace_bytes": int(st.trace_bytes),
                         "cigar_slot_runs": int(st.cigar_runs)},
         "gpu_launches": int(launches),

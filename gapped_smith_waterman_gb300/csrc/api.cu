@@ -391,6 +391,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   ctx->stats.eager = hc.bin_count[0];
   for (int k = 0; k < 5; ++k) ctx->stats.bin[k] = hc.bin_count[k + 1];
   ctx->stats.wide = hc.wide_count;
+  ctx->stats.retried = hc.retry_count;
   ctx->stats.extensions = hc.bin_count[7];
   return FZ_OK;
 }

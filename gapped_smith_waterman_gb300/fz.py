@@ -37,7 +37,8 @@ class FzStats(ctypes.Structure):
     _fields_ = [("live_cells", ctypes.c_uint64), ("exec_cells", ctypes.c_uint64), ("eager", ctypes.c_uint32),
                 ("bin", ctypes.c_uint32 * 5), ("extensions", ctypes.c_uint32), ("wide", ctypes.c_uint32),
                 ("trace_bytes", ctypes.c_uint64), ("cigar_runs", ctypes.c_uint64), ("launches", ctypes.c_uint32),
-                ("profiled", ctypes.c_uint32), ("phase_ms", ctypes.c_float * 6)]
+                ("profiled", ctypes.c_uint32), ("phase_ms", ctypes.c_float * 6),
+                ("retried", ctypes.c_uint32)]
 
 
 class FzError(RuntimeError):

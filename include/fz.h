@@ -95,6 +95,8 @@ typedef struct {
     float phase_ms[6];      /* device time per phase: 0 inspector (register window),
                                1 inspector (wide band), 2 binning + scans, 3 executor,
                                4 CIGAR emission, 5 whole batch */
+    uint32_t retried;       /* extensions whose live band outgrew the first register
+                               window and resumed in the 512-row one */
 } fz_stats;
 
 /*

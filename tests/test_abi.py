@@ -46,7 +46,8 @@ def test_struct_layouts_match_header():
     assert W.SEED_DTYPE.itemsize == 24
     assert fz.RESULT_DTYPE.itemsize == 24
     assert fz.ALIGNMENT_DTYPE.itemsize == 48
-    assert ctypes.sizeof(fz.FzStats) == 8 + 8 + 4 + 20 + 4 + 4 + 8 + 8 + 4 + 4 + 24
+    # fields of fz_stats in order, then tail padding to its 8-byte alignment
+    assert ctypes.sizeof(fz.FzStats) == 8 + 8 + 4 + 20 + 4 + 4 + 8 + 8 + 4 + 4 + 24 + 4 + 4
 
 
 @pytest.mark.parametrize("args", [
