@@ -54,6 +54,9 @@ struct Counters {
   uint32_t bin_cursor[8];
   uint32_t ckpt_used;          // window checkpoint slots taken (may exceed the pool)
   uint32_t pad_;
+  uint32_t order_hist[17];     // inspector order: extensions per key
+  uint32_t order_cursor[17];
+  uint32_t pad2_[2];
   uint64_t seg_total[3];       // executor segments per tier (384 rows, 512 rows, wide)
 };
 
@@ -71,6 +74,7 @@ struct fz_ctx {
   uint32_t mcol[4] = {0, 0, 0, 0};
   std::string err;
   DevBuf rec, ext_bin, exec_list, exec_pos, trace_sz, cig_cap, scan_tmp, wide_list, retry_list, counters;
+  DevBuf order_key, order_list;      // inspector work order (likely long extensions first)
   DevBuf cigar, cigar_packed, trace, scratch, spill;
   DevBuf ckpt, seg_cnt, seg;         // window checkpoints, executor segments
   DevBuf comb_off, comb_cig;         // two-sided alignments (fz_combine)
@@ -131,6 +135,8 @@ fz_status ensure_batch_buffers(fz_ctx* ctx, uint32_t n_ext) {
   CU(ctx->scan_tmp.ensure((size_t)scan_tmp_elems((uint32_t)n) * 8));
   CU(ctx->wide_list.ensure(n * 4));
   CU(ctx->retry_list.ensure(n * 4));
+  CU(ctx->order_key.ensure(n));
+  CU(ctx->order_list.ensure(n * 4));
   CU(ctx->seg_cnt.ensure(3 * n * 8));
   CU(ctx->counters.ensure(sizeof(Counters)));
   if (ctx->mode == FZ_EXTEND) {
@@ -212,8 +218,11 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   mark(ctx, 0, st);
   if (ctx->fast_ok) {
     // 384-row window for every extension; retries with 512 rows; then the wide band
+    CU(launch_order(ctx->p, n_ext, ctx->order_key.as<uint8_t>(), dc->order_hist, dc->order_cursor,
+                    ctx->order_list.as<uint32_t>(), st));
+    ctx->launches += 2;
     WorkArgs a = wa;
-    a.list = nullptr;
+    a.list = ctx->order_list.as<uint32_t>();
     a.n_work = n_ext;
     a.counter = &dc->work[0];
     a.ovf_list = ctx->retry_list.as<uint32_t>();
@@ -673,7 +682,8 @@ void fz_destroy(fz_ctx* ctx) {
   DevBuf* bufs[] = {&ctx->rec, &ctx->ext_bin, &ctx->exec_list, &ctx->exec_pos, &ctx->trace_sz, &ctx->cig_cap,
                     &ctx->scan_tmp, &ctx->wide_list, &ctx->retry_list, &ctx->counters, &ctx->cigar, &ctx->trace, &ctx->scratch,
                     &ctx->spill, &ctx->in_t, &ctx->in_q, &ctx->in_seeds, &ctx->out_res, &ctx->cigar_packed,
-                    &ctx->ckpt, &ctx->seg_cnt, &ctx->seg, &ctx->comb_off, &ctx->comb_cig};
+                    &ctx->ckpt, &ctx->seg_cnt, &ctx->seg, &ctx->comb_off, &ctx->comb_cig, &ctx->order_key,
+                    &ctx->order_list};
   for (DevBuf* b : bufs) b->release();
   if (ctx->h_cnt) cudaFreeHost(ctx->h_cnt);
   for (cudaEvent_t& e : ctx->ev)

@@ -84,6 +84,10 @@ struct PipeArgs {
   int32_t max_sub;             // max(0, largest substitution score)
 };
 cudaError_t launch_classify(const PipeArgs& a, cudaStream_t st);
+// inspector work order: extensions with more homologous 32-base blocks near
+// the anchor first (key: per extension; hist, cursor: [17], zeroed)
+cudaError_t launch_order(const Params& p, uint32_t n_ext, uint8_t* key, uint32_t* hist, uint32_t* cursor,
+                         uint32_t* list, cudaStream_t st);
 cudaError_t launch_scatter(const PipeArgs& a, cudaStream_t st);
 // exclusive scan of n uint64 values in place; total written to *total
 cudaError_t launch_scan_u64(uint64_t* data, uint32_t n, uint64_t* block_tmp, uint64_t* total, cudaStream_t st);

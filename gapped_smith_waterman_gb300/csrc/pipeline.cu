@@ -36,6 +36,79 @@ __device__ __forceinline__ uint64_t cigar_cap(int32_t i, int32_t j, int32_t oe, 
   return runs < ops ? runs : ops;
 }
 
+// ---- inspector order: likely long extensions first ----
+//
+// The inspector's warps take extensions from one work counter, so one long
+// extension taken near the end of the batch sets the kernel's tail.  FastZ
+// section 3.3 balances its executors by sorting on the inspected length; the
+// inspector has no length yet, so it is predicted: lane k of a warp looks at
+// the window's k-th 32-base block (bases 32k+1 .. 32k+32 of both sequences,
+// k < 16) and calls it homologous when some diagonal offset of -8..8 (indels
+// so far) matches at least 24 of the 32 bases; the key is the number of
+// homologous blocks, and the work list runs from the highest key down.  Only
+// the order of the work changes, never a result.
+constexpr int ORDER_KEYS = 17;
+
+__device__ __forceinline__ uint32_t same_bases(uint32_t a, uint32_t b) {
+  const uint32_t z = ~(a ^ b);
+  return __popc(z & (z >> 1) & 0x55555555u);   // 2-bit fields that are equal
+}
+
+__global__ void k_order_key(Params p, uint32_t n_ext, uint8_t* key, uint32_t* hist) {
+  __shared__ uint32_t h[ORDER_KEYS];
+  if (threadIdx.x < ORDER_KEYS) h[threadIdx.x] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const uint32_t ext = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (ext < n_ext) {                                // warp-uniform
+    const Window w = make_window(p, ext);
+    uint32_t homologous = 0;
+    if (lane < 16 && w.requested && 32 * lane + 32 <= w.m && 32 * lane + 32 <= w.n) {
+      const int64_t b0 = 32 * lane + 1;
+      const uint32_t t0 = fetch16(p.t2, p.t_len, w.tg0, w.dir, b0);
+      const uint32_t t1 = fetch16(p.t2, p.t_len, w.tg0, w.dir, b0 + 16);
+      const uint32_t q0 = fetch16(p.q2, p.q_len, w.qg0, w.dir, b0 - 8);
+      const uint32_t q1 = fetch16(p.q2, p.q_len, w.qg0, w.dir, b0 + 8);
+      const uint32_t q2 = fetch16(p.q2, p.q_len, w.qg0, w.dir, b0 + 24);
+      uint32_t best = 0;
+#pragma unroll
+      for (int s = 0; s <= 16; ++s) {               // query offset s - 8
+        const uint32_t a0 = s < 16 ? __funnelshift_r(q0, q1, 2 * s) : q1;
+        const uint32_t a1 = s < 16 ? __funnelshift_r(q1, q2, 2 * s) : q2;
+        const uint32_t c = same_bases(t0, a0) + same_bases(t1, a1);
+        best = c > best ? c : best;
+      }
+      homologous = best >= 24u ? 1u : 0u;
+    }
+    const uint32_t k = __popc(__ballot_sync(FULL, homologous != 0u));
+    if (lane == 0) {
+      key[ext] = (uint8_t)k;
+      atomicAdd(&h[k], 1u);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < ORDER_KEYS && h[threadIdx.x]) atomicAdd(&hist[threadIdx.x], h[threadIdx.x]);
+}
+
+// list[start(key) + rank] = ext, start(key) = extensions with a higher key
+__global__ void k_order_scatter(uint32_t n_ext, const uint8_t* key, const uint32_t* hist, uint32_t* cursor,
+                                uint32_t* list) {
+  __shared__ uint32_t start[ORDER_KEYS];
+  if (threadIdx.x == 0) {
+    uint32_t acc = 0;
+    for (int k = ORDER_KEYS - 1; k >= 0; --k) {
+      start[k] = acc;
+      acc += hist[k];
+    }
+  }
+  __syncthreads();
+  const uint32_t x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x < n_ext) {
+    const uint32_t k = key[x];
+    list[start[k] + atomicAdd(&cursor[k], 1u)] = x;
+  }
+}
+
 __global__ void k_classify(PipeArgs a) {
   __shared__ uint32_t h[8];
   if (threadIdx.x < 8) h[threadIdx.x] = 0;
@@ -582,6 +655,15 @@ __global__ void __launch_bounds__(EMIT_T) k_emit_exec(EmitArgs a) {
 }
 
 }  // namespace
+
+cudaError_t launch_order(const Params& p, uint32_t n_ext, uint8_t* key, uint32_t* hist, uint32_t* cursor,
+                         uint32_t* list, cudaStream_t st) {
+  if (n_ext == 0) return cudaSuccess;
+  const uint32_t gk = (uint32_t)(((uint64_t)n_ext * 32 + TB - 1) / TB);
+  k_order_key<<<gk, TB, 0, st>>>(p, n_ext, key, hist);
+  k_order_scatter<<<(n_ext + TB - 1) / TB, TB, 0, st>>>(n_ext, key, hist, cursor, list);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_classify(const PipeArgs& a, cudaStream_t st) {
   const uint32_t g = (a.n_ext + TB - 1) / TB;
