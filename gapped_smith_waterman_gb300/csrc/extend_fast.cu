@@ -807,13 +807,15 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
 // the context is created).  Results, live counts and checkpoints are those of the
 // 32-bit sweep: checkpoints are written in its layout, so the 512-row tier and
 // the executor resume from them unchanged.
-constexpr int PK = K_TIER0 / 2;   // register pairs per lane (12 rows)
+constexpr int PK = K_TIER0 / 2;   // register pairs per lane at most (12 rows, a 384-row window)
+constexpr int NP_SMALL = 4;       // pairs per lane of the small window (8 rows, 256 rows)
 constexpr int32_t PMG = 2048;
 
-// Register p of a lane holds its rows p (low half) and p + PK (high half).
-// The row above a pair is then the previous pair (both halves), so a step
-// reads its neighbours without moving halves; only pair 0 combines the row
-// above the lane (lane l-1's row 11) with the lane's own row 5.
+// With NP active pairs (2 NP rows per lane), register p < NP of a lane holds
+// its rows p (low half) and p + NP (high half).  The row above a pair is then
+// the previous pair (both halves), so a step reads its neighbours without
+// moving halves; only pair 0 combines the row above the lane (lane l-1's row
+// 2 NP - 1) with the lane's own row NP - 1.
 struct PairState {
   uint32_t H[PK];     // h = S - o - e
   uint32_t HP[PK];    // h of the previous anti-diagonal + (o + e): the diagonal source
@@ -831,8 +833,9 @@ __device__ __forceinline__ uint32_t sel_hi(uint32_t q) { return 0xc4u + 17u * q;
 __device__ __forceinline__ uint32_t lo16(uint32_t x) { return x & 0xffffu; }
 __device__ __forceinline__ uint32_t hi16(uint32_t x) { return x >> 16; }
 __device__ __forceinline__ uint32_t dup16(int32_t v) { return ((uint32_t)v & 0xffffu) * 0x10001u; }
+template <int NP>
 __device__ __forceinline__ uint32_t prow(const uint32_t (&X)[PK], int r) {
-  return r < PK ? lo16(X[r]) : hi16(X[r - PK]);
+  return r < NP ? lo16(X[r]) : hi16(X[r - NP]);
 }
 
 // Live mask of a pair of stored h values: hn + lb2 (lb2 = 0x8000 - threshold
@@ -851,51 +854,56 @@ __device__ __forceinline__ uint32_t live_count(uint32_t s) {
 }
 
 // Lane max and live-mask sum over the pairs of a step, two pairs at a time
-// (a 3-way max and a 3-input add): `keep` holds a pair's values back for the
-// next one, `first` starts the max.
-__device__ __forceinline__ void fold2(bool keep, bool first, uint32_t h, uint32_t live, uint32_t& hk,
+// (a 3-way max and a 3-input add).  q counts the pairs in the order they are
+// computed: an even one is held back for the next, an odd one folds both,
+// and with an odd count the last folds alone.
+__device__ __forceinline__ void fold2(int q, bool last, uint32_t h, uint32_t live, uint32_t& hk,
                                       uint32_t& lk, uint32_t& lm2, uint32_t& live2) {
-  if (keep) {
+  if (q & 1) {
+    live2 = live2 + lk + live;
+    lm2 = q == 1 ? __vmaxs2(hk, h) : __vimax3_s16x2(lm2, hk, h);
+  } else if (last) {
+    live2 += live;
+    lm2 = q == 0 ? h : __vmaxs2(lm2, h);
+  } else {
     hk = h;
     lk = live;
-  } else {
-    live2 = live2 + lk + live;
-    lm2 = first ? __vmaxs2(hk, h) : __vimax3_s16x2(lm2, hk, h);
   }
 }
 
-// One step of the pair sweep; returns the pair-wise max of the new h (both
-// halves); live2 accumulates the live masks.
-template <bool SHIFT, bool EDGE>
+// One step of the pair sweep with NP active pairs; returns the pair-wise max
+// of the new h (both halves); live2 accumulates the live masks.
+template <int NP, bool SHIFT, bool EDGE>
 __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t noe2, uint32_t oe2, uint32_t lb2,
                                           int lane, uint32_t qb, uint32_t mr_new, int32_t vlo, int32_t vhi,
                                           uint32_t& live2) {
   uint32_t lm2 = 0, hk = 0, lk = 0;
   if (!SHIFT) {
-    // above pair 0 (rows -1 and 5): lane l-1's row 11 (high half of its pair 5) and own row 5
-    uint32_t hu = __shfl_up_sync(FULL, L.H[PK - 1], 1);
-    uint32_t du = __shfl_up_sync(FULL, L.D[PK - 1], 1);
-    uint32_t pu = __shfl_up_sync(FULL, L.HP[PK - 1], 1);
-    uint32_t su = __shfl_up_sync(FULL, L.SEL[PK - 1], 1);
+    // above pair 0 (rows -1 and NP-1): lane l-1's row 2NP-1 (high half of its
+    // pair NP-1) and the lane's own row NP-1
+    uint32_t hu = __shfl_up_sync(FULL, L.H[NP - 1], 1);
+    uint32_t du = __shfl_up_sync(FULL, L.D[NP - 1], 1);
+    uint32_t pu = __shfl_up_sync(FULL, L.HP[NP - 1], 1);
+    uint32_t su = __shfl_up_sync(FULL, L.SEL[NP - 1], 1);
     if (lane == 0) { hu = 0u; du = 0u; pu = oe2; su = sel_hi(qb) << 8; }   // above row b: nothing; its new column
-    const uint32_t ha0 = __funnelshift_r(hu, L.H[PK - 1], 16);
-    const uint32_t da0 = __funnelshift_r(du, L.D[PK - 1], 16);
-    const uint32_t pa0 = __funnelshift_r(pu, L.HP[PK - 1], 16);
-    const uint32_t sel0 = prmt(su, L.SEL[PK - 1], 0x0041u) + 0x43bcu;   // query roles swap halves
+    const uint32_t ha0 = __funnelshift_r(hu, L.H[NP - 1], 16);
+    const uint32_t da0 = __funnelshift_r(du, L.D[NP - 1], 16);
+    const uint32_t pa0 = __funnelshift_r(pu, L.HP[NP - 1], 16);
+    const uint32_t sel0 = prmt(su, L.SEL[NP - 1], 0x0041u) + 0x43bcu;   // query roles swap halves
 #pragma unroll
-    for (int p = PK - 1; p >= 0; --p) {
+    for (int p = NP - 1; p >= 0; --p) {
       const uint32_t ha = p ? L.H[p - 1] : ha0;
       const uint32_t da = p ? L.D[p - 1] : da0;
       const uint32_t pa = p ? L.HP[p - 1] : pa0;
       const uint32_t sel = p ? L.SEL[p - 1] : sel0;               // each row takes the next query base
       const uint32_t ic = __viaddmax_s16x2_relu(L.I[p], ne2, L.H[p]);
       const uint32_t dc = __viaddmax_s16x2_relu(da, ne2, ha);
-      const uint32_t g = __vadd2(pa, prmt(L.MR[p], L.MR[p + PK], sel));
+      const uint32_t g = __vadd2(pa, prmt(L.MR[p], L.MR[p + NP], sel));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
       const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
       uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
-        live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + PK >= vlo && p + PK <= vhi) ? 0xffff0000u : 0u);
+        live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + NP >= vlo && p + NP <= vhi) ? 0xffff0000u : 0u);
       }
       const uint32_t h = hn & live;
       L.HP[p] = L.H[p] + oe2;                                       // no carry: h + o + e < 2^16
@@ -903,46 +911,47 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
       L.I[p] = ic;
       L.D[p] = dc;
       L.SEL[p] = sel;
-      fold2(p & 1, p == PK - 2, h, live, hk, lk, lm2, live2);
+      fold2(NP - 1 - p, p == 0, h, live, hk, lk, lm2, live2);
     }
   } else {
-    // the base moves up a row: new row r is old row r + 1; new row 11 is lane
-    // l+1's old row 0 (low half of its pair 0)
+    // the base moves up a row: new row r is old row r + 1; new row 2NP-1 is
+    // lane l+1's old row 0 (low half of its pair 0)
     uint32_t hd = __shfl_down_sync(FULL, L.H[0], 1);
     uint32_t id = __shfl_down_sync(FULL, L.I[0], 1);
     uint32_t md = __shfl_down_sync(FULL, L.MR[0], 1);
     if (lane == 31) { hd = 0u; id = 0u; md = mr_new; }
-    const uint32_t ho5 = __funnelshift_r(L.H[0], hd, 16);          // old rows 6 and 12
-    const uint32_t io5 = __funnelshift_r(L.I[0], id, 16);
+    const uint32_t hol = __funnelshift_r(L.H[0], hd, 16);          // old rows NP and 2NP
+    const uint32_t iol = __funnelshift_r(L.I[0], id, 16);
 #pragma unroll
-    for (int r = 0; r < 2 * PK - 1; ++r) L.MR[r] = L.MR[r + 1];
-    L.MR[2 * PK - 1] = md;
+    for (int r = 0; r < 2 * NP - 1; ++r) L.MR[r] = L.MR[r + 1];
+    L.MR[2 * NP - 1] = md;
 #pragma unroll
-    for (int p = 0; p < PK; ++p) {
-      const uint32_t ho = p < PK - 1 ? L.H[p + 1] : ho5;            // the row itself, one step back
-      const uint32_t io = p < PK - 1 ? L.I[p + 1] : io5;
+    for (int p = 0; p < NP; ++p) {
+      const uint32_t ho = p < NP - 1 ? L.H[p + 1] : hol;            // the row itself, one step back
+      const uint32_t io = p < NP - 1 ? L.I[p + 1] : iol;
       const uint32_t ic = __viaddmax_s16x2_relu(io, ne2, ho);
       const uint32_t dc = __viaddmax_s16x2_relu(L.D[p], ne2, L.H[p]);
-      const uint32_t g = __vadd2(L.HP[p], prmt(L.MR[p], L.MR[p + PK], L.SEL[p]));
+      const uint32_t g = __vadd2(L.HP[p], prmt(L.MR[p], L.MR[p + NP], L.SEL[p]));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
       const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
       uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
-        live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + PK >= vlo && p + PK <= vhi) ? 0xffff0000u : 0u);
+        live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + NP >= vlo && p + NP <= vhi) ? 0xffff0000u : 0u);
       }
       const uint32_t h = hn & live;
       L.HP[p] = ho + oe2;
       L.H[p] = h;
       L.I[p] = ic;
       L.D[p] = dc;
-      fold2(!(p & 1), p == 1, h, live, hk, lk, lm2, live2);
+      fold2(p, p == NP - 1, h, live, hk, lk, lm2, live2);
     }
   }
   return lm2;
 }
 
 // Checkpoint of the pair sweep after anti-diagonal d, in the 32-bit layout
-// (rows u = 12 lane + r): h and I, D back in score space, dead as NEG.
+// (rows u = K lane + r, K = 2 NP): h and I, D back in score space, dead as NEG.
+template <int NP>
 __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const PairState& L, int lane, uint32_t head,
                                                   const CkScalars& cs, int32_t B, int32_t oe, uint32_t cnt,
                                                   uint32_t cnt_hi, const int32_t* sT) {
@@ -953,11 +962,11 @@ __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const Pair
   int32_t* c = wa.ckpt + (uint64_t)slot * CK_SLOT_WORDS;
   const int32_t c1 = oe - 128;
 #pragma unroll
-  for (int r = 0; r < 2 * PK; ++r) {
-    const uint32_t h = prow(L.H, r);
-    const uint32_t hp = prow(L.HP, r);
-    const uint32_t iv = prow(L.I, r);
-    const uint32_t dv = prow(L.D, r);
+  for (int r = 0; r < 2 * NP; ++r) {
+    const uint32_t h = prow<NP>(L.H, r);
+    const uint32_t hp = prow<NP>(L.HP, r);
+    const uint32_t iv = prow<NP>(L.I, r);
+    const uint32_t dv = prow<NP>(L.D, r);
     c[CK_HDR + r * 32 + lane] = h ? (int32_t)h + B : NEG;
     c[CK_HDR + CK_WIN_MAX + r * 32 + lane] = ((int32_t)hp > oe ? (int32_t)hp - oe + B : NEG) + c1;
     c[CK_HDR + 2 * CK_WIN_MAX + r * 32 + lane] = iv ? (int32_t)iv + B : NEG;
@@ -967,16 +976,219 @@ __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const Pair
   c[CK_CNT + lane] = (int32_t)cnt;
   if (lane == 0) {
     c[CK_T + 32] = sT[32];
-    c[CK_D] = cs.d; c[CK_B] = cs.b; c[CK_K] = 2 * PK; c[CK_BEST] = cs.best; c[CK_BI] = cs.bi; c[CK_BJ] = cs.bj;
+    c[CK_D] = cs.d; c[CK_B] = cs.b; c[CK_K] = 2 * NP; c[CK_BEST] = cs.best; c[CK_BI] = cs.bi; c[CK_BJ] = cs.bj;
     c[CK_DLAST] = cs.d_last; c[CK_FLAGS] = 0; c[CK_PREV] = (int32_t)head;
     c[CK_CNT_HI] = (int32_t)cnt_hi;
   }
   return slot + 1;
 }
 
+// Warp-uniform control state of the pair sweep.  Stored values are score
+// minus B; T is the prune threshold, pend the part of its rises not yet
+// moved out of the stored values, wbest the stored h of a cell scoring best.
+struct PairCtl {
+  int32_t b, d, best, bi, bj, d_last;
+  int32_t B, T, pend, wbest;
+  uint32_t lb2;              // live_mask bias: 0x8000 - the stored threshold
+  uint32_t live2;            // live masks summed since the last fold (live_count)
+  uint32_t cnt;              // live cells of this lane (the 32-bit sweep's count)
+  bool rowb_alive;
+};
+
+// After each step: the anti-diagonal's best (warp max of the stored h), a
+// rise of the best score, the last live anti-diagonal, and one ballot with
+// row b's liveness (bit 0, lane 0) and the top lane's (bit 31, lane 31).
+template <int NP>
+__device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_t lm2, const Params& p, int lane,
+                                               int32_t* sT, uint32_t m0, uint32_t m31) {
+  const int32_t oe = p.oe;
+  const int32_t lm = imax((int32_t)lo16(lm2), (int32_t)hi16(lm2));
+  const int32_t wm = __reduce_max_sync(FULL, lm);
+  const uint32_t bits = __ballot_sync(FULL, ((L.H[0] & m0) | ((uint32_t)lm & m31)) != 0u);
+  if (wm > c.wbest) {                       // implies a live cell (wbest > 0)
+    int rf = 2 * NP;
+#pragma unroll
+    for (int r = 2 * NP - 1; r >= 0; --r) rf = (int32_t)prow<NP>(L.H, r) == wm ? r : rf;
+    const uint32_t fm = __ballot_sync(FULL, rf < 2 * NP);
+    const int Ln = __ffs(fm) - 1;
+    const int rr = __shfl_sync(FULL, rf, Ln);
+    c.bi = c.b + Ln * 2 * NP + rr;
+    c.bj = c.d - c.bi;
+    c.best = wm + oe + c.B;
+    if (c.d <= 2 * EAGER_N && lane == 0) sT[c.d] = c.best;
+    const int32_t Tn = threshold(c.best, p.ydrop);
+    c.pend += Tn - c.T;
+    c.T = Tn;
+    if (c.pend > p.pair_slack) {
+      const uint32_t dl = dup16(-c.pend);   // move every value down by the rise
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        L.H[q] = __viaddmax_s16x2_relu(L.H[q], dl, 0u);
+        L.HP[q] = __viaddmax_s16x2_relu(L.HP[q], dl, 0u);
+        L.I[q] = __viaddmax_s16x2_relu(L.I[q], dl, 0u);
+        L.D[q] = __viaddmax_s16x2_relu(L.D[q], dl, 0u);
+      }
+      c.B += c.pend;
+      c.pend = 0;
+    }
+    c.lb2 = dup16(0x8000 - (PMG - oe + c.pend));
+    c.wbest = c.best - oe - c.B;
+  }
+  c.d_last = wm != 0 ? c.d : c.d_last;
+  return bits;
+}
+
+// Per-warp shared buffer for changing the number of pairs per lane: the
+// stored 16-bit values of up to 384 rows, row u at index u.
+struct PairRelay {
+  uint16_t H[64 * PK], HP[64 * PK], I[64 * PK], D[64 * PK];
+};
+
+template <int NP>
+__device__ __forceinline__ void prelay_store(const PairState& L, int lane, PairRelay* rb) {
+#pragma unroll
+  for (int r = 0; r < 2 * NP; ++r) {
+    const int u = 2 * NP * lane + r;
+    rb->H[u] = (uint16_t)prow<NP>(L.H, r);
+    rb->HP[u] = (uint16_t)prow<NP>(L.HP, r);
+    rb->I[u] = (uint16_t)prow<NP>(L.I, r);
+    rb->D[u] = (uint16_t)prow<NP>(L.D, r);
+  }
+  __syncwarp();
+}
+
+// Loads rows 0 .. rows_old-1 of the relay buffer into NP pairs per lane (rows
+// beyond them are dead) and rebuilds every row's substitution row and query
+// selector from the sequences: row b + u has target base b + u and, after
+// anti-diagonal d, sits at column d - (b + u).
+template <int NP>
+__device__ __forceinline__ void prelay_load(PairState& L, int rows_old, const PairCtl& c, int lane,
+                                            const PairRelay* rb, const Params& p, const Window& w,
+                                            const uint32_t* s_mrow16) {
+  const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)c.b + (int64_t)lane * 2 * NP);
+  const uint32_t qw = fetch16(p.q2, p.q_len, w.qg0, w.dir, (int64_t)c.d - c.b - (int64_t)lane * 2 * NP - 15);
+  const uint32_t oe = (uint32_t)p.oe;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) {
+    const int u0 = 2 * NP * lane + q, u1 = u0 + NP;
+    const bool a0 = u0 < rows_old, a1 = u1 < rows_old;
+    L.H[q] = (a0 ? rb->H[u0] : 0u) | ((a1 ? rb->H[u1] : 0u) << 16);
+    L.HP[q] = (a0 ? rb->HP[u0] : oe) | ((a1 ? rb->HP[u1] : oe) << 16);
+    L.I[q] = (a0 ? rb->I[u0] : 0u) | ((a1 ? rb->I[u1] : 0u) << 16);
+    L.D[q] = (a0 ? rb->D[u0] : 0u) | ((a1 ? rb->D[u1] : 0u) << 16);
+    L.SEL[q] = sel_lo((qw >> (2 * (15 - q))) & 3u) | (sel_hi((qw >> (2 * (15 - q - NP))) & 3u) << 8);
+  }
+#pragma unroll
+  for (int r = 0; r < 2 * NP; ++r) L.MR[r] = s_mrow16[(tw >> (2 * r)) & 3u];
+  __syncwarp();
+}
+
+// Lanes (from lane 0) that hold a live cell of anti-diagonal d or d - 1.
+template <int NP>
+__device__ __forceinline__ int pair_live_lanes(const PairState& L, uint32_t oe2) {
+  uint32_t a = 0;
+#pragma unroll
+  for (int q = 0; q < NP; ++q) a |= L.H[q] | (L.HP[q] ^ oe2);
+  const uint32_t bits = __ballot_sync(FULL, a != 0u);
+  return bits ? 32 - __clz(bits) : 0;
+}
+
+// Steps of the pair sweep with NP pairs per lane (a 64 NP-row window) from
+// anti-diagonal c.d until the sweep ends (returns 2), the live band reaches
+// the window's top lane while row b is live (1: the window must grow, or the
+// extension overflows at 384 rows), or c.d reaches d_stop (0).
+//
+// Steps that cannot touch the window's edges run without edge masks: the base
+// grows by at most one row per step, so b + 64 NP <= m and b >= d - n hold
+// for that many steps.  An overflow test of one step suffices: a cell beyond
+// the window's top row at d needs that row live at d-1 (gap) or d-2
+// (diagonal) with the base kept since, which the test of that step saw.
+template <int NP>
+__device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& p, const Window& w, int lane,
+                                     Reservoir& qr, Reservoir& tr, const uint32_t* s_mrow16, int32_t* sT,
+                                     int32_t d_stop, uint32_t m0, uint32_t m31) {
+  constexpr int32_t WIN = 64 * NP;
+  const int32_t m = w.m, n = w.n, mn = w.m + w.n, oe = p.oe;
+  const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe);
+  for (;;) {
+    const int32_t d_fast = imin(d_stop, c.d + imin(m - WIN - c.b, c.b - c.d + n));
+    bool ovf;
+    if (d_fast > c.d) {
+      do {
+        const bool shift = !c.rowb_alive;
+        uint32_t lm2;
+        if (!shift) {
+          const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
+          lm2 = pstep<NP, false, false>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2);
+        } else {
+          const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+          lm2 = pstep<NP, true, false>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, 0, 0, c.live2);
+          ++c.b;
+        }
+        ++c.d;
+        const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
+        c.rowb_alive = bits & 1u;
+        ovf = (bits & 0x80000001u) == 0x80000001u;
+      } while (c.d != d_fast && c.d - c.d_last < 2 && !ovf);
+    } else {
+      // one step at the window's edges: rows beyond m or columns beyond n are dead
+      const bool shift = !c.rowb_alive;
+      const int32_t bn = c.b + (shift ? 1 : 0), dn = c.d + 1;
+      const int32_t rowbase = bn + lane * 2 * NP;
+      const int32_t vhi = m - rowbase, vlo = dn - n - rowbase;
+      uint32_t lm2;
+      if (!shift) {
+        const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
+        lm2 = pstep<NP, false, true>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, vlo, vhi, c.live2);
+      } else {
+        const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+        lm2 = pstep<NP, true, true>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, vlo, vhi, c.live2);
+      }
+      c.b = bn;
+      c.d = dn;
+      const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
+      c.rowb_alive = bits & 1u;
+      // (no overflow once the window reaches row m: no row lies beyond it)
+      ovf = (bits & 0x80000001u) == 0x80000001u && c.b + WIN <= m;
+    }
+    if (c.d - c.d_last >= 2 || c.d + 1 > mn) return 2;
+    if (ovf) return 1;
+    if (c.d >= d_stop) return 0;
+  }
+}
+
+// Changes the window from NPO to NPN pairs per lane, keeping base row b:
+// rows move through the per-warp relay buffer.  When shrinking, the caller
+// has checked that the dropped rows are dead at d and d - 1 (a cell above the
+// new top can then only become live through the rows below it, which the
+// overflow test watches).
+template <int NPO, int NPN>
+__device__ __forceinline__ void pair_resize(PairState& L, const PairCtl& c, int lane, PairRelay* rb,
+                                            const Params& p, const Window& w, const uint32_t* s_mrow16,
+                                            Reservoir& tr) {
+  prelay_store<NPO>(L, lane, rb);
+  prelay_load<NPN>(L, 64 * NPO, c, lane, rb, p, w, s_mrow16);
+  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)c.b + 64 * NPN);   // target rows entering at the new top
+}
+
+__device__ __forceinline__ uint32_t pair_ckpt(int np, const WorkArgs& wa, const PairState& L, int lane,
+                                              uint32_t head, const PairCtl& c, int32_t oe, const int32_t* sT) {
+  const CkScalars cs{c.b, c.d, c.best, c.bi, c.bj, c.d_last};
+  return np == NP_SMALL ? ck_write_pair<NP_SMALL>(wa, L, lane, head, cs, c.B, oe, c.cnt, 0u, sT)
+                        : ck_write_pair<PK>(wa, L, lane, head, cs, c.B, oe, c.cnt, 0u, sT);
+}
+
+// The pair sweep of one extension.  The window has two sizes: 256 rows (4
+// pairs per lane) to start with, and 384 rows (6 pairs): it grows when the
+// live band reaches the top lane of the small one while row b is live, and
+// every 64 anti-diagonals the large one shrinks back when the rows live at d
+// and d - 1 fit in the small one's first 30 lanes.  At 384 rows the same
+// top-lane test is the first tier's overflow, as for a fixed 384-row window:
+// the base row follows the same rule at both sizes, so the values, best
+// cells, live counts and the overflow decision do not depend on the size.
 __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t ext, int lane, int32_t* sT,
-                                 uint8_t* tile, const uint32_t* s_mrow16, const int32_t* s_sub) {
-  constexpr int32_t WIN = 64 * PK;
+                                 uint8_t* tile, const uint32_t* s_mrow16, const int32_t* s_sub, PairRelay* rb) {
+  constexpr int32_t WIN = 64 * PK;   // the first tier's largest window (the executor's row width)
   const Window w = make_window(p, ext);
   ExtRec* R = wa.rec + ext;
   if (!w.requested) {
@@ -987,18 +1199,26 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     return;
   }
   const int32_t m = w.m, n = w.n, oe = p.oe, mn = w.m + w.n;
-  int32_t best = 0, bi = 0, bj = 0, d_last = 0, b = 0, d = 0;
-  int32_t T = threshold(0, p.ydrop);
-  int32_t B = T - PMG;                      // stored value = score-space value - B
-  const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe);
+  PairCtl c;
+  c.b = 0; c.d = 0; c.best = 0; c.bi = 0; c.bj = 0; c.d_last = 0;
+  c.T = threshold(0, p.ydrop);
+  c.B = c.T - PMG;                          // stored value = score-space value - B
   // A rise of the threshold is first only added to the stored threshold
   // (pend); the values move down once pend passes the slack that the 16-bit
   // range leaves (Params::pair_slack).
-  int32_t pend = 0;
-  uint32_t lb2 = dup16(0x8000 - (PMG - oe));   // live_mask bias: 0x8000 - the stored threshold
+  c.pend = 0;
+  c.wbest = c.best - oe - c.B;
+  c.lb2 = dup16(0x8000 - (PMG - oe));
+  c.live2 = 0u;
+  c.cnt = lane == 0 ? 1u : 0u;
+  c.rowb_alive = true;
+  const uint32_t oe2 = dup16(oe);
+  const uint32_t m0 = lane == 0 ? 0xffffu : 0u;          // lane 0 reports row b,
+  const uint32_t m31 = lane == 31 ? 0xffffffffu : 0u;    // lane 31 its rows (the window's top lane)
+  int np = NP_SMALL;
   PairState L;
   {
-    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * 2 * PK);
+    const uint32_t tw = fetch16(p.t2, p.t_len, w.tg0, w.dir, (int64_t)lane * 2 * NP_SMALL);
 #pragma unroll
     for (int r = 0; r < 2 * PK; ++r) L.MR[r] = s_mrow16[(tw >> (2 * r)) & 3u];
 #pragma unroll
@@ -1006,140 +1226,56 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       L.H[q] = 0u; L.HP[q] = oe2; L.I[q] = 0u; L.D[q] = 0u;
       L.SEL[q] = sel_lo(0) | (sel_hi(0) << 8);
     }
-    if (lane == 0) L.H[0] = (uint32_t)(-oe - B) & 0xffffu;      // origin: S(0,0) = 0
+    if (lane == 0) L.H[0] = (uint32_t)(-oe - c.B) & 0xffffu;      // origin: S(0,0) = 0
   }
-  bool rowb_alive = true;
-  uint32_t live2 = 0u;                      // live masks summed since the last fold (live_count)
-  uint32_t cnt = lane == 0 ? 1u : 0u;       // live cells of this lane (the 32-bit sweep's count)
   uint32_t head = 0u;
-  int32_t wbest = best - oe - B;            // stored h of a cell scoring best: a rise is wm > wbest
-  const uint32_t m0 = lane == 0 ? 0xffffu : 0u;          // lane 0 reports row b,
-  const uint32_t m31 = lane == 31 ? 0xffffffffu : 0u;    // lane 31 its rows (the window's top lane)
   sT[lane] = NEG;
   if (lane == 0) sT[32] = NEG;
   __syncwarp();
   Reservoir qr, tr;
   res_init(qr, p.q2, p.q_len, w.qg0, w.dir, 1);
-  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, WIN);
+  res_init(tr, p.t2, p.t_len, w.tg0, w.dir, 64 * NP_SMALL);
   // the sweep stops every ex_mask + 1 anti-diagonals (at most 2048, so that
   // each half's live count stays below 2^15 for live_count) to fold the live
-  // count and to write the checkpoints
+  // count and to write the checkpoints, and with the large window every 64
+  // anti-diagonals to see whether the small one holds the band again
   const uint32_t ck_mask = wa.ckpt ? (uint32_t)wa.ckpt_every - 1u : 0xffffffffu;
   const uint32_t ex_mask = (wa.ckpt && wa.ckpt_every <= 2048) ? (uint32_t)wa.ckpt_every - 1u : 2047u;
   bool overflow = false;
 
-  // After each step: the anti-diagonal's best (warp max of the stored h), a
-  // rise of the best score, the last live anti-diagonal, and one ballot with
-  // row b's liveness (bit 0) and the top lane's (bit 31).
-  auto after_step = [&](uint32_t lm2) -> uint32_t {
-    const int32_t lm = imax((int32_t)lo16(lm2), (int32_t)hi16(lm2));
-    const int32_t wm = __reduce_max_sync(FULL, lm);
-    const uint32_t bits = __ballot_sync(FULL, ((L.H[0] & m0) | ((uint32_t)lm & m31)) != 0u);
-    if (wm > wbest) {                         // implies a live cell (wbest > 0)
-      int rf = 2 * PK;
-#pragma unroll
-      for (int r = 2 * PK - 1; r >= 0; --r) rf = (int32_t)prow(L.H, r) == wm ? r : rf;
-      const uint32_t fm = __ballot_sync(FULL, rf < 2 * PK);
-      const int Ln = __ffs(fm) - 1;
-      const int rr = __shfl_sync(FULL, rf, Ln);
-      bi = b + Ln * 2 * PK + rr;
-      bj = d - bi;
-      best = wm + oe + B;
-      if (d <= 2 * EAGER_N && lane == 0) sT[d] = best;
-      const int32_t Tn = threshold(best, p.ydrop);
-      pend += Tn - T;
-      T = Tn;
-      if (pend > p.pair_slack) {
-        const uint32_t dl = dup16(-pend);     // move every value down by the rise
-#pragma unroll
-        for (int q = 0; q < PK; ++q) {
-          L.H[q] = __viaddmax_s16x2_relu(L.H[q], dl, 0u);
-          L.HP[q] = __viaddmax_s16x2_relu(L.HP[q], dl, 0u);
-          L.I[q] = __viaddmax_s16x2_relu(L.I[q], dl, 0u);
-          L.D[q] = __viaddmax_s16x2_relu(L.D[q], dl, 0u);
-        }
-        B += pend;
-        pend = 0;
+  int why = c.d + 1 > mn ? 2 : 0;   // 0 boundary, 1 top lane live with the base kept, 2 end
+  while (why != 2) {
+    const uint32_t mask = np == PK ? (ex_mask & 63u) : ex_mask;
+    const int32_t d_stop = (int32_t)(((uint32_t)c.d | mask) + 1u);
+    why = np == PK ? pair_run<PK>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31)
+                   : pair_run<NP_SMALL>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31);
+    if (why != 0 || ((uint32_t)c.d & ex_mask) == 0u) {
+      c.cnt += live_count(c.live2);
+      c.live2 = 0u;
+    }
+    if (why == 2) break;
+    if (why == 1) {
+      if (np == PK) {
+        overflow = true;   // the live band may grow past the 384-row window
+        break;
       }
-      lb2 = dup16(0x8000 - (PMG - oe + pend));
-      wbest = best - oe - B;
+      pair_resize<NP_SMALL, PK>(L, c, lane, rb, p, w, s_mrow16, tr);
+      np = PK;
+      continue;
     }
-    d_last = wm != 0 ? d : d_last;
-    return bits;
-  };
-
-  // Exits after a step: the end of the sweep (two anti-diagonals without a
-  // live cell, or the window's last one), an overflow (row b is live, so the
-  // base stays, and the top lane is live) and every fold boundary.  The
-  // overflow test of one step suffices: a cell beyond the window's top row at
-  // d needs that row live at d-1 (gap) or d-2 (diagonal) with the base kept
-  // since, which the test of that step saw.
-  int why = d + 1 > mn ? 2 : 0;   // 0 boundary, 1 overflow, 2 end
-  while (why == 0) {
-    // steps that cannot touch the window's edges: the base grows by at most
-    // one per step, so b + WIN <= m and b >= d - n hold for this many steps
-    const int32_t d_fold = (int32_t)(((uint32_t)d | ex_mask) + 1u);
-    const int32_t d_fast = imin(d_fold, d + imin(m - WIN - b, b - d + n));
-    bool ovf;
-    if (d_fast > d) {
-      do {
-        const bool shift = !rowb_alive;
-        uint32_t lm2;
-        if (!shift) {
-          const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-          lm2 = pstep<false, false>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, 0, 0, live2);
-        } else {
-          const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-          lm2 = pstep<true, false>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, 0, 0, live2);
-          ++b;
-        }
-        ++d;
-        const uint32_t bits = after_step(lm2);
-        rowb_alive = bits & 1u;
-        ovf = (bits & 0x80000001u) == 0x80000001u;
-      } while (d != d_fast && d - d_last < 2 && !ovf);
-    } else {
-      // one step at the window's edges: rows beyond m or columns beyond n are dead
-      const bool shift = !rowb_alive;
-      const int32_t bn = b + (shift ? 1 : 0), dn = d + 1;
-      const int32_t rowbase = bn + lane * 2 * PK;
-      const int32_t vhi = m - rowbase, vlo = dn - n - rowbase;
-      uint32_t lm2;
-      if (!shift) {
-        const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-        lm2 = pstep<false, true>(L, ne2, noe2, oe2, lb2, lane, qb, 0u, vlo, vhi, live2);
-      } else {
-        const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-        lm2 = pstep<true, true>(L, ne2, noe2, oe2, lb2, lane, 0u, mr_new, vlo, vhi, live2);
+    if (((uint32_t)c.d & ck_mask) == 0u && c.d - (c.bi + c.bj) <= wa.ckpt_recent)
+      head = pair_ckpt(np, wa, L, lane, head, c, oe, sT);
+    if (np == PK) {
+      const int lanes = pair_live_lanes<PK>(L, oe2);   // lanes with a live cell at d or d-1
+      if (lanes * 2 * PK <= 60 * NP_SMALL) {
+        pair_resize<PK, NP_SMALL>(L, c, lane, rb, p, w, s_mrow16, tr);
+        np = NP_SMALL;
       }
-      b = bn;
-      d = dn;
-      const uint32_t bits = after_step(lm2);
-      rowb_alive = bits & 1u;
-      // (no overflow once the window reaches row m: no row lies beyond it)
-      ovf = (bits & 0x80000001u) == 0x80000001u && b + WIN <= m;
-    }
-    const bool end_ = d - d_last >= 2 || d + 1 > mn;
-    why = end_ ? 2 : (ovf ? 1 : 0);
-    if (why != 0 || ((uint32_t)d & ex_mask) == 0u) {
-      // bring the live count up to date (checkpoints and the end need it)
-      cnt += live_count(live2);
-      live2 = 0u;
-    }
-    if (why == 0 && ((uint32_t)d & ck_mask) == 0u && d - (bi + bj) <= wa.ckpt_recent) {
-      const CkScalars cs{b, d, best, bi, bj, d_last};
-      head = ck_write_pair(wa, L, lane, head, cs, B, oe, cnt, 0u, sT);
     }
   }
-  if (why == 1) {
-    overflow = true;
-    if (wa.ckpt) {
-      const CkScalars cs{b, d, best, bi, bj, d_last};
-      head = ck_write_pair(wa, L, lane, head, cs, B, oe, cnt, 0u, sT);
-    }
-  }
+  if (overflow && wa.ckpt) head = pair_ckpt(PK, wa, L, lane, head, c, oe, sT);
 
-  uint64_t tot = cnt;
+  uint64_t tot = c.cnt;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
   if (overflow) {
@@ -1155,6 +1291,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     }
     return;
   }
+  const int32_t best = c.best, bi = c.bi, bj = c.bj;
   uint64_t path = 0;
   uint32_t npath = 0;
   uint32_t flags = FZ_FLAG_DONE;
@@ -1175,7 +1312,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   }
   if (lane == 0) {
     ExtRec o;
-    o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
+    o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = c.d_last;
     o.live = tot; o.path = path; o.flags = flags; o.npath = npath;
     o.m = m; o.n = n; o.width = width; o.ckpt = head;
     *R = o;
@@ -1186,6 +1323,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
 __global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
   __shared__ int32_t s_T[WARPS][2 * EAGER_N + 2];
   __shared__ uint8_t s_tile[WARPS][(EAGER_N + 1) * (EAGER_N + 1)];
+  __shared__ PairRelay s_relay[WARPS];
   __shared__ uint32_t s_mrow16[4];
   __shared__ int32_t s_sub[16];
   if (threadIdx.x < 4) s_mrow16[threadIdx.x] = p.mrow16[threadIdx.x];
@@ -1199,7 +1337,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
     const uint32_t nw = wa.n_work_dev ? *wa.n_work_dev : wa.n_work;
     if (idx >= nw) break;
     const uint32_t ext = wa.list ? wa.list[idx] : idx;
-    run_inspect_pair(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow16, s_sub);
+    run_inspect_pair(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow16, s_sub, &s_relay[warp]);
   }
 }
 

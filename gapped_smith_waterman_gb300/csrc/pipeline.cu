@@ -90,10 +90,12 @@ __global__ void k_order_key(Params p, uint32_t n_ext, uint8_t* key, uint32_t* hi
   if (threadIdx.x < ORDER_KEYS && h[threadIdx.x]) atomicAdd(&hist[threadIdx.x], h[threadIdx.x]);
 }
 
-// list[start(key) + rank] = ext, start(key) = extensions with a higher key
+// list[start(key) + rank] = ext, start(key) = extensions with a higher key;
+// ranks are taken per block in shared memory, then one range per key and block
 __global__ void k_order_scatter(uint32_t n_ext, const uint8_t* key, const uint32_t* hist, uint32_t* cursor,
                                 uint32_t* list) {
-  __shared__ uint32_t start[ORDER_KEYS];
+  __shared__ uint32_t start[ORDER_KEYS], count[ORDER_KEYS], base[ORDER_KEYS];
+  if (threadIdx.x < ORDER_KEYS) count[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
     uint32_t acc = 0;
     for (int k = ORDER_KEYS - 1; k >= 0; --k) {
@@ -103,10 +105,15 @@ __global__ void k_order_scatter(uint32_t n_ext, const uint8_t* key, const uint32
   }
   __syncthreads();
   const uint32_t x = blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t k = 0, rank = 0;
   if (x < n_ext) {
-    const uint32_t k = key[x];
-    list[start[k] + atomicAdd(&cursor[k], 1u)] = x;
+    k = key[x];
+    rank = atomicAdd(&count[k], 1u);
   }
+  __syncthreads();
+  if (threadIdx.x < ORDER_KEYS && count[threadIdx.x]) base[threadIdx.x] = atomicAdd(&cursor[threadIdx.x], count[threadIdx.x]);
+  __syncthreads();
+  if (x < n_ext) list[start[k] + base[k] + rank] = x;
 }
 
 __global__ void k_classify(PipeArgs a) {
