@@ -992,7 +992,8 @@ struct PairCtl {
   uint32_t lb2;              // live_mask bias: 0x8000 - the stored threshold
   uint32_t live2;            // live masks summed since the last fold (live_count)
   uint32_t cnt;              // live cells of this lane (the 32-bit sweep's count)
-  bool rowb_alive;
+  bool rowb_alive;           // row b is live at d
+  bool top;                  // the window's top lane holds a live cell at d
 };
 
 // After each step: the anti-diagonal's best (warp max of the stored h), a
@@ -1098,6 +1099,18 @@ __device__ __forceinline__ int pair_live_lanes(const PairState& L, uint32_t oe2)
 // the window's top lane while row b is live (1: the window must grow, or the
 // extension overflows at 384 rows), or c.d reaches d_stop (0).
 //
+// Away from the window's edges the steps run in fixed pairs: a step that
+// keeps the base, then one that moves it up a row.  A loop with one kind of
+// step after the other needs no register moves between them, where a loop
+// choosing the kind per step pays for both register layouts every step.  The
+// pair leaves after its first step when row b is live (the base cannot move:
+// the next pair starts right away) and after its second when the top lane is
+// live (the next step is then taken alone).  Keeping the base while row b is
+// dead only leaves a dead row at the bottom, so every live cell stays inside
+// the window; the base never passes the base of the shift-by-one rule, and
+// the two agree whenever row b is live, which is when the window has to grow
+// or the extension overflows — the same decisions as the shift-by-one rule.
+//
 // Steps that cannot touch the window's edges run without edge masks: the base
 // grows by at most one row per step, so b + 64 NP <= m and b >= d - n hold
 // for that many steps.  An overflow test of one step suffices: a cell beyond
@@ -1113,25 +1126,31 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
   for (;;) {
     const int32_t d_fast = imin(d_stop, c.d + imin(m - WIN - c.b, c.b - c.d + n));
     bool ovf;
-    if (d_fast > c.d) {
-      do {
-        const bool shift = !c.rowb_alive;
-        uint32_t lm2;
-        if (!shift) {
+    if (d_fast > c.d && !c.top) {
+      uint32_t bits;
+      for (;;) {
+        {
           const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-          lm2 = pstep<NP, false, false>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2);
-        } else {
-          const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-          lm2 = pstep<NP, true, false>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, 0, 0, c.live2);
-          ++c.b;
+          const uint32_t lm2 = pstep<NP, false, false>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2);
+          ++c.d;
+          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
         }
-        ++c.d;
-        const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
-        c.rowb_alive = bits & 1u;
-        ovf = (bits & 0x80000001u) == 0x80000001u;
-      } while (c.d != d_fast && c.d - c.d_last < 2 && !ovf);
+        if ((bits & 1u) || c.d == d_fast || c.d - c.d_last >= 2) break;
+        {
+          const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
+          const uint32_t lm2 = pstep<NP, true, false>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, 0, 0, c.live2);
+          ++c.b;
+          ++c.d;
+          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
+        }
+        if ((int32_t)bits < 0 || c.d == d_fast || c.d - c.d_last >= 2) break;
+      }
+      c.rowb_alive = bits & 1u;
+      c.top = (int32_t)bits < 0;
+      ovf = c.rowb_alive && c.top;
     } else {
-      // one step at the window's edges: rows beyond m or columns beyond n are dead
+      // one step of the shift-by-one rule, with edge masks: rows beyond m or
+      // columns beyond n are dead
       const bool shift = !c.rowb_alive;
       const int32_t bn = c.b + (shift ? 1 : 0), dn = c.d + 1;
       const int32_t rowbase = bn + lane * 2 * NP;
@@ -1148,6 +1167,7 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
       c.d = dn;
       const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
       c.rowb_alive = bits & 1u;
+      c.top = (int32_t)bits < 0;
       // (no overflow once the window reaches row m: no row lies beyond it)
       ovf = (bits & 0x80000001u) == 0x80000001u && c.b + WIN <= m;
     }
@@ -1212,6 +1232,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   c.live2 = 0u;
   c.cnt = lane == 0 ? 1u : 0u;
   c.rowb_alive = true;
+  c.top = false;
   const uint32_t oe2 = dup16(oe);
   const uint32_t m0 = lane == 0 ? 0xffffu : 0u;          // lane 0 reports row b,
   const uint32_t m31 = lane == 31 ? 0xffffffffu : 0u;    // lane 31 its rows (the window's top lane)
@@ -1261,6 +1282,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       }
       pair_resize<NP_SMALL, PK>(L, c, lane, rb, p, w, s_mrow16, tr);
       np = PK;
+      c.top = false;        // the new top lane's rows lay beyond the old window: dead
       continue;
     }
     if (((uint32_t)c.d & ck_mask) == 0u && c.d - (c.bi + c.bj) <= wa.ckpt_recent)
@@ -1270,6 +1292,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       if (lanes * 2 * PK <= 60 * NP_SMALL) {
         pair_resize<PK, NP_SMALL>(L, c, lane, rb, p, w, s_mrow16, tr);
         np = NP_SMALL;
+        c.top = false;      // rows 240 and up are dead at d and d - 1
       }
     }
   }
