@@ -838,11 +838,13 @@ __device__ __forceinline__ uint32_t prow(const uint32_t (&X)[PK], int r) {
   return r < NP ? lo16(X[r]) : hi16(X[r - NP]);
 }
 
-// Live mask of a pair of stored h values: hn + lb2 (lb2 = 0x8000 - threshold
-// in both halves) sets bit 15 of a half exactly when h >= threshold, without
-// a carry between the halves (0 <= h < 2^15, 0 < threshold <= 2^15); the
+// Live mask of a pair of new h values.  hn = S - (o + e) comes from a packed
+// add, so a half lies in [-(o + e), 2^15) (two's complement); hn + lb2 as a
+// packed add (lb2 = 0x8000 - threshold in both halves, 0 < threshold <= 8192 +
+// 2048) sets bit 15 of a half exactly when 0 <= hn and hn >= threshold: a
+// negative half wraps to 0x8000 - |hn| - threshold, below 0x8000.  The
 // sign-replicating byte permute spreads that bit over the half.
-__device__ __forceinline__ uint32_t live_mask(uint32_t hn, uint32_t lb2) { return prmt(hn + lb2, 0u, 0xbb99u); }
+__device__ __forceinline__ uint32_t live_mask(uint32_t hn, uint32_t lb2) { return prmt(__vadd2(hn, lb2), 0u, 0xbb99u); }
 
 // Live cells from a sum of live masks (0xffff per live low half, 0xffff0000
 // per live high half, mod 2^32): with n_lo, n_hi < 2^15 the low 16 bits give
@@ -900,7 +902,7 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
       const uint32_t dc = __viaddmax_s16x2_relu(da, ne2, ha);
       const uint32_t g = __vadd2(pa, prmt(L.MR[p], L.MR[p + NP], sel));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
-      const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
+      const uint32_t hn = __vadd2(sv, noe2);          // a dead half may go negative: live_mask
       uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
         live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + NP >= vlo && p + NP <= vhi) ? 0xffff0000u : 0u);
@@ -933,7 +935,7 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
       const uint32_t dc = __viaddmax_s16x2_relu(L.D[p], ne2, L.H[p]);
       const uint32_t g = __vadd2(L.HP[p], prmt(L.MR[p], L.MR[p + NP], L.SEL[p]));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
-      const uint32_t hn = __viaddmax_s16x2_relu(sv, noe2, 0u);
+      const uint32_t hn = __vadd2(sv, noe2);          // a dead half may go negative: live_mask
       uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
         live &= ((p >= vlo && p <= vhi) ? 0xffffu : 0u) | ((p + NP >= vlo && p + NP <= vhi) ? 0xffff0000u : 0u);
