@@ -51,7 +51,7 @@ __device__ __forceinline__ void res_init(Reservoir& r, const uint8_t* s, uint64_
 
 __device__ __forceinline__ uint32_t res_take(Reservoir& r, const uint8_t* s, uint64_t len, int64_t g0, int dir) {
   const uint32_t b = r.cur & 3u;
-  r.cur >>= 2;
+  r.cur = __umulhi(r.cur, 1u << 30);   // >> 2, on the multiply-add pipe
   if (r.cur == 1u) {
     r.cur = (r.nxt & 0x3fffffffu) | 0x40000000u;
     r.nxt = fetch16(s, len, g0, dir, r.next);
@@ -883,14 +883,19 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
   if (!SHIFT) {
     // above pair 0 (rows -1 and NP-1): lane l-1's row 2NP-1 (high half of its
     // pair NP-1) and the lane's own row NP-1
-    uint32_t hu = __shfl_up_sync(FULL, L.H[NP - 1], 1);
-    uint32_t du = __shfl_up_sync(FULL, L.D[NP - 1], 1);
-    uint32_t pu = __shfl_up_sync(FULL, L.HP[NP - 1], 1);
+    const uint32_t hu = __shfl_up_sync(FULL, L.H[NP - 1], 1);
+    const uint32_t du = __shfl_up_sync(FULL, L.D[NP - 1], 1);
+    const uint32_t pu = __shfl_up_sync(FULL, L.HP[NP - 1], 1);
     uint32_t su = __shfl_up_sync(FULL, L.SEL[NP - 1], 1);
-    if (lane == 0) { hu = 0u; du = 0u; pu = oe2; su = sel_hi(qb) << 8; }   // above row b: nothing; its new column
-    const uint32_t ha0 = __funnelshift_r(hu, L.H[NP - 1], 16);
-    const uint32_t da0 = __funnelshift_r(du, L.D[NP - 1], 16);
-    const uint32_t pa0 = __funnelshift_r(pu, L.HP[NP - 1], 16);
+    if (lane == 0) su = sel_hi(qb) << 8;                            // row b's new column
+    // The shuffled high half under the own low half; lane 0 has no row
+    // above row b and takes the sign of its own byte 1 instead: 0 for h and
+    // D (below 2^15), 0 or -1 for the diagonal source, which then stays far
+    // below any live value like a dead cell's.
+    const uint32_t fs = lane == 0 ? 0x54ddu : 0x5432u;
+    const uint32_t ha0 = prmt(hu, L.H[NP - 1], fs);
+    const uint32_t da0 = prmt(du, L.D[NP - 1], fs);
+    const uint32_t pa0 = prmt(pu, L.HP[NP - 1], fs);
     const uint32_t sel0 = prmt(su, L.SEL[NP - 1], 0x0041u) + 0x43bcu;   // query roles swap halves
 #pragma unroll
     for (int p = NP - 1; p >= 0; --p) {
@@ -918,12 +923,15 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
   } else {
     // the base moves up a row: new row r is old row r + 1; new row 2NP-1 is
     // lane l+1's old row 0 (low half of its pair 0)
-    uint32_t hd = __shfl_down_sync(FULL, L.H[0], 1);
-    uint32_t id = __shfl_down_sync(FULL, L.I[0], 1);
+    const uint32_t hd = __shfl_down_sync(FULL, L.H[0], 1);
+    const uint32_t id = __shfl_down_sync(FULL, L.I[0], 1);
     uint32_t md = __shfl_down_sync(FULL, L.MR[0], 1);
-    if (lane == 31) { hd = 0u; id = 0u; md = mr_new; }
-    const uint32_t hol = __funnelshift_r(L.H[0], hd, 16);          // old rows NP and 2NP
-    const uint32_t iol = __funnelshift_r(L.I[0], id, 16);
+    if (lane == 31) md = mr_new;
+    // old rows NP and 2NP; lane 31's row 2NP lies above the window: the sign
+    // of its own byte 1 (h and I are below 2^15) makes it dead
+    const uint32_t fs = lane == 31 ? 0x9932u : 0x5432u;
+    const uint32_t hol = prmt(L.H[0], hd, fs);
+    const uint32_t iol = prmt(L.I[0], id, fs);
 #pragma unroll
     for (int r = 0; r < 2 * NP - 1; ++r) L.MR[r] = L.MR[r + 1];
     L.MR[2 * NP - 1] = md;
@@ -987,10 +995,12 @@ __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const Pair
 
 // Warp-uniform control state of the pair sweep.  Stored values are score
 // minus B; T is the prune threshold, pend the part of its rises not yet
-// moved out of the stored values, wbest the stored h of a cell scoring best.
+// moved out of the stored values, wbest2 the stored h of a cell scoring best
+// in both halves.
 struct PairCtl {
   int32_t b, d, best, bi, bj, d_last;
-  int32_t B, T, pend, wbest;
+  int32_t B, T, pend;
+  uint32_t wbest2;
   uint32_t lb2;              // live_mask bias: 0x8000 - the stored threshold
   uint32_t live2;            // live masks summed since the last fold (live_count)
   uint32_t cnt;              // live cells of this lane (the 32-bit sweep's count)
@@ -1005,10 +1015,13 @@ template <int NP>
 __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_t lm2, const Params& p, int lane,
                                                int32_t* sT, uint32_t m0, uint32_t m31) {
   const int32_t oe = p.oe;
-  const int32_t lm = imax((int32_t)lo16(lm2), (int32_t)hi16(lm2));
-  const int32_t wm = __reduce_max_sync(FULL, lm);
-  const uint32_t bits = __ballot_sync(FULL, ((L.H[0] & m0) | ((uint32_t)lm & m31)) != 0u);
-  if (wm > c.wbest) {                       // implies a live cell (wbest > 0)
+  // the lane max in both halves (a 32-bit compare of such values orders them
+  // like their halves)
+  const uint32_t lmd = __vmaxs2(lm2, prmt(lm2, 0u, 0x1032u));
+  const uint32_t wmd = __reduce_max_sync(FULL, lmd);
+  const uint32_t bits = __ballot_sync(FULL, ((L.H[0] & m0) | (lmd & m31)) != 0u);
+  if (wmd > c.wbest2) {                     // implies a live cell (wbest2 > 0)
+    const int32_t wm = (int32_t)lo16(wmd);
     int rf = 2 * NP;
 #pragma unroll
     for (int r = 2 * NP - 1; r >= 0; --r) rf = (int32_t)prow<NP>(L.H, r) == wm ? r : rf;
@@ -1035,9 +1048,9 @@ __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_
       c.pend = 0;
     }
     c.lb2 = dup16(0x8000 - (PMG - oe + c.pend));
-    c.wbest = c.best - oe - c.B;
+    c.wbest2 = dup16(c.best - oe - c.B);
   }
-  c.d_last = wm != 0 ? c.d : c.d_last;
+  c.d_last = wmd != 0u ? c.d : c.d_last;
   return bits;
 }
 
@@ -1229,7 +1242,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   // (pend); the values move down once pend passes the slack that the 16-bit
   // range leaves (Params::pair_slack).
   c.pend = 0;
-  c.wbest = c.best - oe - c.B;
+  c.wbest2 = dup16(c.best - oe - c.B);
   c.lb2 = dup16(0x8000 - (PMG - oe));
   c.live2 = 0u;
   c.cnt = lane == 0 ? 1u : 0u;
