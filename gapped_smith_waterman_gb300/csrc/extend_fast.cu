@@ -436,70 +436,86 @@ __device__ __forceinline__ int ck_stage(Relay<KS>* rb, const int32_t* c, int lan
 // A segment replays the inspector's sweep from the origin or from a
 // checkpoint up to d_stop with KA active rows per lane.  The step loop for one
 // KA carries only what the replay needs: the threshold (from the best score),
-// row b's liveness (shift test) and the top lane's (growth test); it leaves
-// when the segment ends or when the band may reach past the top of the
-// KA-row window, and the caller re-lays the window out two rows per lane
-// wider.  A window of KS rows per lane never needs to grow: the inspector of
-// this tier swept the extension in it without an overflow, with the same
-// base rows (the shift decisions are the same).
+// row b's liveness and the top lane's; it leaves when the segment ends or when
+// the band may reach past the top of the KA-row window, and the caller re-lays
+// the window out two rows per lane wider.
+//
+// Away from the window's edges and while the top lane is dead the steps run
+// in fixed pairs, a step that keeps the base and then one that moves it up
+// when row b is dead, as in the inspector's pair sweep (one register layout
+// per pair instead of a join of two every step).  The base then may trail the
+// shift-by-one base, but only while row b is dead; a step that keeps the base
+// with the top lane live is taken alone, and only when row b is live, so the
+// base is the shift-by-one base there.  A window of KS rows per lane never
+// needs to grow: keeping the base with row b live leaves the window at or
+// above the inspector's window of the next anti-diagonal (the inspector's base
+// never passes the shift-by-one base either), which held every live cell.
 struct ExecState {
   int32_t b, d, best, T;
   bool rowb_alive, top, top_prev;
   Reservoir qr, tr;
 };
 
+// One replay step to anti-diagonal s.d + 1 and its bookkeeping.
+template <int KS, int KA, bool SHIFT, bool EDGE>
+__device__ __forceinline__ void exec_step(LaneState<KS>& L, ExecState& s, StepIn& in, const Params& p,
+                                          const Window& w, int lane, const uint32_t* s_mrow, uint8_t* tbase,
+                                          int32_t* lo_arr) {
+  constexpr int32_t WMAX = 32 * KS;
+  const int32_t dn = s.d + 1;
+  const int32_t bn = s.b + (SHIFT ? 1 : 0);
+  in.Th = s.T - in.oe;
+  uint64_t packed = 0;
+  uint32_t no_cnt = 0;
+  if (EDGE) {
+    const int32_t rowbase = bn + lane * KA;
+    in.vhi = w.m - rowbase;
+    in.vlo = dn - w.n - rowbase;
+  }
+  if (!SHIFT) in.qb = res_take(s.qr, p.q2, p.q_len, w.qg0, w.dir);
+  else in.mr_new = s_mrow[res_take(s.tr, p.t2, p.t_len, w.tg0, w.dir)];
+  const int32_t lm = step<KS, KA, true, SHIFT, EDGE>(L, in, lane, no_cnt, packed);
+  store_codes<KA>(tbase + (uint64_t)dn * (WMAX / 2), lane, packed);
+  const int32_t wm = __reduce_max_sync(FULL, lm);
+  const bool edge_lane = (lane == 0 && L.H[0] >= in.Th) || (lane == 31 && lm >= in.Th);
+  const uint32_t bits = __ballot_sync(FULL, edge_lane);
+  if (wm + in.oe > s.best) {                       // the replay needs only the threshold
+    s.best = wm + in.oe;
+    s.T = threshold(s.best, p.ydrop);
+  }
+  if (lane == 0) lo_arr[dn] = bn;
+  s.rowb_alive = bits & 1u;
+  s.top_prev = s.top && !SHIFT;
+  s.top = (bits >> 31) != 0u;
+  s.b = bn;
+  s.d = dn;
+}
+
 template <int KS, int KA>
 __device__ __forceinline__ bool exec_loop(LaneState<KS>& L, ExecState& s, StepIn& in, const Params& p,
                                           const Window& w, int lane, const uint32_t* s_mrow, uint8_t* tbase,
                                           int32_t* lo_arr, int32_t d_stop) {
-  constexpr int32_t WIN = 32 * KA, WMAX = 32 * KS;
+  constexpr int32_t WIN = 32 * KA;
   const int32_t m = w.m, n = w.n;
-  uint32_t no_cnt = 0;
   for (;;) {
     if (s.d >= d_stop) return false;
-    const int32_t dn = s.d + 1;
+    // steps that cannot touch the window's edges (the base grows by at most
+    // one row per step)
+    const int32_t d_fast = imin(d_stop, s.d + imin(m - WIN - s.b, s.b - s.d + n));
+    if (d_fast > s.d && !s.top && !s.top_prev) {
+      for (;;) {
+        exec_step<KS, KA, false, false>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr);
+        if (s.rowb_alive || s.d == d_fast) break;
+        exec_step<KS, KA, true, false>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr);
+        if (s.top || s.d == d_fast) break;
+      }
+      continue;
+    }
+    // one step of the shift-by-one rule, with edge masks
     const bool shift = !s.rowb_alive;
-    const int32_t bn = s.b + (shift ? 1 : 0);
     if (KA < KS && !shift && (s.top || s.top_prev) && s.b + WIN <= m) return true;   // grow
-    in.Th = s.T - in.oe;
-    const bool edge = bn + WIN - 1 > m || bn < dn - n;
-    uint64_t packed = 0;
-    int32_t lm;
-    if (!shift) {
-      in.qb = res_take(s.qr, p.q2, p.q_len, w.qg0, w.dir);
-      if (edge) {
-        const int32_t rowbase = bn + lane * KA;
-        in.vhi = m - rowbase;
-        in.vlo = dn - n - rowbase;
-        lm = step<KS, KA, true, false, true>(L, in, lane, no_cnt, packed);
-      } else {
-        lm = step<KS, KA, true, false, false>(L, in, lane, no_cnt, packed);
-      }
-    } else {
-      in.mr_new = s_mrow[res_take(s.tr, p.t2, p.t_len, w.tg0, w.dir)];
-      if (edge) {
-        const int32_t rowbase = bn + lane * KA;
-        in.vhi = m - rowbase;
-        in.vlo = dn - n - rowbase;
-        lm = step<KS, KA, true, true, true>(L, in, lane, no_cnt, packed);
-      } else {
-        lm = step<KS, KA, true, true, false>(L, in, lane, no_cnt, packed);
-      }
-    }
-    store_codes<KA>(tbase + (uint64_t)dn * (WMAX / 2), lane, packed);
-    const int32_t wm = __reduce_max_sync(FULL, lm);
-    const bool edge_lane = (lane == 0 && L.H[0] >= in.Th) || (lane == 31 && lm >= in.Th);
-    const uint32_t bits = __ballot_sync(FULL, edge_lane);
-    if (wm + in.oe > s.best) {                       // the replay needs only the threshold
-      s.best = wm + in.oe;
-      s.T = threshold(s.best, p.ydrop);
-    }
-    if (lane == 0) lo_arr[dn] = bn;
-    s.rowb_alive = bits & 1u;
-    s.top_prev = s.top && !shift;
-    s.top = (bits >> 31) != 0u;
-    s.b = bn;
-    s.d = dn;
+    if (!shift) exec_step<KS, KA, false, true>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr);
+    else exec_step<KS, KA, true, true>(L, s, in, p, w, lane, s_mrow, tbase, lo_arr);
   }
 }
 
