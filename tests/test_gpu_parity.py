@@ -319,6 +319,50 @@ def test_pair_sweep_equals_32bit_sweep(monkeypatch):
     assert sa.live_cells == int(ores["live_cells"].sum())
 
 
+def _gap_run_pairs(rng, n_pairs):
+    """High-identity pairs with long gap runs: a deletion from the query moves
+    the live band up one row per anti-diagonal (the window's base must follow
+    every step), an insertion holds the band's bottom row while its top rises
+    (the window keeps its base and may have to grow)."""
+    pairs = []
+    for k in range(n_pairs):
+        t = rng.integers(0, 4, int(rng.integers(1200, 2400))).astype(np.uint8)
+        q = W.mutate(rng, t, 0.03, 0.0, 1.0)
+        cuts = np.sort(rng.choice(np.arange(150, min(t.size, q.size) - 150), size=3, replace=False))
+        parts, last = [], 0
+        for c in cuts:
+            parts.append(q[last:c])
+            glen = int(rng.integers(40, 260))
+            if rng.random() < 0.5:
+                parts.append(rng.integers(0, 4, glen).astype(np.uint8))     # insertion
+                last = c
+            else:
+                last = min(q.size, c + glen)                                 # deletion
+        parts.append(q[last:])
+        q = np.concatenate(parts).astype(np.uint8)
+        pairs.append((t, q) if k % 2 == 0 else (q, t))                       # gaps on either sequence
+    return pairs
+
+
+def test_gap_runs_move_the_band(monkeypatch):
+    """Long gap runs (up to 260 bases, costing up to o + 260 e = 8,200 < ydrop)
+    make the live band climb a row per step or hold its bottom while it widens:
+    the pair sweep's keep/shift pairs leave early, take single steps with the
+    top lane live, grow the window and overflow to the 512-row tier; with a
+    checkpoint every 32 anti-diagonals the executor resumes segments at bases
+    that trail the shift-by-one base.  Records and CIGARs equal the oracle's,
+    and the 16-bit and 32-bit sweeps agree on every count."""
+    rng = np.random.default_rng(47)
+    w, _ = _batch_from_pairs(_gap_run_pairs(rng, 60))
+    monkeypatch.setenv("FZ_CKPT_EVERY", "32")
+    a, acig, st, ores = _check(w, label="gap runs")
+    assert st.live_cells == int(ores["live_cells"].sum())
+    monkeypatch.setenv("FZ_NO_PAIR", "1")
+    b, bcig, sb = G.gpu_run(w)
+    assert np.array_equal(a, b) and np.array_equal(acig, bcig)
+    assert st.live_cells == sb.live_cells and st.exec_cells == sb.exec_cells and st.retried == sb.retried
+
+
 @pytest.mark.parametrize("ydrop", [20000, 20252])
 def test_pair_sweep_at_its_range_limit(ydrop, monkeypatch):
     """The 16-bit pair sweep at the largest y-drops it takes with HOXD70 and
