@@ -1029,7 +1029,7 @@ struct PairCtl {
 // row b's liveness (bit 0, lane 0) and the top lane's (bit 31, lane 31).
 template <int NP>
 __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_t lm2, const Params& p, int lane,
-                                               int32_t* sT, uint32_t m0, uint32_t m31) {
+                                               int32_t* sT, uint32_t m0, uint32_t m31, uint32_t& wmd_out) {
   const int32_t oe = p.oe;
   // the lane max in both halves (a 32-bit compare of such values orders them
   // like their halves)
@@ -1067,6 +1067,7 @@ __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_
     c.wbest2 = dup16(c.best - oe - c.B);
   }
   c.d_last = wmd != 0u ? c.d : c.d_last;
+  wmd_out = wmd;
   return bits;
 }
 
@@ -1154,31 +1155,39 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
   constexpr int32_t WIN = 64 * NP;
   const int32_t m = w.m, n = w.n, mn = w.m + w.n, oe = p.oe;
   const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe);
+  // the last anti-diagonal up to which steps cannot touch the window's edges;
+  // it never decreases (d - b and b + n never do), so it is recomputed only
+  // once reached
+  int32_t d_fast = c.d;
   for (;;) {
-    const int32_t d_fast = imin(d_stop, c.d + imin(m - WIN - c.b, c.b - c.d + n));
+    if (d_fast <= c.d) d_fast = imin(d_stop, c.d + imin(m - WIN - c.b, c.b - c.d + n));
     bool ovf;
     if (d_fast > c.d && !c.top) {
-      uint32_t bits;
+      uint32_t bits, wmd;
       for (;;) {
         {
           const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
           const uint32_t lm2 = pstep<NP, false, false>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2);
           ++c.d;
-          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
+          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
         }
-        if ((bits & 1u) || c.d == d_fast || c.d - c.d_last >= 2) break;
+        if ((bits & 1u) || c.d == d_fast || wmd == 0u) break;
         {
           const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
           const uint32_t lm2 = pstep<NP, true, false>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, 0, 0, c.live2);
           ++c.b;
           ++c.d;
-          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
+          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
         }
-        if ((int32_t)bits < 0 || c.d == d_fast || c.d - c.d_last >= 2) break;
+        if ((int32_t)bits < 0 || c.d == d_fast || wmd == 0u) break;
       }
+      // (an anti-diagonal without a live cell leaves the pairs; two in a row end the sweep)
       c.rowb_alive = bits & 1u;
       c.top = (int32_t)bits < 0;
-      ovf = c.rowb_alive && c.top;
+      if (c.d - c.d_last >= 2) return 2;
+      if (c.rowb_alive && c.top) return 1;
+      if (c.d >= d_stop) return 0;
+      continue;
     } else {
       // one step of the shift-by-one rule, with edge masks: rows beyond m or
       // columns beyond n are dead
@@ -1196,7 +1205,8 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
       }
       c.b = bn;
       c.d = dn;
-      const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31);
+      uint32_t wmd;
+      const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
       c.rowb_alive = bits & 1u;
       c.top = (int32_t)bits < 0;
       // (no overflow once the window reaches row m: no row lies beyond it)
