@@ -36,10 +36,25 @@ from gapped_smith_waterman_gb300 import workloads as W  # noqa: E402
 
 METRIC = "GCUPS and seed extensions/s (affine y-drop batch) at 1 GB300; % of DPX roofline"
 # Roofline of the integer pipes: a Gotoh cell in DPX form is 2 add-max + 1 three-way max
-# (64 lanes/clk/SM each on GB300) + 2 adds (128 lanes/clk/SM): 4/64 SM-clocks per cell,
-# i.e. 16 cells/clk/SM; x 152 SMs x 2.07 GHz max SM clock.
+# (64 lanes/clk/SM each on GB300) + 2 adds (128 lanes/clk/SM): 4/64 SM-clocks per lane
+# and cell, i.e. 16 cells/clk/SM with 32-bit lanes; x 152 SMs x 2.07 GHz max SM clock.
+# The first-tier inspector keeps two cells in each 32-bit lane (16-bit halves) when the
+# y-drop range allows it: the same instructions then advance two cells, 32 cells/clk/SM.
 SMS, SM_MAX_GHZ, CELLS_PER_CLK_SM = 152, 2.07, 16.0
 PEAK_GCUPS = SMS * SM_MAX_GHZ * CELLS_PER_CLK_SM
+
+
+def pair_sweep_used(w):
+    """Whether the library runs this workload's first tier as the 16-bit pair
+    sweep: the rule it applies when the context is created (scores in bytes,
+    finite y-drop, ydrop + 2048 + 4 (o + e + max|M|) <= 30000, o + e + max|M|
+    + 16 < 2048, FZ_NO_PAIR unset)."""
+    sub = np.asarray(w.sub, np.int64).reshape(16)
+    smax = int(np.abs(sub).max())
+    oe = int(w.gap_open) + int(w.gap_extend)
+    nop = os.environ.get("FZ_NO_PAIR", "")
+    return (w.mode == W.MODE_EXTEND and bool(np.all((sub >= -128) & (sub <= 127))) and w.ydrop != W.YDROP_INF
+            and w.ydrop + 2048 + 4 * (oe + smax) <= 30000 and oe + smax + 16 < 2048 and not (nop and nop != "0"))
 # Dominant kernel per mode: (name, source file, committed DRAM-traffic summary).
 DOMINANT = {
     "extend": ("inspector (register-window sweep; first tier two 16-bit rows per register)", "extend_fast.cu",
@@ -281,10 +296,12 @@ def main():
     if not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, args.cpu_seconds)
     mode = "local" if w.mode == W.MODE_LOCAL else "extend"
+    cells_per_lane = 2 if pair_sweep_used(w) else 1
+    peak = PEAK_GCUPS * cells_per_lane
     measured_peak = None
     if rates:
         r = rates
-        measured_peak = 1.0 / (2.0 / r["viaddmax"] + 1.0 / r["vimax3"] + 2.0 / r["iadd"]) / 1e9
+        measured_peak = cells_per_lane / (2.0 / r["viaddmax"] + 1.0 / r["vimax3"] + 2.0 / r["iadd"]) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GCUPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -295,10 +312,12 @@ def main():
         "extensions_per_s": ext_per_s,
         "live_cells_per_step": int(cells / args.steps),
         "roofline": {"bound": "alu", "kernel": DOMINANT[mode][0],
-                     "achieved": insp_gcups, "peak": PEAK_GCUPS, "unit": "Gcell/s",
-                     "frac": (insp_gcups / PEAK_GCUPS) if insp_gcups else None,
-                     "peak_basis": "152 SM x 2.07 GHz x 16 cells/clk/SM (2 DPX add-max + 1 DPX max3 at 64/clk, "
-                                   "2 IADD at 128/clk per cell)",
+                     "achieved": insp_gcups, "peak": peak, "unit": "Gcell/s",
+                     "frac": (insp_gcups / peak) if insp_gcups else None,
+                     "peak_basis": (f"152 SM x 2.07 GHz x {16 * cells_per_lane} cells/clk/SM (2 DPX add-max + 1 DPX "
+                                    "max3 at 64 lanes/clk, 2 adds at 128 lanes/clk per lane-cell; "
+                                    + ("two 16-bit cells per 32-bit lane: the first-tier pair sweep)" if cells_per_lane == 2
+                                       else "one 32-bit cell per lane)")),
                      "peak_measured_int_pipes": measured_peak,
                      "int_rates_gops": {k: v / 1e9 for k, v in (rates or {}).items()},
                      "traffic": traffic_for_current_kernel(mode, args.config),
