@@ -146,12 +146,39 @@ struct StepIn {
   uint32_t mr_new;     // SHIFT: substitution row entering lane 31
 };
 
+// Direction code of a cell, added into nibble r of the lane's codes: bits 0-1
+// the source of S (0 diagonal, 1 I, 2 D, in that order of preference), bit 2
+// set when I opens from h on the left, bit 3 when D opens from h above.  I >= h
+// and D >= h_up always, so "opens" is "h - I is not negative": the sign bit of
+// h - I, taken with a high multiply, is the complement of bit 2 (likewise for
+// D).  The nibble is then 12 + S choice - 4 (I extends) - 8 (D extends), added
+// with multiply-adds into two 32-bit words (rows 0-7 and 8-15); the caller
+// starts both words at 12 in every nibble it stores, so each nibble's sum is
+// its code in 0..15 and the words hold the codes once all rows are added.
+template <int KA>
+__device__ __forceinline__ void packed_code(uint32_t (&packed)[2], int r, int32_t G, int32_t S, int32_t Ic,
+                                            int32_t Dc, int32_t hl, int32_t hu, int32_t one) {
+  // (one is a runtime 1: the products stay multiply-adds on the FMA pipe)
+  const uint32_t sc = G == S ? 0u : (Ic == S ? 1u : 2u);
+  const uint32_t ie = __umulhi((uint32_t)imad(Ic, -one, hl), 2u);     // I extends
+  const uint32_t de = __umulhi((uint32_t)imad(Dc, -one, hu), 2u);     // D extends
+  const uint32_t nib = (uint32_t)imad((int32_t)de, -8, imad((int32_t)ie, -4, (int32_t)sc));
+  packed[r >> 3] = (uint32_t)imad((int32_t)nib, (int32_t)(1u << (4 * (r & 7))), (int32_t)packed[r >> 3]);
+}
+
+// Word w of a lane's packed codes before any row is added: 12 in each of the
+// nibbles the lane stores (rows 0..KA-1).
+template <int KA>
+__host__ __device__ constexpr uint32_t packed_base(int w) {
+  return (KA >= 8 * (w + 1)) ? 0xccccccccu : (KA <= 8 * w ? 0u : (0xccccccccu >> (32 - 4 * (KA - 8 * w))));
+}
+
 // One anti-diagonal step over the first KA slots of every lane (a 32*KA-row
 // window).  Returns the lane max of the pruned h; cnt counts live cells;
 // packed receives the direction codes in TRACE mode.
 template <int KS, int KA, bool TRACE, bool SHIFT, bool EDGE>
 __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int lane, uint32_t& cnt,
-                                        uint64_t& packed) {
+                                        uint32_t (&packed)[2]) {
   static_assert(KA <= KS && KA % 2 == 0, "active slots");
   constexpr int KH = KA / 2;
   int32_t lm = NEG;
@@ -180,8 +207,7 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
       if (TRACE) {
         const int32_t hu = r ? L.H[r - 1] : hu_top;
-        const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
-        packed += (uint64_t)code * (1ull << (4 * r));   // disjoint nibbles: add = or
+        packed_code<KA>(packed, r, G, S, Ic, Dc, hl, hu, in.one);
       }
       L.HP[r] = imad(hl, in.one, in.c1);   // next step's diagonal source, offset by o + e - 128
       L.H[r] = alive ? hn : NEG;
@@ -212,10 +238,7 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       const int32_t hn = imad(S, in.one, -in.oe);
       bool alive = hn >= in.Th;
       if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
-      if (TRACE) {
-        const uint32_t code = (G == S ? 0u : (Ic == S ? 1u : 2u)) | (Ic == hl ? 4u : 0u) | (Dc == hu ? 8u : 0u);
-        packed += (uint64_t)code * (1ull << (4 * r));
-      }
+      if (TRACE) packed_code<KA>(packed, r, G, S, Ic, Dc, hl, hu, in.one);
       L.HP[r] = imad(hl, in.one, in.c1);
       L.H[r] = alive ? hn : NEG;
       L.I[r] = Ic;
@@ -230,7 +253,8 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
 // Lane l's KA direction codes of one anti-diagonal: nibbles l*KA .. l*KA+KA-1
 // of the row (KA/2 bytes; 16-bit stores when they stay aligned).
 template <int KA>
-__device__ __forceinline__ void store_codes(uint8_t* row, int lane, uint64_t packed) {
+__device__ __forceinline__ void store_codes(uint8_t* row, int lane, const uint32_t (&pk)[2]) {
+  const uint64_t packed = ((uint64_t)pk[1] << 32) | pk[0];
   uint8_t* dst = row + lane * (KA / 2);
   if (KA % 4 == 0) {
 #pragma unroll
@@ -465,7 +489,7 @@ __device__ __forceinline__ void exec_step(LaneState<KS>& L, ExecState& s, StepIn
   const int32_t dn = s.d + 1;
   const int32_t bn = s.b + (SHIFT ? 1 : 0);
   in.Th = s.T - in.oe;
-  uint64_t packed = 0;
+  uint32_t packed[2] = {packed_base<KA>(0), packed_base<KA>(1)};
   uint32_t no_cnt = 0;
   if (EDGE) {
     const int32_t rowbase = bn + lane * KA;
@@ -669,7 +693,7 @@ __device__ void run_inspect(const Params& p, const WorkArgs& wa, uint32_t ext, i
   in.one = p.one;
   in.Th = threshold(best, p.ydrop) - oe;
   bool overflow = false;
-  uint64_t no_codes = 0;   // direction codes are the executor's
+  uint32_t no_codes[2] = {0u, 0u};   // direction codes are the executor's
   const uint32_t ck_mask = wa.ckpt ? (uint32_t)wa.ckpt_every - 1u : 0xffffffffu;
 
   // The step loop leaves at the end of the sweep, on an overflow, and at every
