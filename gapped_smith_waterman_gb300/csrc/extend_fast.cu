@@ -50,8 +50,9 @@ __device__ __forceinline__ void res_init(Reservoir& r, const uint8_t* s, uint64_
 }
 
 __device__ __forceinline__ uint32_t res_take(Reservoir& r, const uint8_t* s, uint64_t len, int64_t g0, int dir) {
-  const uint32_t b = r.cur & 3u;
-  r.cur = __umulhi(r.cur, 1u << 30);   // >> 2, on the multiply-add pipe
+  const uint32_t nx = __umulhi(r.cur, 1u << 30);              // cur >> 2 and
+  const uint32_t b = (uint32_t)imad((int32_t)nx, -4, (int32_t)r.cur);   // cur & 3, on the FMA pipe
+  r.cur = nx;
   if (r.cur == 1u) {
     r.cur = (r.nxt & 0x3fffffffu) | 0x40000000u;
     r.nxt = fetch16(s, len, g0, dir, r.next);
