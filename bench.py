@@ -44,17 +44,6 @@ SMS, SM_MAX_GHZ, CELLS_PER_CLK_SM = 152, 2.07, 16.0
 PEAK_GCUPS = SMS * SM_MAX_GHZ * CELLS_PER_CLK_SM
 
 
-def pair_sweep_used(w):
-    """Whether the library runs this workload's first tier as the 16-bit pair
-    sweep: the rule it applies when the context is created (scores in bytes,
-    finite y-drop, ydrop + 2048 + 4 (o + e + max|M|) <= 30000, o + e + max|M|
-    + 16 < 2048, FZ_NO_PAIR unset)."""
-    sub = np.asarray(w.sub, np.int64).reshape(16)
-    smax = int(np.abs(sub).max())
-    oe = int(w.gap_open) + int(w.gap_extend)
-    nop = os.environ.get("FZ_NO_PAIR", "")
-    return (w.mode == W.MODE_EXTEND and bool(np.all((sub >= -128) & (sub <= 127))) and w.ydrop != W.YDROP_INF
-            and w.ydrop + 2048 + 4 * (oe + smax) <= 30000 and oe + smax + 16 < 2048 and not (nop and nop != "0"))
 # Dominant kernel per mode: (name, source file, committed DRAM-traffic summary).
 DOMINANT = {
     "extend": ("inspector (register-window sweep; first tier two 16-bit rows per register)", "extend_fast.cu",
@@ -296,7 +285,7 @@ def main():
     if not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, args.cpu_seconds)
     mode = "local" if w.mode == W.MODE_LOCAL else "extend"
-    cells_per_lane = 2 if pair_sweep_used(w) else 1
+    cells_per_lane = 2 if fz.fz_pair_sweep_used(w.sub, w.gap_open, w.gap_extend, w.ydrop, w.mode) else 1
     peak = PEAK_GCUPS * cells_per_lane
     measured_peak = None
     if rates:

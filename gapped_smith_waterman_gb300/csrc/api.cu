@@ -407,6 +407,30 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
 
 }  // namespace
 
+namespace {
+
+// The first tier runs as the 16-bit pair sweep when the scores fit in bytes,
+// the y-drop is finite, the stored values (relative to the threshold - 2048)
+// stay below ydrop + 2048 + 2 max|sub| with room for the rises kept back
+// (slack, written to *slack), and a dead cell stays below the threshold after
+// adding o + e + max sub; FZ_NO_PAIR=1 turns it off.
+bool pair_rule(const int32_t sub[16], int32_t gap_open, int32_t gap_extend, int32_t ydrop, int32_t* slack) {
+  int64_t smax = 0;
+  bool bytes = true;
+  for (int k = 0; k < 16; ++k) {
+    smax = std::max<int64_t>(smax, std::llabs((long long)sub[k]));
+    if (sub[k] < -128 || sub[k] > 127) bytes = false;
+  }
+  const int64_t oe = (int64_t)gap_open + gap_extend;
+  const char* nop = getenv("FZ_NO_PAIR");
+  const bool ok = bytes && ydrop != FZ_YDROP_INF && ydrop >= 0 && (int64_t)ydrop + 2048 + 4 * (oe + smax) <= 30000 &&
+                  oe + smax + 16 < 2048 && !(nop && *nop && *nop != '0');
+  if (slack) *slack = ok ? (int32_t)std::min<int64_t>(8192, 30000 - ((int64_t)ydrop + 2048 + 4 * (oe + smax))) : 0;
+  return ok;
+}
+
+}  // namespace
+
 extern "C" {
 
 fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32_t gap_extend, int32_t ydrop,
@@ -446,18 +470,7 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     ctx->max_sub = std::max(ctx->max_sub, sub[k]);
   }
   ctx->fast_ok = bytes;
-  {
-    // 16-bit pair sweep: stored values (relative to the threshold - 2048) stay
-    // below ydrop + 2048 + 2 max|sub| and a dead cell must stay below the
-    // threshold after adding o + e + max sub
-    int64_t smax = 0;
-    for (int k = 0; k < 16; ++k) smax = std::max<int64_t>(smax, std::llabs((long long)sub[k]));
-    const int64_t oe = (int64_t)gap_open + gap_extend;
-    const char* nop = getenv("FZ_NO_PAIR");
-    p.pair_ok = (bytes && ydrop != FZ_YDROP_INF && (int64_t)ydrop + 2048 + 4 * (oe + smax) <= 30000 &&
-                 oe + smax + 16 < 2048 && !(nop && *nop && *nop != '0')) ? 1 : 0;
-    p.pair_slack = p.pair_ok ? (int32_t)std::min<int64_t>(8192, 30000 - ((int64_t)ydrop + 2048 + 4 * (oe + smax))) : 0;
-  }
+  p.pair_ok = pair_rule(sub, gap_open, gap_extend, ydrop, &p.pair_slack) ? 1 : 0;
   for (int t = 0; t < 4; ++t) {
     uint32_t row = 0, col = 0;
     for (int q = 0; q < 4; ++q) {
@@ -694,6 +707,11 @@ void fz_destroy(fz_ctx* ctx) {
 fz_status fz_bench_int_rates(double rates[4]) {
   if (!rates) return FZ_ERR_ARG;
   return bench_int_rates(rates) == cudaSuccess ? FZ_OK : FZ_ERR_CUDA;
+}
+
+int fz_pair_sweep_used(const int32_t sub[16], int32_t gap_open, int32_t gap_extend, int32_t ydrop, fz_mode mode) {
+  if (!sub || mode != FZ_EXTEND) return 0;
+  return pair_rule(sub, gap_open, gap_extend, ydrop, nullptr) ? 1 : 0;
 }
 
 }  // extern "C"

@@ -21,7 +21,8 @@ FZ_FLAG_DONE, FZ_FLAG_EAGER, FZ_FLAG_WIDE = 1, 2, 4
 FZ_FLAG_BIN_SHIFT = 4
 
 SYMBOLS = ("fz_create", "fz_extend_batch", "fz_extend_batch_host", "fz_get_stats", "fz_set_profiling",
-           "fz_last_error", "fz_destroy", "fz_bench_int_rates", "fz_local_fill_noalloc", "fz_combine")
+           "fz_last_error", "fz_destroy", "fz_bench_int_rates", "fz_local_fill_noalloc", "fz_combine",
+           "fz_pair_sweep_used")
 
 RESULT_DTYPE = np.dtype([("score", "<i4"), ("t_end", "<i4"), ("q_end", "<i4"), ("cigar_off", "<u4"),
                          ("cigar_len", "<u4"), ("flags", "<u4")])
@@ -87,6 +88,9 @@ def load(path: str | None = None, build_if_missing: bool = False):
     L.fz_combine.restype = ctypes.c_int
     L.fz_bench_int_rates.argtypes = [ctypes.POINTER(ctypes.c_double)]
     L.fz_bench_int_rates.restype = ctypes.c_int
+    L.fz_pair_sweep_used.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.c_int]
+    L.fz_pair_sweep_used.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -167,6 +171,14 @@ def fz_bench_int_rates():
     out = (ctypes.c_double * 4)()
     _check(None, load().fz_bench_int_rates(out))
     return {"viaddmax": out[0], "vimax3": out[1], "iadd": out[2], "imax": out[3]}
+
+
+def fz_pair_sweep_used(sub, gap_open: int, gap_extend: int, ydrop: int, mode: int) -> bool:
+    """Whether a context with these arguments runs its first inspector tier as
+    the 16-bit pair sweep (host only)."""
+    s = np.ascontiguousarray(np.asarray(sub, np.int32).reshape(16))
+    return bool(load().fz_pair_sweep_used(s.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(gap_open),
+                                          int(gap_extend), int(ydrop), int(mode)))
 
 
 # ---------------------------------------------------------------------------

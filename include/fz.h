@@ -237,6 +237,19 @@ fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_open, int32_t
  */
 fz_status fz_bench_int_rates(double rates[4]);
 
+/*
+ * Whether a context created by fz_create with these arguments runs the first
+ * inspector tier as the 16-bit pair sweep (two cells per 32-bit lane, see the
+ * design notes on the inspector): mode FZ_EXTEND, every sub[k] in [-128, 127],
+ * a finite ydrop with ydrop + 2048 + 4 (gap_open + gap_extend + max|sub|) <=
+ * 30000, gap_open + gap_extend + max|sub| + 16 < 2048, and the environment
+ * variable FZ_NO_PAIR unset or "0" (read at the call).  Returns 1 or 0 (0 for
+ * a null sub).  Host only: no device, no allocation.  The roofline of the
+ * dominant kernel depends on it (cells per lane and instruction).
+ */
+int fz_pair_sweep_used(const int32_t sub[16], int32_t gap_open, int32_t gap_extend, int32_t ydrop,
+                       fz_mode mode);
+
 #ifdef __cplusplus
 }
 #endif

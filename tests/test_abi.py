@@ -31,7 +31,7 @@ def test_header_declares_entry_points():
     names = declared_functions()
     assert {"fz_create", "fz_extend_batch", "fz_destroy", "fz_extend_batch_host", "fz_get_stats",
             "fz_last_error", "fz_set_profiling", "fz_bench_int_rates", "fz_local_fill_noalloc",
-            "fz_combine"} <= set(names)
+            "fz_combine", "fz_pair_sweep_used"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -97,3 +97,24 @@ def test_no_cpu_fallback_in_product_path():
 
 def test_combine_rejects_null_context_without_gpu(lib):
     assert lib.fz_combine(None, None, 0, None, None, None, None, None) == fz.FZ_ERR_ARG
+
+
+def test_pair_sweep_rule(lib, monkeypatch):
+    """The host-only rule that picks the 16-bit first tier (and with it the
+    roofline's cells per lane): the benchmark scoring takes it; a y-drop or gap
+    costs past the 16-bit range, scores outside bytes, no pruning, the local
+    mode and FZ_NO_PAIR=1 do not."""
+    monkeypatch.delenv("FZ_NO_PAIR", raising=False)
+    hox = W.HOXD70
+    assert fz.fz_pair_sweep_used(hox, 400, 30, 9400, W.MODE_EXTEND)
+    # ydrop + 2048 + 4 (o + e + max|M|) <= 30000: HOXD70 (max 125), o + e = 430 leaves ydrop <= 25732
+    assert fz.fz_pair_sweep_used(hox, 400, 30, 25732, W.MODE_EXTEND)
+    assert not fz.fz_pair_sweep_used(hox, 400, 30, 25733, W.MODE_EXTEND)
+    assert not fz.fz_pair_sweep_used(hox, 400, 30, W.YDROP_INF, W.MODE_EXTEND)
+    assert not fz.fz_pair_sweep_used(hox * 3, 1200, 90, 9400, W.MODE_EXTEND)      # scores beyond a byte
+    assert not fz.fz_pair_sweep_used(hox, 1900, 30, 2000, W.MODE_EXTEND)         # o + e + max|M| + 16 >= 2048
+    assert not fz.fz_pair_sweep_used(hox, 400, 30, 9400, W.MODE_LOCAL)
+    monkeypatch.setenv("FZ_NO_PAIR", "1")
+    assert not fz.fz_pair_sweep_used(hox, 400, 30, 9400, W.MODE_EXTEND)
+    monkeypatch.setenv("FZ_NO_PAIR", "0")
+    assert fz.fz_pair_sweep_used(hox, 400, 30, 9400, W.MODE_EXTEND)
