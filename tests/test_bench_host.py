@@ -1,0 +1,97 @@
+"""Host logic of bench.py (no GPU): the reference arm's JSON line, the clock
+sampler's parsing of nvidia-smi samples, and the lookup of committed DRAM
+traffic (taken only for the same workload and an unchanged kernel source)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+        "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"}
+
+
+def _run(args, env_extra=None):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, capture_output=True, text=True,
+                          env=env, timeout=600, cwd=ROOT)
+
+
+def test_reference_arm_prints_one_contract_line():
+    p = _run(["--impl", "reference", "--config", "1", "--steps", "1", "--warmup", "0"])
+    assert p.returncode == 0, p.stderr
+    lines = [l for l in p.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert KEYS <= set(d)
+    assert d["impl"] == "reference" and d["unit"] == "GCUPS" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["config"]["workload"] == "short-256bp"
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    p = _run(["--impl", "reference", "--config", "1", "--steps", "1", "--warmup", "0"],
+             {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert p.returncode == 0, p.stderr
+    assert p.stdout.strip() == ""
+
+
+def test_clock_sampler_parses_samples_and_reasons(tmp_path):
+    s = bench.ClockSampler(0)
+    path = tmp_path / "clocks.csv"
+    path.write_text("0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                    "0, 1950, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active\n"
+                    "0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                    "garbage line\n")
+    s.path = str(path)
+
+    class _P:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s.proc = _P()
+    c = s.stop()
+    assert c["sm_mhz"] == 2070.0 and c["sm_max_mhz"] == 2070.0 and c["samples"] == 3
+    assert c["reasons"] == ["sw_power_cap"]
+    assert not path.exists()
+
+
+def test_clock_sampler_without_samples():
+    s = bench.ClockSampler(0)
+    assert s.stop()["reasons"] == ["clocks not sampled"]
+
+
+def test_traffic_only_for_the_captured_workload_and_source():
+    t = bench.traffic_for_current_kernel("extend", 2)
+    prof = json.load(open(os.path.join(ROOT, "profiles", "inspector_traffic.json")))
+    assert t == prof["dram_bytes_per_launch_full_batch"]
+    assert bench.traffic_for_current_kernel("extend", 3) is None      # another workload
+    assert bench.traffic_for_current_kernel("local", 5) is not None
+
+
+@pytest.mark.parametrize("mode", ["extend", "local"])
+def test_traffic_none_when_the_source_changed(mode, monkeypatch, tmp_path):
+    _, src, prof_name = bench.DOMINANT[mode]
+    real_open = open
+
+    def fake_open(path, *a, **k):
+        if str(path).endswith(os.path.join("csrc", src)):
+            f = tmp_path / "changed.cu"
+            f.write_bytes(real_open(path, "rb").read() + b"\n// changed\n")
+            return real_open(f, *a, **k)
+        return real_open(path, *a, **k)
+
+    prof = json.load(open(os.path.join(ROOT, "profiles", prof_name)))
+    monkeypatch.setattr("builtins.open", fake_open)
+    assert bench.traffic_for_current_kernel(mode, prof["config"]) is None
