@@ -58,6 +58,8 @@ struct Counters {
   uint32_t order_cursor[17];
   uint32_t pad2_[2];
   uint64_t seg_total[3];       // executor segments per tier (384 rows, 512 rows, wide)
+  uint32_t sub_count[16];      // bin 1 by walk length (k_classify), longest first
+  uint32_t sub_cursor[16];
 };
 
 constexpr uint64_t TRACE_CAP_DEFAULT = 1ull << 30;   // smallest executor arena cap before chunking
@@ -264,6 +266,8 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   pa.ext_bin = ctx->ext_bin.as<uint32_t>();
   pa.bin_count = dc->bin_count;
   pa.bin_cursor = dc->bin_cursor;
+  pa.sub_count = dc->sub_count;
+  pa.sub_cursor = dc->sub_cursor;
   pa.exec_list = ctx->exec_list.as<uint32_t>();
   pa.exec_pos = ctx->exec_pos.as<uint32_t>();
   pa.trace_sz = ctx->trace_sz.as<uint64_t>();

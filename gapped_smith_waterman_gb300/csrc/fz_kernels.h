@@ -74,6 +74,8 @@ struct PipeArgs {
   uint32_t* ext_bin;           // per extension: 0 none / eager, 1..5 executor bin
   uint32_t* bin_count;         // [8]: 0 eager, 1..5 bins, 6 unused, 7 requested
   uint32_t* bin_cursor;        // [8]
+  uint32_t* sub_count;         // [16]: bin 1 by the best cell's anti-diagonal, longest first
+  uint32_t* sub_cursor;        // [16]
   uint32_t* exec_list;         // executor order: bins 5, 4, .., 1
   uint32_t* exec_pos;          // per extension: index in exec_list
   uint64_t* trace_sz;          // per exec item

@@ -24,6 +24,14 @@ __device__ __forceinline__ uint32_t bin_of(int32_t i, int32_t j) {
   return mx <= 512 ? 1u : mx <= 2048 ? 2u : mx <= 8192 ? 3u : mx <= 32768 ? 4u : 5u;
 }
 
+// Bin 1 is laid out by the best cell's anti-diagonal i + j (<= 1024), in 16
+// buckets of 64, longest first: one thread walks each of its extensions, and a
+// warp of walks of like length waits less for its longest one.
+__device__ __forceinline__ uint32_t sub_of(int32_t i, int32_t j) {
+  const int32_t b = (i + j) >> 6;
+  return 15u - (uint32_t)(b > 15 ? 15 : b);
+}
+
 // Upper bound on the CIGAR runs of an alignment ending at (i, j).  The traced
 // alignment scores S* >= 0, so its g gap runs (each costing at least o + e)
 // are paid for by at most min(i, j) diagonal scores of at most max_sub each:
@@ -117,8 +125,9 @@ __global__ void k_order_scatter(uint32_t n_ext, const uint8_t* key, const uint32
 }
 
 __global__ void k_classify(PipeArgs a) {
-  __shared__ uint32_t h[8];
+  __shared__ uint32_t h[8], hs[16];
   if (threadIdx.x < 8) h[threadIdx.x] = 0;
+  if (threadIdx.x < 16) hs[threadIdx.x] = 0;
   __syncthreads();
   const uint32_t x = blockIdx.x * blockDim.x + threadIdx.x;
   if (x < a.n_ext) {
@@ -134,6 +143,7 @@ __global__ void k_classify(PipeArgs a) {
         } else {
           bin = bin_of(r.i_end, r.j_end);
           atomicAdd(&h[bin], 1u);
+          if (bin == 1u) atomicAdd(&hs[sub_of(r.i_end, r.j_end)], 1u);
         }
       }
     }
@@ -142,6 +152,7 @@ __global__ void k_classify(PipeArgs a) {
   }
   __syncthreads();
   if (threadIdx.x < 8 && h[threadIdx.x]) atomicAdd(&a.bin_count[threadIdx.x], h[threadIdx.x]);
+  if (threadIdx.x < 16 && hs[threadIdx.x]) atomicAdd(&a.sub_count[threadIdx.x], hs[threadIdx.x]);
 }
 
 // cursor[k] = first executor slot of bin k; bins are laid out 5, 4, 3, 2, 1
@@ -150,29 +161,41 @@ __global__ void k_bin_starts(PipeArgs a) {
     uint32_t c = 0;
     for (int k = 5; k >= 1; --k) {
       a.bin_cursor[k] = c;
-      c += a.bin_count[k];
+      if (k == 1)
+        for (int s = 0; s < 16; ++s) {
+          a.sub_cursor[s] = c;
+          c += a.sub_count[s];
+        }
+      else
+        c += a.bin_count[k];
     }
     a.bin_cursor[0] = c;   // executor items
   }
 }
 
 __global__ void k_scatter(PipeArgs a) {
-  __shared__ uint32_t cnt[8], base[8];
-  if (threadIdx.x < 8) cnt[threadIdx.x] = 0;
+  // slots 2..5: bins 2..5; slots 8..23: bin 1's length buckets
+  __shared__ uint32_t cnt[24], base[24];
+  if (threadIdx.x < 24) cnt[threadIdx.x] = 0;
   __syncthreads();
   const uint32_t x = blockIdx.x * blockDim.x + threadIdx.x;
-  uint32_t bin = 0, local_pos = 0;
+  uint32_t bin = 0, slot = 0, local_pos = 0;
+  ExtRec r;
   if (x < a.n_ext) {
     bin = a.ext_bin[x];
-    if (bin) local_pos = atomicAdd(&cnt[bin], 1u);
+    if (bin) {
+      r = a.rec[x];
+      slot = bin == 1u ? 8u + sub_of(r.i_end, r.j_end) : bin;
+      local_pos = atomicAdd(&cnt[slot], 1u);
+    }
   }
   __syncthreads();
-  if (threadIdx.x >= 1 && threadIdx.x <= 5 && cnt[threadIdx.x])
-    base[threadIdx.x] = atomicAdd(&a.bin_cursor[threadIdx.x], cnt[threadIdx.x]);
+  if (threadIdx.x >= 2 && threadIdx.x < 24 && (threadIdx.x <= 5 || threadIdx.x >= 8) && cnt[threadIdx.x])
+    base[threadIdx.x] = atomicAdd(threadIdx.x >= 8 ? &a.sub_cursor[threadIdx.x - 8] : &a.bin_cursor[threadIdx.x],
+                                  cnt[threadIdx.x]);
   __syncthreads();
   if (x < a.n_ext && bin) {
-    const uint32_t pos = base[bin] + local_pos;
-    const ExtRec r = a.rec[x];
+    const uint32_t pos = base[slot] + local_pos;
     a.exec_list[pos] = x;
     a.exec_pos[x] = pos;
     a.trace_sz[pos] = trace_bytes(r.width, r.i_end + r.j_end);
