@@ -72,26 +72,26 @@ def test_clock_sampler_without_samples():
     assert s.stop()["reasons"] == ["clocks not sampled"]
 
 
-def test_traffic_only_for_the_captured_workload_and_source():
-    t = bench.traffic_for_current_kernel("extend", 2)
-    prof = json.load(open(os.path.join(ROOT, "profiles", "inspector_traffic.json")))
-    assert t == prof["dram_bytes_per_launch_full_batch"]
-    assert bench.traffic_for_current_kernel("extend", 3) is None      # another workload
-    assert bench.traffic_for_current_kernel("local", 5) is not None
+def _fake_tree(tmp_path, mode, config, src_bytes, traffic):
+    import hashlib
+    _, src, prof_name = bench.DOMINANT[mode]
+    (tmp_path / "profiles").mkdir(exist_ok=True)
+    csrc = tmp_path / "gapped_smith_waterman_gb300" / "csrc"
+    csrc.mkdir(parents=True, exist_ok=True)
+    (csrc / src).write_bytes(src_bytes)
+    (tmp_path / "profiles" / prof_name).write_text(json.dumps({
+        "config": config, "source_sha1": hashlib.sha1(src_bytes).hexdigest(),
+        "dram_bytes_per_launch_full_batch": traffic}))
+    return csrc / src
 
 
 @pytest.mark.parametrize("mode", ["extend", "local"])
-def test_traffic_none_when_the_source_changed(mode, monkeypatch, tmp_path):
-    _, src, prof_name = bench.DOMINANT[mode]
-    real_open = open
-
-    def fake_open(path, *a, **k):
-        if str(path).endswith(os.path.join("csrc", src)):
-            f = tmp_path / "changed.cu"
-            f.write_bytes(real_open(path, "rb").read() + b"\n// changed\n")
-            return real_open(f, *a, **k)
-        return real_open(path, *a, **k)
-
-    prof = json.load(open(os.path.join(ROOT, "profiles", prof_name)))
-    monkeypatch.setattr("builtins.open", fake_open)
-    assert bench.traffic_for_current_kernel(mode, prof["config"]) is None
+def test_traffic_only_for_the_captured_workload_and_source(mode, monkeypatch, tmp_path):
+    src = _fake_tree(tmp_path, mode, 2, b"// kernel source\n", 123456)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for_current_kernel(mode, 2) == 123456
+    assert bench.traffic_for_current_kernel(mode, 3) is None           # another workload
+    src.write_bytes(b"// kernel source, changed\n")
+    assert bench.traffic_for_current_kernel(mode, 2) is None           # the kernel changed since
+    (tmp_path / "profiles" / bench.DOMINANT[mode][2]).unlink()
+    assert bench.traffic_for_current_kernel(mode, 2) is None           # no capture
