@@ -60,6 +60,7 @@ struct Counters {
   uint64_t seg_total[3];       // executor segments per tier (384 rows, 512 rows, wide)
   uint32_t sub_count[16];      // bin 1 by walk length (k_classify), longest first
   uint32_t sub_cursor[16];
+  unsigned long long exec_live;   // live cells the executors replayed
 };
 
 constexpr uint64_t TRACE_CAP_DEFAULT = 1ull << 30;   // smallest executor arena cap before chunking
@@ -201,6 +202,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   wa.wide_count = &dc->wide_count;
   wa.live_total = &dc->live_total;
   wa.exec_total = &dc->exec_total;
+  wa.exec_live = &dc->exec_live;
   wa.err = &dc->err;
   wa.scratch = ctx->scratch.as<int32_t>();
   wa.scratch_stride = wide_scratch_elems(ctx->p.max_len);
@@ -336,10 +338,9 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
       uint32_t a = 0;
       while (a < n_exec) {
         uint32_t b = a + 1;
+        // (a single extension larger than the cap is a chunk of its own; the
+        // arena below grows to the largest chunk)
         while (b < n_exec && toff[b + 1] - toff[a] <= ctx->trace_cap) ++b;
-        if (toff[b] - toff[a] > ctx->trace_cap && b - a == 1) {
-          // a single extension larger than the cap: grow for it
-        }
         chunks.push_back({a, b});
         a = b;
       }
@@ -662,6 +663,7 @@ fz_status fz_get_stats(fz_ctx* ctx, fz_stats* out) {
   fz_status s = check_device_error(ctx);
   ctx->stats.live_cells = ctx->h_cnt->live_total;
   ctx->stats.exec_cells = ctx->h_cnt->exec_total;
+  ctx->stats.exec_live_cells = ctx->h_cnt->exec_live;
   ctx->stats.launches = ctx->launches;
   ctx->stats.profiled = 0;
   for (float& f : ctx->stats.phase_ms) f = 0.f;
@@ -712,7 +714,7 @@ void fz_destroy(fz_ctx* ctx) {
   delete ctx;
 }
 
-fz_status fz_bench_int_rates(double rates[4]) {
+fz_status fz_bench_int_rates(double rates[FZ_INT_RATES]) {
   if (!rates) return FZ_ERR_ARG;
   return bench_int_rates(rates) == cudaSuccess ? FZ_OK : FZ_ERR_CUDA;
 }

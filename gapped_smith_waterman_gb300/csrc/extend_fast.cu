@@ -215,7 +215,7 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       L.I[r] = Ic;
       L.D[r] = Dc;
       if ((r & 1) == 0) lm = __vimax3_s32(lm, L.H[r], L.H[r + 1]);   // rows r, r+1 are both new
-      if (!TRACE) cnt += alive ? 1u : 0u;                // the replay does not count
+      cnt += alive ? 1u : 0u;
     }
   } else {
     const int32_t itop = __viaddmax_s32(L.I[0], in.ne, L.H[0]);
@@ -245,7 +245,7 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       L.I[r] = Ic;
       L.D[r] = Dc;
       if (r & 1) lm = __vimax3_s32(lm, L.H[r - 1], L.H[r]);           // rows r-1, r are both new
-      if (!TRACE) cnt += alive ? 1u : 0u;
+      cnt += alive ? 1u : 0u;
     }
   }
   return lm;
@@ -477,6 +477,7 @@ __device__ __forceinline__ int ck_stage(Relay<KS>* rb, const int32_t* c, int lan
 // never passes the shift-by-one base either), which held every live cell.
 struct ExecState {
   int32_t b, d, best, T;
+  uint32_t cnt;              // live cells this lane replayed
   bool rowb_alive, top, top_prev;
   Reservoir qr, tr;
 };
@@ -491,7 +492,6 @@ __device__ __forceinline__ void exec_step(LaneState<KS>& L, ExecState& s, StepIn
   const int32_t bn = s.b + (SHIFT ? 1 : 0);
   in.Th = s.T - in.oe;
   uint32_t packed[2] = {packed_base<KA>(0), packed_base<KA>(1)};
-  uint32_t no_cnt = 0;
   if (EDGE) {
     const int32_t rowbase = bn + lane * KA;
     in.vhi = w.m - rowbase;
@@ -499,7 +499,7 @@ __device__ __forceinline__ void exec_step(LaneState<KS>& L, ExecState& s, StepIn
   }
   if (!SHIFT) in.qb = res_take(s.qr, p.q2, p.q_len, w.qg0, w.dir);
   else in.mr_new = s_mrow[res_take(s.tr, p.t2, p.t_len, w.tg0, w.dir)];
-  const int32_t lm = step<KS, KA, true, SHIFT, EDGE>(L, in, lane, no_cnt, packed);
+  const int32_t lm = step<KS, KA, true, SHIFT, EDGE>(L, in, lane, s.cnt, packed);
   store_codes<KA>(tbase + (uint64_t)dn * (WMAX / 2), lane, packed);
   const int32_t wm = __reduce_max_sync(FULL, lm);
   const bool edge_lane = (lane == 0 && L.H[0] >= in.Th) || (lane == 31 && lm >= in.Th);
@@ -591,6 +591,7 @@ __device__ void run_exec(const Params& p, const WorkArgs& wa, uint32_t ext, uint
     s.rowb_alive = lo_c == s.b;
   }
   s.T = threshold(s.best, p.ydrop);
+  s.cnt = 0;
   s.top = false;
   s.top_prev = false;
   res_init(s.qr, p.q2, p.q_len, w.qg0, w.dir, (int64_t)s.d + 1 - s.b);   // query columns entering at row b
@@ -615,7 +616,13 @@ __device__ void run_exec(const Params& p, const WorkArgs& wa, uint32_t ext, uint
     s.top = false;
     s.top_prev = false;
   }
-  if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)(d_stop - (int32_t)sg.w) * (unsigned long long)WMAX);
+  uint64_t tot = s.cnt;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+  if (lane == 0) {
+    atomicAdd(wa.exec_total, (unsigned long long)(d_stop - (int32_t)sg.w) * (unsigned long long)WMAX);
+    atomicAdd(wa.exec_live, (unsigned long long)tot);
+  }
 }
 
 // Inspector sweep with a fixed window of KS rows per lane.  The loop keeps

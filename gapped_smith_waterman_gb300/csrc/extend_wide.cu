@@ -138,7 +138,10 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
   if (TRACE) {
-    if (lane == 0) atomicAdd(wa.exec_total, (unsigned long long)tot);
+    if (lane == 0) {
+      atomicAdd(wa.exec_total, (unsigned long long)tot);
+      atomicAdd(wa.exec_live, (unsigned long long)tot);
+    }
     return;
   }
   if (lane == 0) {

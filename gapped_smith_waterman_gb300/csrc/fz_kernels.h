@@ -22,6 +22,7 @@ struct WorkArgs {
   uint64_t trace_sub;          // executor: subtracted from trace_off (chunked runs)
   unsigned long long* live_total;
   unsigned long long* exec_total;
+  unsigned long long* exec_live;   // executor: live cells replayed
   uint32_t* err;               // device error word (0 = fine)
   int32_t* scratch;            // wide path: per-warp anti-diagonal buffers
   uint64_t scratch_stride;     // int32 elements per warp
@@ -145,6 +146,6 @@ cudaError_t launch_comb(const fz_seed* seeds, uint32_t n_seeds, const fz_result*
                         const uint64_t* off, uint32_t* out_cig, fz_alignment* aln, cudaStream_t st);
 
 // integer pipe microbenchmark (microbench.cu)
-cudaError_t bench_int_rates(double rates[4]);
+cudaError_t bench_int_rates(double rates[FZ_INT_RATES]);
 
 }  // namespace fz

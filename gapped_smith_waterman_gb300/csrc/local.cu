@@ -279,16 +279,24 @@ namespace {
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[256] = {};   // device address of g_noalloc_scratch, per device ordinal
 
-// Resolves the scratch array's device address for the current device (once
-// per device).  The name g_noalloc_scratch in host code is only a host-side
-// stand-in; kernels must be given this address instead.
-cudaError_t noalloc_scratch(int dev, int32_t** out) {
+// Resolves the scratch array's device address for the current device.  The
+// name g_noalloc_scratch in host code is only a host-side stand-in; kernels
+// must be given this address instead.  Outside stream capture the address is
+// looked up again on every call (a context made after cudaDeviceReset gets a
+// new one); while the stream is capturing, the address cached by the last
+// call outside capture is used, and without one the call fails.
+cudaError_t noalloc_scratch(int dev, cudaStream_t st, int32_t** out) {
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t ce = cudaStreamIsCapturing(st, &cs);
+  if (ce != cudaSuccess) return ce;
+  if (cs == cudaStreamCaptureStatusNone) {
     void* ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, fz::g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev] = ptr;
+  } else if (!g_noalloc_ptr[dev]) {
+    return cudaErrorStreamCaptureUnsupported;
   }
   *out = static_cast<int32_t*>(g_noalloc_ptr[dev]);
   return cudaSuccess;
@@ -312,6 +320,10 @@ extern "C" fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_op
   }
   if (amax * (2 * (int64_t)max_len + 1) >= (1ll << 28)) return FZ_ERR_ARG;
   if (n_seeds == 0) return FZ_OK;
+  // an error left pending by earlier, unrelated work is the caller's: report
+  // it without clearing it and before touching the stream
+  if (cudaPeekAtLastError() != cudaSuccess) return FZ_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) { (void)cudaGetLastError(); return FZ_ERR_CUDA; }
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -319,7 +331,7 @@ extern "C" fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_op
     return FZ_ERR_CUDA;
   }
   int32_t* scratch = nullptr;
-  if (noalloc_scratch(dev, &scratch) != cudaSuccess) { (void)cudaGetLastError(); return FZ_ERR_CUDA; }
+  if (noalloc_scratch(dev, st, &scratch) != cudaSuccess) { (void)cudaGetLastError(); return FZ_ERR_CUDA; }
   Params p{};
   p.t2 = d_target2; p.q2 = d_query2; p.t_len = t_len; p.q_len = q_len;
   p.seeds = d_seeds; p.n_seeds = n_seeds;
@@ -332,7 +344,6 @@ extern "C" fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_op
     for (int q = 0; q < 4; ++q) col |= (uint32_t)(sub[q * 4 + t] + 128) << (8 * q);
     mc[t] = col;
   }
-  const cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   // the work counter must start at zero; the spill rows need no clearing
   if (cudaMemsetAsync(scratch, 0, NA_HEAD * sizeof(int32_t), st) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -340,6 +351,6 @@ extern "C" fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_op
   }
   const int grid = sms < NA_MAX_BLOCKS ? sms : NA_MAX_BLOCKS;
   k_local_noalloc<<<grid, WL * 32, 0, st>>>(p, 2 * n_seeds, scratch, d_out, make_uint4(mc[0], mc[1], mc[2], mc[3]));
-  if (cudaGetLastError() != cudaSuccess) return FZ_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FZ_ERR_CUDA;   // this launch's error (none was pending)
   return FZ_OK;
 }

@@ -1,5 +1,6 @@
 // Integer-pipe throughput microbenchmark (sm_103a): whole-GPU op/s of the
-// instructions a Gotoh cell is built from.  Each thread runs CH independent
+// instructions a Gotoh cell is built from, in 32-bit and 16-bit pair forms,
+// and cells/s of the costed cell itself in both forms.  Each thread runs CH independent
 // dependency chains so that issue, not latency, limits the rate.  Chains mix
 // in the loop counter so the compiler cannot fold them.
 #include <cuda_runtime.h>
@@ -69,9 +70,136 @@ __global__ void k_imax(int* out, int b) {
   out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// The 16-bit pair forms the first inspector tier issues: each instruction
+// advances two cells (two 16-bit halves).
+__global__ void k_viaddmax16(int* out, int b) {
+  unsigned a[CH];
+#pragma unroll
+  for (int k = 0; k < CH; ++k) a[k] = threadIdx.x * 0x10001u + k;
+  for (int i = 0; i < ITERS; ++i) {
+#pragma unroll
+    for (int k = 0; k < CH; ++k) a[k] = __viaddmax_s16x2_relu(a[k], (unsigned)b, (unsigned)i);
+  }
+  unsigned s = 0;
+#pragma unroll
+  for (int k = 0; k < CH; ++k) s ^= a[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = (int)s;
+}
+
+__global__ void k_vimax3_16(int* out, int b) {
+  unsigned a[CH];
+#pragma unroll
+  for (int k = 0; k < CH; ++k) a[k] = threadIdx.x * 0x10001u + k;
+  for (int i = 0; i < ITERS; ++i) {
+#pragma unroll
+    for (int k = 0; k < CH; ++k) a[k] = __vimax3_s16x2_relu(a[k], (unsigned)(i + k), (unsigned)b);
+  }
+  unsigned s = 0;
+#pragma unroll
+  for (int k = 0; k < CH; ++k) s ^= a[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = (int)s;
+}
+
+__global__ void k_vadd2(int* out, int b) {
+  unsigned a[CH];
+#pragma unroll
+  for (int k = 0; k < CH; ++k) a[k] = threadIdx.x * 0x10001u + k + (unsigned)b;
+  for (int i = 0; i < ITERS; ++i) {
+#pragma unroll
+    for (int k = 0; k < CH; ++k) a[k] = __vadd2(a[k], (unsigned)i);
+  }
+  unsigned s = 0;
+#pragma unroll
+  for (int k = 0; k < CH; ++k) s ^= a[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = (int)s;
+}
+
+// A 32-bit add written as a multiply-add by a runtime 1 (the form the kernels
+// use to put adds on the FMA pipe).
+__global__ void k_imad(int* out, int b) {
+  int a[CH];
+#pragma unroll
+  for (int k = 0; k < CH; ++k) a[k] = threadIdx.x + k + b;
+  const int one = b - 2;   // 1 at run time (b = 3)
+  for (int i = 0; i < ITERS; ++i) {
+#pragma unroll
+    for (int k = 0; k < CH; ++k) asm volatile("mad.lo.s32 %0, %0, %1, %2;" : "+r"(a[k]) : "r"(one), "r"(i));
+  }
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < CH; ++k) s ^= a[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
+// The costed operations of one Gotoh cell pair in the 16-bit pair form, with
+// independent cells per thread: two add-max (I, D), the diagonal add, the
+// 3-way max and the add for h = S - (o + e).  Cells per second of this loop
+// is the integer-pipe roofline of the pair sweep measured directly (the DPX
+// forms and the packed adds issue on different pipes, so this is not the
+// harmonic mean of the single-operation rates).
+constexpr int CC = 4;   // independent cell chains per thread
+__global__ void k_cellmix16(int* out, int b) {
+  unsigned h[CC], hp[CC], I[CC], D[CC];
+#pragma unroll
+  for (int k = 0; k < CC; ++k) {
+    h[k] = threadIdx.x * 0x10001u + k;
+    hp[k] = h[k] ^ 0x00070007u;
+    I[k] = h[k] + 0x00030003u;
+    D[k] = h[k] + 0x00050005u;
+  }
+  const unsigned ne2 = (unsigned)b * 0x10001u, noe2 = (unsigned)(b + 1) * 0x10001u;
+  for (int i = 0; i < ITERS; ++i) {
+    const unsigned s = (unsigned)i * 0x10001u;
+#pragma unroll
+    for (int k = 0; k < CC; ++k) {
+      I[k] = __viaddmax_s16x2_relu(I[k], ne2, h[k]);
+      D[k] = __viaddmax_s16x2_relu(D[k], ne2, hp[k]);
+      const unsigned g = __vadd2(hp[k], s);
+      const unsigned sv = __vimax3_s16x2_relu(g, I[k], D[k]);
+      hp[k] = h[k];
+      h[k] = __vadd2(sv, noe2);
+    }
+  }
+  unsigned s = 0;
+#pragma unroll
+  for (int k = 0; k < CC; ++k) s ^= h[k] ^ I[k] ^ D[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = (int)s;
+}
+
+// The same cell in 32-bit form (one cell per lane and instruction), adds as
+// multiply-adds by a runtime 1 as the 32-bit sweeps and the local fill write them.
+__global__ void k_cellmix32(int* out, int b) {
+  int h[CC], hp[CC], I[CC], D[CC];
+#pragma unroll
+  for (int k = 0; k < CC; ++k) {
+    h[k] = threadIdx.x + k;
+    hp[k] = h[k] ^ 7;
+    I[k] = h[k] + 3;
+    D[k] = h[k] + 5;
+  }
+  const int one = b - 2, ne = -b, noe = -(b + 1);
+  for (int i = 0; i < ITERS; ++i) {
+#pragma unroll
+    for (int k = 0; k < CC; ++k) {
+      I[k] = __viaddmax_s32(I[k], ne, h[k]);
+      D[k] = __viaddmax_s32(D[k], ne, hp[k]);
+      int g, hn;
+      asm volatile("mad.lo.s32 %0, %1, %2, %3;" : "=r"(g) : "r"(hp[k]), "r"(one), "r"(i));
+      const int sv = __vimax3_s32(g, I[k], D[k]);
+      asm volatile("mad.lo.s32 %0, %1, %2, %3;" : "=r"(hn) : "r"(sv), "r"(one), "r"(noe));
+      hp[k] = h[k];
+      h[k] = hn;
+    }
+  }
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < CC; ++k) s ^= h[k] ^ I[k] ^ D[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 }  // namespace
 
-cudaError_t bench_int_rates(double rates[4]) {
+cudaError_t bench_int_rates(double rates[FZ_INT_RATES]) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -84,8 +212,11 @@ cudaError_t bench_int_rates(double rates[4]) {
   cudaEventCreate(&e0);
   cudaEventCreate(&e1);
   typedef void (*kfn)(int*, int);
-  kfn ks[4] = {k_viaddmax, k_vimax3, k_iadd, k_imax};
-  for (int k = 0; k < 4; ++k) {
+  // operations per thread and loop iteration (cells for the two cell mixes)
+  const double per[FZ_INT_RATES] = {CH, CH, CH, CH, CH, CH, CH, CH, 2.0 * CC, CC};
+  kfn ks[FZ_INT_RATES] = {k_viaddmax, k_vimax3, k_iadd, k_imax, k_viaddmax16, k_vimax3_16, k_vadd2, k_imad,
+                          k_cellmix16, k_cellmix32};
+  for (int k = 0; k < FZ_INT_RATES; ++k) {
     ks[k]<<<blocks, threads>>>(out, 3);
     float best = 1e30f;
     for (int rep = 0; rep < 5; ++rep) {
@@ -97,7 +228,7 @@ cudaError_t bench_int_rates(double rates[4]) {
       cudaEventElapsedTime(&ms, e0, e1);
       if (ms < best) best = ms;
     }
-    rates[k] = (double)blocks * threads * ITERS * CH / (best * 1e-3);
+    rates[k] = (double)blocks * threads * ITERS * per[k] / (best * 1e-3);
   }
   e = cudaGetLastError();
   cudaEventDestroy(e0);

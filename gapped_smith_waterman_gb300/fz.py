@@ -39,7 +39,7 @@ class FzStats(ctypes.Structure):
                 ("bin", ctypes.c_uint32 * 5), ("extensions", ctypes.c_uint32), ("wide", ctypes.c_uint32),
                 ("trace_bytes", ctypes.c_uint64), ("cigar_runs", ctypes.c_uint64), ("launches", ctypes.c_uint32),
                 ("profiled", ctypes.c_uint32), ("phase_ms", ctypes.c_float * 6),
-                ("retried", ctypes.c_uint32)]
+                ("retried", ctypes.c_uint32), ("exec_live_cells", ctypes.c_uint64)]
 
 
 class FzError(RuntimeError):
@@ -167,10 +167,17 @@ def fz_combine(ctx, d_seeds: int, n_seeds: int, d_res: int, d_cigar: int, d_aln:
     return cig.value or 0
 
 
+FZ_INT_RATES = 10
+INT_RATE_NAMES = ("viaddmax", "vimax3", "iadd", "imax", "viaddmax_s16x2", "vimax3_s16x2", "vadd2", "imad",
+                  "cell16_per_s", "cell32_per_s")
+
+
 def fz_bench_int_rates():
-    out = (ctypes.c_double * 4)()
+    """Integer-pipe rates (fz.h lists the entries): op/s, and cells/s of the
+    costed cell in the 16-bit pair and 32-bit forms."""
+    out = (ctypes.c_double * FZ_INT_RATES)()
     _check(None, load().fz_bench_int_rates(out))
-    return {"viaddmax": out[0], "vimax3": out[1], "iadd": out[2], "imax": out[3]}
+    return dict(zip(INT_RATE_NAMES, list(out)))
 
 
 def fz_pair_sweep_used(sub, gap_open: int, gap_extend: int, ydrop: int, mode: int) -> bool:

@@ -83,7 +83,8 @@ typedef struct {
 
 typedef struct {
     uint64_t live_cells;    /* live cells of all inspector sweeps (EXTEND) or m*n cells (LOCAL) */
-    uint64_t exec_cells;    /* window cells the executor recomputed (register-window path) */
+    uint64_t exec_cells;    /* executor trace cells: anti-diagonals replayed x trace row width
+                               (register-window path; live cells on the wide path) */
     uint32_t eager;         /* extensions traced back inside the inspector */
     uint32_t bin[5];        /* executor bins: max(i*, j*) <= 512, 2048, 8192, 32768, 131072 */
     uint32_t extensions;    /* one-sided extensions computed */
@@ -97,6 +98,8 @@ typedef struct {
                                4 CIGAR emission, 5 whole batch */
     uint32_t retried;       /* extensions whose live band outgrew the first register
                                window and resumed in the 512-row one */
+    uint64_t exec_live_cells;   /* live cells the executor replayed (anti-diagonals
+                               1 .. i* + j* of each executor extension) */
 } fz_stats;
 
 /*
@@ -216,13 +219,25 @@ void fz_destroy(fz_ctx* ctx);
  *
  * Scratch (the work counter and the per-warp strip spill rows, about 10 MB)
  * is one file-scope device array of the library: every GPU that loads the
- * library holds it until the process exits.  No cudaMalloc, cudaFree or other
- * allocating call is made.  The first call on a device resolves that array's
- * device address (cudaGetSymbolAddress) for the current device; make that
- * first call before any stream capture.  Every call shares the one array and
- * clears the counter at its start, so calls that overlap on the GPU (different
- * streams, or host threads, on the same device) race and must be serialised
- * by the caller.  Asynchronous on cuda_stream.
+ * library holds it until the process exits.  This function makes no
+ * cudaMalloc, cudaFree or other allocating call.  With CUDA's lazy module
+ * loading (the default) the driver loads the library's device code, array
+ * included, the first time it is used on a device -- normally at the first
+ * call of this function there -- and takes the 10 MB then; make that first
+ * call at start-up, before any stream capture.
+ *
+ * The array's device address is looked up (cudaGetSymbolAddress, current
+ * device) at every call made outside stream capture; a call on a capturing
+ * stream reuses the address found by the last call outside capture on that
+ * device (none yet: FZ_ERR_CUDA).  After cudaDeviceReset, make one call
+ * outside capture before capturing again.
+ *
+ * Every call shares the one array and clears its work counter at the start,
+ * so calls that overlap on the GPU (different streams, or host threads, on
+ * the same device) race and must be serialised by the caller.  Asynchronous
+ * on cuda_stream.  A CUDA error already pending when the call starts (left by
+ * earlier work) is returned as FZ_ERR_CUDA and left pending; nothing is
+ * launched then.
  */
 fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_open, int32_t gap_extend,
                                 int32_t max_len, const uint8_t* d_target2, uint64_t t_len,
@@ -230,17 +245,33 @@ fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_open, int32_t
                                 uint32_t n_seeds, fz_result* d_out, void* cuda_stream);
 
 /*
- * Integer-pipe throughput microbenchmark (whole GPU, current device): op/s of
- * DPX add-max (__viaddmax_s32), DPX 3-way max (__vimax3_s32), 32-bit add and
- * 32-bit max, written to rates[0..3].  Independent dependency chains per
- * thread, every SM busy; synchronises the device.  Used for the roofline.
+ * Integer-pipe throughput microbenchmark (whole GPU, current device), written
+ * to rates[0 .. FZ_INT_RATES-1]:
+ *   0  DPX add-max __viaddmax_s32            op/s (one 32-bit lane each)
+ *   1  DPX 3-way max __vimax3_s32            op/s
+ *   2  32-bit add                            op/s
+ *   3  32-bit max                            op/s
+ *   4  DPX add-max __viaddmax_s16x2_relu     op/s (two 16-bit halves each)
+ *   5  DPX 3-way max __vimax3_s16x2_relu     op/s
+ *   6  packed 16-bit add __vadd2             op/s
+ *   7  32-bit multiply-add by a runtime 1    op/s
+ *   8  cells/s of the costed Gotoh cell in the 16-bit pair form (2 add-max,
+ *      1 3-way max, 2 packed adds per two cells), independent cells
+ *   9  cells/s of the costed Gotoh cell in 32-bit form (2 add-max, 1 3-way
+ *      max, 2 multiply-adds per cell)
+ * Independent dependency chains per thread, every SM busy; synchronises the
+ * device; allocates and frees a small output buffer.  Rates 8 and 9 are the
+ * measured integer-pipe rooflines of the extension sweeps.
  */
-fz_status fz_bench_int_rates(double rates[4]);
+#define FZ_INT_RATES 10
+fz_status fz_bench_int_rates(double rates[FZ_INT_RATES]);
 
 /*
  * Whether a context created by fz_create with these arguments runs the first
- * inspector tier as the 16-bit pair sweep (two cells per 32-bit lane, see the
- * design notes on the inspector): mode FZ_EXTEND, every sub[k] in [-128, 127],
+ * inspector tier as the 16-bit pair sweep (two cells per 32-bit lane: two
+ * window rows kept as 16-bit halves of each register, values relative to the
+ * moving prune threshold, so that each DPX s16x2 instruction advances two
+ * cells): mode FZ_EXTEND, every sub[k] in [-128, 127],
  * a finite ydrop with ydrop + 2048 + 4 (gap_open + gap_extend + max|sub|) <=
  * 30000, gap_open + gap_extend + max|sub| + 16 < 2048, and the environment
  * variable FZ_NO_PAIR unset or "0" (read at the call).  Returns 1 or 0 (0 for

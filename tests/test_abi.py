@@ -46,8 +46,32 @@ def test_struct_layouts_match_header():
     assert W.SEED_DTYPE.itemsize == 24
     assert fz.RESULT_DTYPE.itemsize == 24
     assert fz.ALIGNMENT_DTYPE.itemsize == 48
-    # fields of fz_stats in order, then tail padding to its 8-byte alignment
-    assert ctypes.sizeof(fz.FzStats) == 8 + 8 + 4 + 20 + 4 + 4 + 8 + 8 + 4 + 4 + 24 + 4 + 4
+    # fields of fz_stats in order (4 bytes of padding before the last 8-byte field)
+    assert ctypes.sizeof(fz.FzStats) == 8 + 8 + 4 + 20 + 4 + 4 + 8 + 8 + 4 + 4 + 24 + 4 + 4 + 8
+
+
+def test_struct_offsets_match_a_c_compiler(tmp_path):
+    """The binding's record layouts against the header as a C compiler lays it out."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    fields = [f for f, _ in fz.FzStats._fields_]
+    prog = ['#include <stdio.h>', '#include <stddef.h>', '#include "fz.h"', 'int main(void) {',
+            'printf("%zu\\n", sizeof(fz_stats));']
+    prog += [f'printf("%zu\\n", offsetof(fz_stats, {f}));' for f in fields]
+    prog += ['printf("%zu %zu %zu\\n", sizeof(fz_seed), sizeof(fz_result), sizeof(fz_alignment));', 'return 0; }']
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(prog) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(root, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert int(out[0]) == ctypes.sizeof(fz.FzStats)
+    for k, f in enumerate(fields):
+        assert int(out[1 + k]) == getattr(fz.FzStats, f).offset, f
+    assert out[1 + len(fields)].split() == ["24", "24", "48"]
 
 
 @pytest.mark.parametrize("args", [
