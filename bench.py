@@ -6,12 +6,17 @@ wide-band inspector, length binning, executor and CIGAR emission (every row of
 the hot path).  Inputs are resident in HBM when a step starts; L2 is flushed
 (a 256 MiB write) between timed steps, outside the timed region.
 
-Default workload: 100,000 right extensions in 6,000 bp windows with skewed
-homology lengths (97% of homologies 8-128 bp), HOXD70, gap open 400, extend 30,
-ydrop 9400.  Metric: GCUPS = live DP cells of the inspector sweeps per second
-of the whole step; extensions/s is reported beside it.
+Default workload: the chromosome-scale batch, the largest configuration on one
+GPU -- 1,000,000 seed anchors on a synthetic 50 Mbp target and a query derived
+from it (15% substitutions, 3% indels, 10 kbp block inversions and moves),
+extended on both sides in 6,000 bp windows (2,000,000 one-sided extensions),
+HOXD70, gap open 400, extend 30, ydrop 9400.  --config 1|2|4|5 runs the others.
+Metric: GCUPS = live DP cells of the inspector sweeps per second of the whole
+step; extensions/s is reported beside it.  The roofline line names the kernel
+that took the most time in the timed steps (CUDA events on the library's stream
+around its phases) and divides its own cells by its own time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fz|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fz|reference] [--config C]
 
 Multi-GPU (torchrun): every rank extends its own copy of the batch (weak
 scaling), no collective on the data path; the step time is the max over ranks.
@@ -36,30 +41,56 @@ from gapped_smith_waterman_gb300 import workloads as W  # noqa: E402
 
 METRIC = "GCUPS and seed extensions/s (affine y-drop batch) at 1 GB300; % of DPX roofline"
 # Roofline of the integer pipes: a Gotoh cell in DPX form is 2 add-max + 1 three-way max
-# (64 lanes/clk/SM each on GB300) + 2 adds (128 lanes/clk/SM): 4/64 SM-clocks per lane
-# and cell, i.e. 16 cells/clk/SM with 32-bit lanes; x 152 SMs x 2.07 GHz max SM clock.
-# The first-tier inspector keeps two cells in each 32-bit lane (16-bit halves) when the
-# y-drop range allows it: the same instructions then advance two cells, 32 cells/clk/SM.
-SMS, SM_MAX_GHZ, CELLS_PER_CLK_SM = 152, 2.07, 16.0
-PEAK_GCUPS = SMS * SM_MAX_GHZ * CELLS_PER_CLK_SM
+# (64 lanes/clk/SM each on GB300) + 2 adds (128 lanes/clk/SM): 4/64 SM-clocks per lane and
+# cell, i.e. 16 cells/clk/SM with one 32-bit cell per lane.  The first-tier inspector keeps
+# two cells in each 32-bit lane (16-bit halves) when the y-drop range allows it: the same
+# instructions then advance two cells, 32 cells/clk/SM.  SM count and maximum SM clock are
+# read from the device at run time.
+CELLS_PER_CLK_SM = 16.0
 
-
-# Dominant kernel per mode: (name, source file, committed DRAM-traffic summary).
-DOMINANT = {
-    "extend": ("inspector (register-window sweep; first tier two 16-bit rows per register)", "extend_fast.cu",
-               "inspector_traffic.json"),
-    "local": ("local fill (k_local)", "local.cu", "local_traffic.json"),
+# Phases of one batch (fz_stats.phase_ms) -> the kernel that runs in it: its name, source,
+# cells (an fz_stats field), whether it computes two cells per lane when the pair sweep is
+# on, and the committed DRAM-traffic summary of that kernel.
+PHASES = {
+    0: ("inspector (register-window sweep; first tier two 16-bit rows per register)", "extend_fast.cu",
+        "live_cells", True, "inspector_traffic.json"),
+    1: ("inspector, wide band (k_wide<0>)", "extend_wide.cu", "live_cells", False, None),
+    3: ("executor (k_extend<K,1,*> replay with 4-bit direction codes)", "extend_fast.cu",
+        "exec_live_cells", False, "executor_traffic.json"),
+    4: ("traceback walk and records (k_emit_*)", "pipeline.cu", None, False, None),
 }
+LOCAL_KERNEL = ("local fill (k_local)", "local.cu", "live_cells", False, "local_traffic.json")
+
+
+def device_peaks(dev_index: int):
+    """SM count (CUDA device properties) and maximum SM clock in GHz (nvidia-smi,
+    else the driver's measured-peaks file, else GB300's nominal 2.07 GHz)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(dev_index), "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20).stdout
+        return sms, float(out.strip().splitlines()[0]) / 1e3, "nvidia-smi clocks.max.sm"
+    except Exception:
+        pass
+    try:
+        return sms, json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["sm_max_mhz"] / 1e3, \
+            "MEASURED_PEAKS.json sm_max_mhz"
+    except Exception:
+        return sms, 2.07, "nominal GB300 maximum"
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["fz", "reference"], default="fz")
-    ap.add_argument("--config", type=int, default=2, help="workload id (1-5); default: the 100k x 6 kbp batch")
+    ap.add_argument("--config", type=int, default=3,
+                    help="workload id (1-5); default: 3, 1M two-sided anchors on a 50 Mbp pair")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="bounded oracle sample for cpu_baseline")
+    ap.add_argument("--ref-step-seconds", type=float, default=6.0,
+                    help="reference arm: oracle time per step (sets its seeds per step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seeds", type=int, default=0, help="use only the first N seeds (profiling captures)")
@@ -121,34 +152,65 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(w, seconds: float):
-    """The oracle, as it stands, on a bounded seeded sample of the same workload,
-    all host cores (a pthread pool over independent extensions)."""
+def cpu_model() -> str:
+    """Host CPU model (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_sample(w, rng, seconds, threads):
+    """A seeded sample of the workload's seeds sized to about `seconds` of oracle
+    time on `threads` threads; returns (GCUPS, extensions/s, description)."""
     import oracle
-    cores = os.cpu_count() or 1
-    rng = np.random.default_rng(123)
-    probe = np.sort(rng.choice(len(w.seeds), size=min(len(w.seeds), 64), replace=False))
+    probe = np.sort(rng.choice(len(w.seeds), size=min(len(w.seeds), max(8, 4 * threads)), replace=False))
     t0 = time.perf_counter()
-    res, _, _ = oracle.extend_batch(w, seeds=w.seeds[probe], nthreads=cores)
+    oracle.extend_batch(w, seeds=w.seeds[probe], nthreads=threads)
     dt = max(time.perf_counter() - t0, 1e-3)
-    n = int(min(len(w.seeds), max(64, len(probe) * seconds / dt)))
+    n = int(min(len(w.seeds), max(len(probe), len(probe) * seconds / dt)))
     idx = np.sort(rng.choice(len(w.seeds), size=n, replace=False))
     t0 = time.perf_counter()
-    res, _, _ = oracle.extend_batch(w, seeds=w.seeds[idx], nthreads=cores)
+    res, _, _ = oracle.extend_batch(w, seeds=w.seeds[idx], nthreads=threads)
     dt = time.perf_counter() - t0
     cells = int(res["live_cells"].sum())
-    return {"value": cells / dt / 1e9, "unit": "GCUPS", "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {len(w.seeds)} seeds (seeded), {cells} live cells, {dt:.1f} s",
-            "extensions_per_s": int(np.count_nonzero(w.seeds[idx]["side"] & 1) +
-                                    np.count_nonzero(w.seeds[idx]["side"] & 2)) / dt}
+    side = w.seeds["side"][idx]
+    nx = int(np.count_nonzero(side & 1) + np.count_nonzero(side & 2))
+    return cells / dt / 1e9, nx / dt, f"{n} of {len(w.seeds)} seeds (seeded), {cells} live cells, {dt:.1f} s"
 
 
-def traffic_for_current_kernel(mode, config):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, if it was taken on this workload and its source has not changed
-    since the capture; else None."""
+def cpu_baseline(w, seconds: float):
+    """The oracle, as it stands, on bounded seeded samples of the same workload:
+    on all host cores (a pthread pool over independent extensions) and on one
+    thread."""
+    cores = os.cpu_count() or 1
+    v, xs, desc = _oracle_sample(w, np.random.default_rng(123), seconds, cores)
+    v1, xs1, desc1 = _oracle_sample(w, np.random.default_rng(124), max(2.0, seconds / 3), 1)
+    return {"value": v, "unit": "GCUPS", "cores": cores, "kind": "oracle", "sample": desc,
+            "extensions_per_s": xs, "cpu_model": cpu_model(),
+            "single_thread": {"value": v1, "unit": "GCUPS", "cores": 1, "extensions_per_s": xs1,
+                              "sample": desc1}}
+
+
+def traffic_for_kernel(kernel, config):
+    """DRAM bytes per step of the named kernel from its committed ncu summary, if
+    it was taken on this workload and its source has not changed since the
+    capture; else None."""
     import hashlib
-    _, src_name, prof_name = DOMINANT[mode]
+    _, src_name, _, _, prof_name = kernel
+    if not prof_name:
+        return None
     try:
         prof = json.load(open(os.path.join(ROOT, "profiles", prof_name)))
         src = open(os.path.join(ROOT, "gapped_smith_waterman_gb300", "csrc", src_name), "rb").read()
@@ -160,13 +222,20 @@ def traffic_for_current_kernel(mode, config):
 
 
 def run_reference(args, ws, rank):
+    """The reference arm: the oracle, as it stands, on the host cores.  Each step
+    extends a fresh seeded sample of the workload's seeds, sized by a probe so
+    that one step takes about --ref-step-seconds."""
     if rank != 0:
         return
     w = W.make(args.config)
     import oracle
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(321)
-    n = min(len(w.seeds), 200)
+    probe = np.sort(rng.choice(len(w.seeds), size=min(len(w.seeds), 2 * cores), replace=False))
+    t0 = time.perf_counter()
+    oracle.extend_batch(w, seeds=w.seeds[probe], nthreads=cores)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(len(w.seeds), max(cores, len(probe) * args.ref_step_seconds / dt)))
     times, cells = [], 0
     for step in range(args.warmup + args.steps):
         idx = np.sort(rng.choice(len(w.seeds), size=n, replace=False))
@@ -183,7 +252,7 @@ def run_reference(args, ws, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
             "config": {"workload": w.name, "note": w.note, "sample_per_step": f"{n} seeds"},
             "cpu_baseline": {"value": v, "unit": "GCUPS", "cores": cores, "kind": "oracle",
-                             "sample": f"{n} random seeds per step of {len(w.seeds)}"},
+                             "sample": f"{n} random seeds per step of {len(w.seeds)}", "cpu_model": cpu_model()},
             "e2e": {"value": v, "unit": "GCUPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -223,7 +292,9 @@ def main():
         ext.run(d_t, w.target.size, d_q, w.query.size, d_s, len(seeds), d_out)
         ext.stats()
     sampler = ClockSampler(lrank)
-    step_ms, insp_ms, cells, launches, exts = [], [], 0, 0, 0
+    step_ms, cells, launches, exts = [], 0, 0, 0
+    phase_tot = [0.0] * 6                      # device ms per phase over the timed steps
+    stat_tot = {"live_cells": 0, "exec_live_cells": 0}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
@@ -237,7 +308,10 @@ def main():
         e1.record(stream)
         st = ext.stats()                       # synchronises the stream
         step_ms.append(e0.elapsed_time(e1))
-        insp_ms.append(st.phase_ms[0])
+        for k in range(6):
+            phase_tot[k] += st.phase_ms[k]
+        stat_tot["live_cells"] += st.live_cells
+        stat_tot["exec_live_cells"] += st.exec_live_cells
         cells += st.live_cells
         launches += st.launches
         exts += st.extensions if w.mode == 0 else n_req
@@ -252,15 +326,15 @@ def main():
         tot_ms = float(t.item())
     value = ws * cells / (tot_ms * 1e-3) / 1e9
     ext_per_s = ws * exts / (tot_ms * 1e-3)
-    insp_gcups = cells / (sum(insp_ms) * 1e-3) / 1e9 if sum(insp_ms) > 0 else None
 
     e2e = None
     if not args.no_e2e:
         pin = lambda a: torch.from_numpy(a).pin_memory().numpy()  # noqa: E731
         h_t, h_q, h_s = pin(t2), pin(q2), pin(seeds.view(np.uint8)).view(W.SEED_DTYPE)
         h_out = np.zeros(2 * len(seeds), fz.RESULT_DTYPE)
-        st0 = ext.stats()
-        h_cig = pin(np.zeros(int(st0.cigar_runs) + 16, np.uint32))
+        res_dev = np.frombuffer(d_out[:2 * len(seeds) * fz.RESULT_DTYPE.itemsize].cpu().numpy().tobytes(),
+                                dtype=fz.RESULT_DTYPE)
+        h_cig = pin(np.zeros(int(res_dev["cigar_len"].astype(np.int64).sum()) + 16, np.uint32))   # runs written
         ne, e2e_s, e2e_cells, d2h = max(1, min(args.steps, 5)), 0.0, 0, 0
         fz.fz_extend_batch_host(ext.ctx, h_t, w.target.size, h_q, w.query.size, h_s, h_out, h_cig, stream.cuda_stream)
         for _ in range(ne):
@@ -284,13 +358,24 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and ws == 1:
         cpu = cpu_baseline(w, args.cpu_seconds)
-    mode = "local" if w.mode == W.MODE_LOCAL else "extend"
-    cells_per_lane = 2 if fz.fz_pair_sweep_used(w.sub, w.gap_open, w.gap_extend, w.ydrop, w.mode) else 1
-    peak = PEAK_GCUPS * cells_per_lane
+    # the roofline names the kernel with the largest share of the timed steps
+    if w.mode == W.MODE_LOCAL:
+        kernel, kphase = LOCAL_KERNEL, 0
+    else:
+        kphase = max(PHASES, key=lambda k: phase_tot[k])
+        if PHASES[kphase][2] is None:         # (the walk has no cell count: report the sweeps)
+            kphase = 0
+        kernel = PHASES[kphase]
+    kname, _, kcells_field, kpair, _ = kernel
+    pair = fz.fz_pair_sweep_used(w.sub, w.gap_open, w.gap_extend, w.ydrop, w.mode)
+    cells_per_lane = 2 if (pair and kpair) else 1
+    sms, ghz, clock_src = device_peaks(lrank)
+    peak = sms * ghz * CELLS_PER_CLK_SM * cells_per_lane
+    k_ms = phase_tot[kphase]
+    achieved = stat_tot[kcells_field] / (k_ms * 1e-3) / 1e9 if k_ms > 0 else None
     measured_peak = None
     if rates:
-        r = rates
-        measured_peak = cells_per_lane / (2.0 / r["viaddmax"] + 1.0 / r["vimax3"] + 2.0 / r["iadd"]) / 1e9
+        measured_peak = (rates["cell16_per_s"] if cells_per_lane == 2 else rates["cell32_per_s"]) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GCUPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -300,21 +385,28 @@ def main():
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{ws}"},
         "extensions_per_s": ext_per_s,
         "live_cells_per_step": int(cells / args.steps),
-        "roofline": {"bound": "alu", "kernel": DOMINANT[mode][0],
-                     "achieved": insp_gcups, "peak": peak, "unit": "Gcell/s",
-                     "frac": (insp_gcups / peak) if insp_gcups else None,
-                     "peak_basis": (f"152 SM x 2.07 GHz x {16 * cells_per_lane} cells/clk/SM (2 DPX add-max + 1 DPX "
-                                    "max3 at 64 lanes/clk, 2 adds at 128 lanes/clk per lane-cell; "
-                                    + ("two 16-bit cells per 32-bit lane: the first-tier pair sweep)" if cells_per_lane == 2
-                                       else "one 32-bit cell per lane)")),
+        "roofline": {"bound": "alu", "kernel": kname,
+                     "achieved": achieved, "peak": peak, "unit": "Gcell/s",
+                     "frac": (achieved / peak) if achieved else None,
+                     "cells": f"{kcells_field} of the timed steps / the kernel's phase time (CUDA events)",
+                     "kernel_share_of_step": k_ms / tot_ms if tot_ms > 0 else None,
+                     "peak_basis": (f"{sms} SM x {ghz:.3f} GHz ({clock_src}) x {16 * cells_per_lane} cells/clk/SM "
+                                    "(2 DPX add-max + 1 DPX max3 at 64 lanes/clk, 2 adds at 128 lanes/clk per "
+                                    "lane-cell; " + ("two 16-bit cells per 32-bit lane: the first-tier pair sweep)"
+                                                     if cells_per_lane == 2 else "one 32-bit cell per lane)")),
                      "peak_measured_int_pipes": measured_peak,
+                     "frac_of_measured": (achieved / measured_peak) if (achieved and measured_peak) else None,
+                     "measured_basis": "fz_bench_int_rates cells/s of the costed cell (" +
+                                       ("16-bit pair form)" if cells_per_lane == 2 else "32-bit form)"),
                      "int_rates_gops": {k: v / 1e9 for k, v in (rates or {}).items()},
-                     "traffic": traffic_for_current_kernel(mode, args.config),
-                     "kernel_ms_per_step": sum(insp_ms) / args.steps},
-        "phase_ms_last_step": [round(x, 4) for x in st.phase_ms],
+                     "traffic": traffic_for_kernel(kernel, args.config),
+                     "traffic_unit": "DRAM bytes per step of this kernel (ncu, scaled to the full batch)",
+                     "kernel_ms_per_step": k_ms / args.steps},
+        "phase_ms_per_step": [round(x / args.steps, 4) for x in phase_tot],
         "phases": "inspector, wide inspector, bins+scans, executors, traceback+records, whole batch",
         "batch_stats": {"eager": int(st.eager), "bins": [int(b) for b in st.bin], "wide": int(st.wide), "retried_512": int(st.retried),
-                        "executor_window_cells": int(st.exec_cells), "trace_bytes": int(st.trace_bytes),
+                        "executor_window_cells": int(st.exec_cells), "executor_live_cells": int(st.exec_live_cells),
+                        "trace_bytes": int(st.trace_bytes),
                         "cigar_slot_runs": int(st.cigar_runs)},
         "gpu_launches": int(launches),
         "clocks": clocks,

@@ -72,9 +72,13 @@ def test_clock_sampler_without_samples():
     assert s.stop()["reasons"] == ["clocks not sampled"]
 
 
+def _kernel(mode):
+    return bench.LOCAL_KERNEL if mode == "local" else bench.PHASES[0]
+
+
 def _fake_tree(tmp_path, mode, config, src_bytes, traffic):
     import hashlib
-    _, src, prof_name = bench.DOMINANT[mode]
+    _, src, _, _, prof_name = _kernel(mode)
     (tmp_path / "profiles").mkdir(exist_ok=True)
     csrc = tmp_path / "gapped_smith_waterman_gb300" / "csrc"
     csrc.mkdir(parents=True, exist_ok=True)
@@ -89,9 +93,20 @@ def _fake_tree(tmp_path, mode, config, src_bytes, traffic):
 def test_traffic_only_for_the_captured_workload_and_source(mode, monkeypatch, tmp_path):
     src = _fake_tree(tmp_path, mode, 2, b"// kernel source\n", 123456)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.traffic_for_current_kernel(mode, 2) == 123456
-    assert bench.traffic_for_current_kernel(mode, 3) is None           # another workload
+    k = _kernel(mode)
+    assert bench.traffic_for_kernel(k, 2) == 123456
+    assert bench.traffic_for_kernel(k, 3) is None           # another workload
     src.write_bytes(b"// kernel source, changed\n")
-    assert bench.traffic_for_current_kernel(mode, 2) is None           # the kernel changed since
-    (tmp_path / "profiles" / bench.DOMINANT[mode][2]).unlink()
-    assert bench.traffic_for_current_kernel(mode, 2) is None           # no capture
+    assert bench.traffic_for_kernel(k, 2) is None           # the kernel changed since
+    (tmp_path / "profiles" / k[4]).unlink()
+    assert bench.traffic_for_kernel(k, 2) is None           # no capture
+
+
+def test_every_phase_kernel_names_a_source_file():
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for k in list(bench.PHASES.values()) + [bench.LOCAL_KERNEL]:
+        assert os.path.exists(os.path.join(root, "gapped_smith_waterman_gb300", "csrc", k[1])), k
+
+
+def test_cpu_model_is_a_nonempty_string():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
