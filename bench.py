@@ -42,24 +42,36 @@ from gapped_smith_waterman_gb300 import workloads as W  # noqa: E402
 METRIC = "GCUPS and seed extensions/s (affine y-drop batch) at 1 GB300; % of DPX roofline"
 # Roofline of the integer pipes: a Gotoh cell in DPX form is 2 add-max + 1 three-way max
 # (64 lanes/clk/SM each on GB300) + 2 adds (128 lanes/clk/SM): 4/64 SM-clocks per lane and
-# cell, i.e. 16 cells/clk/SM with one 32-bit cell per lane.  The first-tier inspector keeps
-# two cells in each 32-bit lane (16-bit halves) when the y-drop range allows it: the same
-# instructions then advance two cells, 32 cells/clk/SM.  SM count and maximum SM clock are
-# read from the device at run time.
-CELLS_PER_CLK_SM = 16.0
+# cell, i.e. 16 cells/clk/SM with one 32-bit cell per lane ("32").  The first-tier inspector
+# keeps two cells in each 32-bit lane (16-bit halves) when the y-drop range allows it: the
+# same instructions then advance two cells, 32 cells/clk/SM ("pair").  The traced pair sweep
+# also decides each cell's four direction bits (4 packed subtractions per two cells, at
+# 128 lanes/clk/SM): 6/64 SM-clocks per lane and two cells, 64/3 cells/clk/SM ("traced").
+# SM count and maximum SM clock are read from the device at run time.
+CELLS_PER_CLK_SM = {"32": 16.0, "pair": 32.0, "traced": 64.0 / 3.0}
+MEASURED_RATE = {"32": "cell32_per_s", "pair": "cell16_per_s", "traced": "cell16_traced_per_s"}
+CELL_BASIS = {"32": "2 DPX add-max + 1 DPX max3 at 64 lanes/clk, 2 adds at 128 lanes/clk, one 32-bit cell per lane",
+              "pair": "2 DPX add-max + 1 DPX max3 at 64 lanes/clk, 2 adds at 128 lanes/clk per lane, two 16-bit "
+                      "cells per lane (the first-tier pair sweep)",
+              "traced": "2 DPX add-max + 1 DPX max3 at 64 lanes/clk, 2 adds + 4 direction tests at 128 lanes/clk "
+                        "per lane, two 16-bit cells per lane (the traced pair sweep)"}
 
-# Phases of one batch (fz_stats.phase_ms) -> the kernel that runs in it: its name, source,
-# cells (an fz_stats field), whether it computes two cells per lane when the pair sweep is
-# on, and the committed DRAM-traffic summary of that kernel.
+# Phases of one batch (fz_stats.phase_ms, index 6 = fz_stats.traced_ms) -> the kernel that
+# runs in it: its name, source, cells (an fz_stats field, or a difference of two), its cell
+# kind (pair kinds fall back to "32" when the pair sweep is off), and the committed
+# DRAM-traffic summary of that kernel.
 PHASES = {
+    6: ("traced pair sweep (k_pair<true>: inspector that also stores direction codes and walks its best "
+        "cell back; the extensions predicted long)", "extend_fast.cu", "traced_live_cells", "traced",
+        "traced_traffic.json"),
     0: ("inspector (register-window sweep; first tier two 16-bit rows per register)", "extend_fast.cu",
-        "live_cells", True, "inspector_traffic.json"),
-    1: ("inspector, wide band (k_wide<0>)", "extend_wide.cu", "live_cells", False, None),
+        "plain_live_cells", "pair", "inspector_traffic.json"),
+    1: ("inspector, wide band (k_wide<0>)", "extend_wide.cu", "live_cells", "32", None),
     3: ("executor (k_extend<K,1,*> replay with 4-bit direction codes)", "extend_fast.cu",
-        "exec_live_cells", False, "executor_traffic.json"),
-    4: ("traceback walk and records (k_emit_*)", "pipeline.cu", None, False, None),
+        "exec_live_cells", "32", "executor_traffic.json"),
+    4: ("traceback walk and records (k_emit_*)", "pipeline.cu", None, "32", None),
 }
-LOCAL_KERNEL = ("local fill (k_local)", "local.cu", "live_cells", False, "local_traffic.json")
+LOCAL_KERNEL = ("local fill (k_local)", "local.cu", "live_cells", "32", "local_traffic.json")
 
 
 def device_peaks(dev_index: int):
@@ -293,8 +305,8 @@ def main():
         ext.stats()
     sampler = ClockSampler(lrank)
     step_ms, cells, launches, exts = [], 0, 0, 0
-    phase_tot = [0.0] * 6                      # device ms per phase over the timed steps
-    stat_tot = {"live_cells": 0, "exec_live_cells": 0}
+    phase_tot = [0.0] * 7                      # device ms per phase over the timed steps (6: traced sweep)
+    stat_tot = {"live_cells": 0, "exec_live_cells": 0, "traced_live_cells": 0, "plain_live_cells": 0}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         dist.barrier()
@@ -310,8 +322,11 @@ def main():
         step_ms.append(e0.elapsed_time(e1))
         for k in range(6):
             phase_tot[k] += st.phase_ms[k]
+        phase_tot[6] += st.traced_ms
         stat_tot["live_cells"] += st.live_cells
         stat_tot["exec_live_cells"] += st.exec_live_cells
+        stat_tot["traced_live_cells"] += st.traced_live_cells
+        stat_tot["plain_live_cells"] += st.live_cells - st.traced_live_cells
         cells += st.live_cells
         launches += st.launches
         exts += st.extensions if w.mode == 0 else n_req
@@ -366,16 +381,15 @@ def main():
         if PHASES[kphase][2] is None:         # (the walk has no cell count: report the sweeps)
             kphase = 0
         kernel = PHASES[kphase]
-    kname, _, kcells_field, kpair, _ = kernel
+    kname, _, kcells_field, kind, _ = kernel
     pair = fz.fz_pair_sweep_used(w.sub, w.gap_open, w.gap_extend, w.ydrop, w.mode)
-    cells_per_lane = 2 if (pair and kpair) else 1
+    if kind == "pair" and not pair:
+        kind = "32"
     sms, ghz, clock_src = device_peaks(lrank)
-    peak = sms * ghz * CELLS_PER_CLK_SM * cells_per_lane
+    peak = sms * ghz * CELLS_PER_CLK_SM[kind]
     k_ms = phase_tot[kphase]
     achieved = stat_tot[kcells_field] / (k_ms * 1e-3) / 1e9 if k_ms > 0 else None
-    measured_peak = None
-    if rates:
-        measured_peak = (rates["cell16_per_s"] if cells_per_lane == 2 else rates["cell32_per_s"]) / 1e9
+    measured_peak = rates[MEASURED_RATE[kind]] / 1e9 if rates else None
     line = {
         "metric": METRIC, "value": value, "unit": "GCUPS", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -390,21 +404,20 @@ def main():
                      "frac": (achieved / peak) if achieved else None,
                      "cells": f"{kcells_field} of the timed steps / the kernel's phase time (CUDA events)",
                      "kernel_share_of_step": k_ms / tot_ms if tot_ms > 0 else None,
-                     "peak_basis": (f"{sms} SM x {ghz:.3f} GHz ({clock_src}) x {16 * cells_per_lane} cells/clk/SM "
-                                    "(2 DPX add-max + 1 DPX max3 at 64 lanes/clk, 2 adds at 128 lanes/clk per "
-                                    "lane-cell; " + ("two 16-bit cells per 32-bit lane: the first-tier pair sweep)"
-                                                     if cells_per_lane == 2 else "one 32-bit cell per lane)")),
+                     "peak_basis": (f"{sms} SM x {ghz:.3f} GHz ({clock_src}) x {CELLS_PER_CLK_SM[kind]:.2f} "
+                                    f"cells/clk/SM ({CELL_BASIS[kind]})"),
                      "peak_measured_int_pipes": measured_peak,
                      "frac_of_measured": (achieved / measured_peak) if (achieved and measured_peak) else None,
-                     "measured_basis": "fz_bench_int_rates cells/s of the costed cell (" +
-                                       ("16-bit pair form)" if cells_per_lane == 2 else "32-bit form)"),
+                     "measured_basis": f"fz_bench_int_rates {MEASURED_RATE[kind]} (the costed cell loop)",
                      "int_rates_gops": {k: v / 1e9 for k, v in (rates or {}).items()},
                      "traffic": traffic_for_kernel(kernel, args.config),
                      "traffic_unit": "DRAM bytes per step of this kernel (ncu, scaled to the full batch)",
                      "kernel_ms_per_step": k_ms / args.steps},
         "phase_ms_per_step": [round(x / args.steps, 4) for x in phase_tot],
-        "phases": "inspector, wide inspector, bins+scans, executors, traceback+records, whole batch",
-        "batch_stats": {"eager": int(st.eager), "bins": [int(b) for b in st.bin], "wide": int(st.wide), "retried_512": int(st.retried),
+        "phases": ("plain inspector, wide inspector, bins+scans, executors, traceback+records, whole batch, "
+                   "traced sweep (with the work order)"),
+        "batch_stats": {"eager": int(st.eager), "bins": [int(b) for b in st.bin], "traced": int(st.traced),
+                        "wide": int(st.wide), "retried_512": int(st.retried),
                         "executor_window_cells": int(st.exec_cells), "executor_live_cells": int(st.exec_live_cells),
                         "trace_bytes": int(st.trace_bytes),
                         "cigar_slot_runs": int(st.cigar_runs)},

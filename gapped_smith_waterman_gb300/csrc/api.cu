@@ -46,7 +46,7 @@ struct Counters {
   uint64_t cig_total;
   uint64_t cig_packed;         // runs actually written (host-copy packing)
   uint64_t comb_total;         // runs of the combined two-sided CIGARs
-  uint32_t work[8];            // dynamic work counters: 0..2 inspectors, 3..5 executors
+  uint32_t work[8];            // dynamic work counters: 0..2 inspectors, 3..5 executors, 6 traced sweep
   uint32_t retry_count;        // extensions retried with the 512-row window
   uint32_t wide_count;
   uint32_t err;
@@ -54,13 +54,16 @@ struct Counters {
   uint32_t bin_cursor[8];
   uint32_t ckpt_used;          // window checkpoint slots taken (may exceed the pool)
   uint32_t pad_;
-  uint32_t order_hist[17];     // inspector order: extensions per key
-  uint32_t order_cursor[17];
-  uint32_t pad2_[2];
+  uint32_t order_hist[34];     // inspector order: extensions per key (17.. predicted long)
+  uint32_t order_cursor[34];
+  uint32_t n_long;             // extensions predicted long (the traced sweep's list)
+  uint32_t pad2_;
   uint64_t seg_total[3];       // executor segments per tier (384 rows, 512 rows, wide)
   uint32_t sub_count[16];      // bin 1 by walk length (k_classify), longest first
   uint32_t sub_cursor[16];
   unsigned long long exec_live;   // live cells the executors replayed
+  unsigned long long truns_used;  // runs the traced sweep asked for in its arena
+  unsigned long long traced_live; // live cells of the traced sweep
 };
 
 constexpr uint64_t TRACE_CAP_DEFAULT = 1ull << 30;   // smallest executor arena cap before chunking
@@ -81,6 +84,12 @@ struct fz_ctx {
   DevBuf cigar, cigar_packed, trace, scratch, spill;
   DevBuf ckpt, seg_cnt, seg;         // window checkpoints, executor segments
   DevBuf comb_off, comb_cig;         // two-sided alignments (fz_combine)
+  DevBuf tpool, truns;               // traced sweep: per-warp trace slots, run arena
+  bool traced_ok = false;            // the traced sweep runs (pair sweep, windows small enough)
+  int grid_traced = 0;
+  uint32_t tslot_rows = 0;
+  uint64_t tslot_bytes = 0;
+  uint64_t truns_demand = 0;         // runs the last batch's traced sweep asked for
   DevBuf in_t, in_q, in_seeds, out_res;
   Counters* h_cnt = nullptr;         // pinned
   cudaStream_t last_stream = nullptr;
@@ -95,8 +104,8 @@ struct fz_ctx {
   bool local_use_smem = true;
   uint32_t launches = 0;
   bool profiling = false;
-  cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
-  bool ev_set[6] = {false, false, false, false, false, false};
+  cudaEvent_t ev[7] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool ev_set[7] = {false, false, false, false, false, false, false};
 };
 
 namespace {
@@ -222,8 +231,10 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   mark(ctx, 0, st);
   if (ctx->fast_ok) {
     // 384-row window for every extension; retries with 512 rows; then the wide band
+    // the traced sweep runs when at least 4 extensions per resident warp are predicted long
+    const uint32_t min_long = ctx->traced_ok ? 4u * 4u * (uint32_t)ctx->grid_traced : 0xffffffffu;
     CU(launch_order(ctx->p, n_ext, ctx->order_key.as<uint8_t>(), dc->order_hist, dc->order_cursor,
-                    ctx->order_list.as<uint32_t>(), st));
+                    ctx->order_list.as<uint32_t>(), &dc->n_long, min_long, st));
     ctx->launches += 2;
     WorkArgs a = wa;
     a.list = ctx->order_list.as<uint32_t>();
@@ -231,6 +242,30 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
     a.counter = &dc->work[0];
     a.ovf_list = ctx->retry_list.as<uint32_t>();
     a.ovf_count = &dc->retry_count;
+    if (ctx->traced_ok) {
+      // the extensions predicted long (the head of the work list) run the traced
+      // sweep, the rest the plain one
+      CU(ctx->tpool.ensure(ctx->tslot_bytes * (uint64_t)ctx->grid_traced * 4u));
+      uint64_t want = std::max<uint64_t>(ctx->truns_demand + ctx->truns_demand / 4, 256ull * n_ext + 4096);
+      // testing: FZ_TRUNS_CAP limits the arena (extensions beyond it go to the executor)
+      const char* tc = getenv("FZ_TRUNS_CAP");
+      if (tc) want = strtoull(tc, nullptr, 10);
+      CU(ctx->truns.ensure(std::max<uint64_t>(want, 1) * 4));
+      WorkArgs t = a;
+      t.n_work_dev = &dc->n_long;
+      t.counter = &dc->work[6];
+      t.tpool = ctx->tpool.as<uint8_t>();
+      t.tslot_bytes = ctx->tslot_bytes;
+      t.tslot_rows = ctx->tslot_rows;
+      t.truns = ctx->truns.as<uint32_t>();
+      t.truns_cap = tc ? want : ctx->truns.bytes / 4;
+      t.truns_used = &dc->truns_used;
+      t.traced_live = &dc->traced_live;
+      CU(launch_inspect_traced(ctx->p, t, ctx->grid_traced, st));
+      mark(ctx, 6, st);
+      a.list_base_dev = &dc->n_long;
+      ctx->launches += 1;
+    }
     CU(launch_inspect_fast(0, ctx->p, a, ctx->grid_fast[0], st));
     WorkArgs b = wa;
     b.list = ctx->retry_list.as<uint32_t>();
@@ -309,6 +344,8 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   const uint64_t seg_base[4] = {0, hc.seg_total[0], hc.seg_total[0] + hc.seg_total[1],
                                 hc.seg_total[0] + hc.seg_total[1] + hc.seg_total[2]};
   const uint64_t n_seg = seg_base[3];
+  ctx->truns_demand = std::max<uint64_t>(ctx->truns_demand, hc.truns_used);
+  ctx->stats.traced = hc.bin_count[6];
   if (wa.ckpt && hc.ckpt_used > wa.ckpt_cap)   // checkpoints were dropped: a larger pool next batch
     ctx->ckpt_demand = std::max<uint64_t>(ctx->ckpt_demand, (uint64_t)hc.ckpt_used + hc.ckpt_used / 4);
   if (n_exec) {
@@ -362,6 +399,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   ea.local = 0;
   ea.oe = ctx->p.oe;
   ea.max_sub = ctx->max_sub;
+  ea.truns = ctx->truns.as<uint32_t>();
   bool first_chunk = true;
   for (auto& c : chunks) {
     const uint64_t sub = toff.empty() ? 0 : toff[c.first];
@@ -397,6 +435,10 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   mark(ctx, 4, st);
   CU(launch_emit_direct(ea, st));
   ctx->launches += 1;
+  if (ctx->traced_ok && hc.bin_count[6]) {
+    CU(launch_emit_traced(ea, st));
+    ctx->launches += 1;
+  }
   if (chunks.size() == 1) {
     EmitArgs ex = ea;
     ex.exec_begin = 0;
@@ -497,6 +539,24 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     ctx->grid_fast_trace[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, true, false);
   }
   ctx->grid_wide = ctx->sms;
+  {
+    // traced sweep: one trace slot per resident warp, enough rows for the
+    // longest sweep (anti-diagonals 0 .. 2 max_len); on when the pool fits in a
+    // quarter of the free device memory (and FZ_TRACED is not "0")
+    const char* tv = getenv("FZ_TRACED");
+    const bool want = p.pair_ok && mode == FZ_EXTEND && !(tv && *tv == '0');
+    ctx->grid_traced = ctx->sms * traced_blocks_per_sm();
+    ctx->tslot_rows = (uint32_t)(2 * (int64_t)max_len + 2);
+    ctx->tslot_bytes = ((uint64_t)ctx->tslot_rows * 264u + 255u) & ~uint64_t(255);
+    size_t fr = 0, tot = 0;
+    if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) fr = 0;
+    (void)cudaGetLastError();
+    const uint64_t pool = ctx->tslot_bytes * (uint64_t)ctx->grid_traced * 4u;
+    ctx->traced_ok = want && pool <= (uint64_t)(fr / 4);
+    // testing: FZ_TRACE_ALL=1 sends every extension through the traced sweep
+    const char* ta = getenv("FZ_TRACE_ALL");
+    p.trace_all = (ctx->traced_ok && ta && *ta && *ta != '0') ? 1 : 0;
+  }
   ctx->local_smem = local_smem_bytes(max_len);
   ctx->local_use_smem = ctx->local_smem <= 200 * 1024;
   ctx->grid_local = ctx->sms * local_blocks_per_sm(ctx->local_use_smem ? ctx->local_smem : 0);
@@ -667,9 +727,16 @@ fz_status fz_get_stats(fz_ctx* ctx, fz_stats* out) {
   ctx->stats.launches = ctx->launches;
   ctx->stats.profiled = 0;
   for (float& f : ctx->stats.phase_ms) f = 0.f;
+  ctx->stats.traced_ms = 0.f;
+  ctx->stats.traced_live_cells = ctx->h_cnt->traced_live;
   if (ctx->profiling && ctx->ev_set[0]) {
     ctx->stats.profiled = 1;
     int prev = 0;
+    if (ctx->ev_set[6]) {          // the traced sweep ran first: phase 0 starts after it
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ctx->ev[0], ctx->ev[6]) == cudaSuccess) ctx->stats.traced_ms = ms;
+      prev = 6;
+    }
     for (int k = 1; k <= 5; ++k) {
       if (!ctx->ev_set[k]) continue;
       float ms = 0.f;
@@ -677,7 +744,7 @@ fz_status fz_get_stats(fz_ctx* ctx, fz_stats* out) {
       prev = k;
     }
     float tot = 0.f;
-    if (cudaEventElapsedTime(&tot, ctx->ev[0], ctx->ev[prev]) == cudaSuccess) ctx->stats.phase_ms[5] = tot;
+    if (prev != 6 && cudaEventElapsedTime(&tot, ctx->ev[0], ctx->ev[prev]) == cudaSuccess) ctx->stats.phase_ms[5] = tot;
     (void)cudaGetLastError();
   }
   if (ctx->mode == FZ_LOCAL) {
@@ -691,7 +758,7 @@ fz_status fz_set_profiling(fz_ctx* ctx, int on) {
   if (!ctx) return FZ_ERR_ARG;
   CU(cudaSetDevice(ctx->device));
   if (on && !ctx->ev[0]) {
-    for (int k = 0; k < 6; ++k) CU(cudaEventCreate(&ctx->ev[k]));
+    for (int k = 0; k < 7; ++k) CU(cudaEventCreate(&ctx->ev[k]));
   }
   ctx->profiling = on != 0;
   return FZ_OK;

@@ -921,12 +921,34 @@ __device__ __forceinline__ void fold2(int q, bool last, uint32_t h, uint32_t liv
   }
 }
 
+// Traced pair sweep: the four direction flags of both cells of pair p, from
+// packed differences whose sign bit (bit 15 of a half) is the flag:
+//   nd = g - S   < 0: S does not come from the diagonal
+//   ni = I - S   < 0: S does not come from I (when not from the diagonal)
+//   ie = hl - I  < 0: I extends (I > h of the cell to the left; a tie opens)
+//   de = hu - D  < 0: D extends (D > h of the cell above; a tie opens)
+// Every value lies in [0, 2^15) and S >= g, I, D, I >= hl, D >= hu, so each
+// difference lies in (-2^15, 2^15) and its sign is exact.  Two sign-replicating
+// byte permutes turn the four words into bytes of 0 or 0xff, and two logic ops
+// with a per-pair mask place them: acc[p / 4] byte 0 holds (nd, ie) of the
+// low-half cell (row p) at bits 7 - 2 (p % 4) and 6 - 2 (p % 4), byte 1 its
+// (ni, de), bytes 2 and 3 the same for the high-half cell (row p + NP).
+// (p is a constant once the caller's pair loop is unrolled)
+__device__ __forceinline__ void pair_flags(uint32_t (&acc)[2], int p, uint32_t g, uint32_t sv, uint32_t ic,
+                                           uint32_t hl, uint32_t dc, uint32_t hu) {
+  const uint32_t w1 = prmt(__vsub2(g, sv), __vsub2(ic, sv), 0xfbd9u);
+  const uint32_t w2 = prmt(__vsub2(hl, ic), __vsub2(hu, dc), 0xfbd9u);
+  const int q = p & 3;
+  acc[p >> 2] |= (w1 & (0x80808080u >> (2 * q))) | (w2 & (0x40404040u >> (2 * q)));
+}
+
 // One step of the pair sweep with NP active pairs; returns the pair-wise max
-// of the new h (both halves); live2 accumulates the live masks.
-template <int NP, bool SHIFT, bool EDGE>
+// of the new h (both halves); live2 accumulates the live masks; with TR, acc
+// receives the direction flags of every cell (pair_flags).
+template <int NP, bool SHIFT, bool EDGE, bool TR>
 __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t noe2, uint32_t oe2, uint32_t lb2,
                                           int lane, uint32_t qb, uint32_t mr_new, int32_t vlo, int32_t vhi,
-                                          uint32_t& live2) {
+                                          uint32_t& live2, uint32_t (&acc)[2]) {
   uint32_t lm2 = 0, hk = 0, lk = 0;
   if (!SHIFT) {
     // above pair 0 (rows -1 and NP-1): lane l-1's row 2NP-1 (high half of its
@@ -955,6 +977,7 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
       const uint32_t dc = __viaddmax_s16x2_relu(da, ne2, ha);
       const uint32_t g = __vadd2(pa, prmt(L.MR[p], L.MR[p + NP], sel));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
+      if (TR) pair_flags(acc, p, g, sv, ic, L.H[p], dc, ha);
       const uint32_t hn = __vadd2(sv, noe2);          // a dead half may go negative: live_mask
       uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
@@ -991,6 +1014,7 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
       const uint32_t dc = __viaddmax_s16x2_relu(L.D[p], ne2, L.H[p]);
       const uint32_t g = __vadd2(L.HP[p], prmt(L.MR[p], L.MR[p + NP], L.SEL[p]));
       const uint32_t sv = __vimax3_s16x2_relu(g, ic, dc);
+      if (TR) pair_flags(acc, p, g, sv, ic, ho, dc, L.H[p]);
       const uint32_t hn = __vadd2(sv, noe2);          // a dead half may go negative: live_mask
       uint32_t live = live_mask(hn, lb2);
       if (EDGE) {
@@ -1158,6 +1182,22 @@ __device__ __forceinline__ int pair_live_lanes(const PairState& L, uint32_t oe2)
   return bits ? 32 - __clz(bits) : 0;
 }
 
+// Per-warp trace of the traced pair sweep.  Anti-diagonal d's flags are row d
+// of `rows`: lane l's 8 bytes (pair_flags' acc[0], acc[1]) cover its 2 NP
+// window rows b + 2 NP l .. b + 2 NP l + 2 NP - 1; hdr[d] = b | NP << 24
+// gives the window of that step.  runs: the walk's runs, in walk order.
+struct TraceSlot {
+  uint2* rows;
+  int32_t* hdr;
+  uint32_t* runs;
+};
+
+template <int NP>
+__device__ __forceinline__ void trace_store(const TraceSlot& ts, const PairCtl& c, int lane, const uint32_t (&acc)[2]) {
+  ts.rows[(uint32_t)c.d * 32u + (uint32_t)lane] = make_uint2(acc[0], acc[1]);
+  if (lane == 0) ts.hdr[c.d] = c.b | (NP << 24);
+}
+
 // Steps of the pair sweep with NP pairs per lane (a 64 NP-row window) from
 // anti-diagonal c.d until the sweep ends (returns 2), the live band reaches
 // the window's top lane while row b is live (1: the window must grow, or the
@@ -1180,10 +1220,12 @@ __device__ __forceinline__ int pair_live_lanes(const PairState& L, uint32_t oe2)
 // for that many steps.  An overflow test of one step suffices: a cell beyond
 // the window's top row at d needs that row live at d-1 (gap) or d-2
 // (diagonal) with the base kept since, which the test of that step saw.
-template <int NP>
+//
+// With TR every step's direction flags go to the trace slot (trace_store).
+template <int NP, bool TR>
 __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& p, const Window& w, int lane,
                                      Reservoir& qr, Reservoir& tr, const uint32_t* s_mrow16, int32_t* sT,
-                                     int32_t d_stop, uint32_t m0, uint32_t m31) {
+                                     int32_t d_stop, uint32_t m0, uint32_t m31, const TraceSlot& ts) {
   constexpr int32_t WIN = 64 * NP;
   const int32_t m = w.m, n = w.n, mn = w.m + w.n, oe = p.oe;
   const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe);
@@ -1199,16 +1241,20 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
       for (;;) {
         {
           const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-          const uint32_t lm2 = pstep<NP, false, false>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2);
+          uint32_t acc[2] = {0u, 0u};
+          const uint32_t lm2 = pstep<NP, false, false, TR>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2, acc);
           ++c.d;
+          if (TR) trace_store<NP>(ts, c, lane, acc);
           bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
         }
         if ((bits & 1u) || c.d == d_fast || wmd == 0u) break;
         {
           const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-          const uint32_t lm2 = pstep<NP, true, false>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, 0, 0, c.live2);
+          uint32_t acc[2] = {0u, 0u};
+          const uint32_t lm2 = pstep<NP, true, false, TR>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, 0, 0, c.live2, acc);
           ++c.b;
           ++c.d;
+          if (TR) trace_store<NP>(ts, c, lane, acc);
           bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
         }
         if ((int32_t)bits < 0 || c.d == d_fast || wmd == 0u) break;
@@ -1228,15 +1274,17 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
       const int32_t rowbase = bn + lane * 2 * NP;
       const int32_t vhi = m - rowbase, vlo = dn - n - rowbase;
       uint32_t lm2;
+      uint32_t acc[2] = {0u, 0u};
       if (!shift) {
         const uint32_t qb = res_take(qr, p.q2, p.q_len, w.qg0, w.dir);
-        lm2 = pstep<NP, false, true>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, vlo, vhi, c.live2);
+        lm2 = pstep<NP, false, true, TR>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, vlo, vhi, c.live2, acc);
       } else {
         const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
-        lm2 = pstep<NP, true, true>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, vlo, vhi, c.live2);
+        lm2 = pstep<NP, true, true, TR>(L, ne2, noe2, oe2, c.lb2, lane, 0u, mr_new, vlo, vhi, c.live2, acc);
       }
       c.b = bn;
       c.d = dn;
+      if (TR) trace_store<NP>(ts, c, lane, acc);
       uint32_t wmd;
       const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
       c.rowb_alive = bits & 1u;
@@ -1248,6 +1296,128 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
     if (ovf) return 1;
     if (c.d >= d_stop) return 0;
   }
+}
+
+// ---- traced pair sweep: the walk ----
+//
+// Per-warp staging of 32 anti-diagonals of the trace: for anti-diagonal
+// d0 - t (lane t) the window origin, the rows per lane and the flags of the
+// lanes that hold rows i - t .. i (every row the walk can reach there from
+// row i of d0: each step back lowers the row by at most one per
+// anti-diagonal).  Those rows span at most 32 rows, i.e. at most 5 lanes of 8
+// or more rows each.
+constexpr int WALK_WORDS = 6;
+struct WalkStage {
+  uint2 w[32][WALK_WORDS];
+  int32_t b[32], rpl[32], l0[32];
+};
+
+// Lane 0's run accumulation in walk order (runs (len << 4) | op; op 0 = M,
+// 1 = I, 2 = D).
+struct WalkRuns {
+  uint32_t* dst;
+  uint32_t cap, nr, op, len;
+  bool bad;
+  __device__ void push_n(uint32_t o, uint32_t n) {
+    if (o == op) { len += n; return; }
+    if (len) {
+      if (nr >= cap) { bad = true; return; }
+      dst[nr++] = (len << 4) | op;
+    }
+    op = o;
+    len = n;
+  }
+  __device__ void flush() {
+    if (!len) return;
+    if (nr >= cap) { bad = true; return; }
+    dst[nr++] = (len << 4) | op;
+    len = 0;
+  }
+};
+
+// Walks from the best cell (bi, bj) in state S back to the origin through the
+// traced flags (the traceback rules of the oracle: in S the diagonal, then I,
+// then D; in a gap state the gap opens when its flag says it does not extend;
+// on row 0 only I moves remain, on column 0 only D moves).  Writes the runs in
+// walk order to ts.runs (at most cap) and returns their number, or
+// 0xffffffff if the walk left the traced window or the run buffer.
+__device__ __noinline__ uint32_t trace_walk(const TraceSlot& ts, int32_t bi, int32_t bj, uint32_t cap, int lane,
+                                            WalkStage* sm) {
+  int32_t i = bi, j = bj, st = 0;
+  WalkRuns wr;
+  wr.dst = ts.runs; wr.cap = cap; wr.nr = 0; wr.op = 0xffu; wr.len = 0; wr.bad = false;
+  bool bad = false;
+  while (i > 0 && j > 0) {
+    const int32_t d0 = i + j;
+    const int32_t dt = d0 - lane;
+    if (dt >= 1) {
+      const int32_t h = __ldcg(ts.hdr + dt);
+      const int32_t b = h & 0xffffff, rpl = 2 * (h >> 24);
+      const int32_t lo = imax(i - lane - b, 0), hi = imin(i - b, 32 * rpl - 1);
+      const int32_t l0 = lo <= hi ? lo / rpl : 0;
+      const int32_t l1 = lo <= hi ? hi / rpl : -1;
+      sm->b[lane] = b;
+      sm->rpl[lane] = rpl;
+      sm->l0[lane] = l0;
+#pragma unroll
+      for (int k = 0; k < WALK_WORDS; ++k)
+        if (l0 + k <= l1) sm->w[lane][k] = __ldcg(ts.rows + (uint32_t)dt * 32u + (uint32_t)(l0 + k));
+    }
+    __syncwarp();
+    if (lane == 0) {
+      while (i > 0 && j > 0) {
+        const int t = d0 - (i + j);
+        if (t > 31) break;
+        const int32_t rpl = sm->rpl[t], np = rpl >> 1;
+        const int32_t u = i - sm->b[t];
+        if (u < 0 || u >= 32 * rpl) { bad = true; break; }
+        const int32_t l = u / rpl, r = u - l * rpl, k = l - sm->l0[t];
+        if (k < 0 || k >= WALK_WORDS) { bad = true; break; }
+        const uint2 wv = sm->w[t][k];
+        const int32_t half = r >= np ? 1 : 0, pp = r - half * np;
+        const uint32_t w32 = (pp < 4 ? wv.x : wv.y) >> (16 * half);
+        const int q = 2 * (pp & 3);
+        if (st == 0) {
+          if (!((w32 >> (7 - q)) & 1u)) {                  // S from the diagonal
+            wr.push_n(0u, 1u);
+            --i;
+            --j;
+          } else {
+            st = ((w32 >> (15 - q)) & 1u) ? 2 : 1;         // S from D, else from I (same cell)
+          }
+        } else if (st == 1) {
+          wr.push_n(1u, 1u);
+          st = ((w32 >> (6 - q)) & 1u) ? 1 : 0;            // I extends, else it opens here
+          --j;
+        } else {
+          wr.push_n(2u, 1u);
+          st = ((w32 >> (14 - q)) & 1u) ? 2 : 0;           // D extends, else it opens here
+          --i;
+        }
+        if (wr.bad) { bad = true; break; }
+      }
+    }
+    i = __shfl_sync(FULL, i, 0);
+    j = __shfl_sync(FULL, j, 0);
+    st = __shfl_sync(FULL, st, 0);
+    bad = __shfl_sync(FULL, bad ? 1 : 0, 0) != 0;
+    __syncwarp();
+    if (bad) break;
+  }
+  if (lane == 0 && !bad) {
+    if (i == 0 && j > 0) {
+      if (st == 2) bad = true;
+      else wr.push_n(1u, (uint32_t)j);                     // row 0: I moves only
+    } else if (j == 0 && i > 0) {
+      if (st == 1) bad = true;
+      else wr.push_n(2u, (uint32_t)i);                     // column 0: D moves only
+    }
+    wr.flush();
+    bad = bad || wr.bad;
+  }
+  const uint32_t nr = __shfl_sync(FULL, bad ? 0xffffffffu : wr.nr, 0);
+  __syncwarp();
+  return nr;
 }
 
 // Changes the window from NPO to NPN pairs per lane, keeping base row b:
@@ -1279,8 +1449,18 @@ __device__ __forceinline__ uint32_t pair_ckpt(int np, const WorkArgs& wa, const 
 // top-lane test is the first tier's overflow, as for a fixed 384-row window:
 // the base row follows the same rule at both sizes, so the values, best
 // cells, live counts and the overflow decision do not depend on the size.
+//
+// TR (the traced sweep): every step's direction flags go to the warp's trace
+// slot, no periodic checkpoints are written (no executor replays this
+// extension), and after the sweep the warp walks its best cell back to the
+// origin (trace_walk) and puts the runs, in forward genomic order, in the
+// traced-run arena; the record then carries FZ_XFLAG_TRACED with the runs'
+// offset (path) and count (npath).  If the arena is full the record is left
+// for the executor, which replays the sweep from the origin.
+template <bool TR>
 __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t ext, int lane, int32_t* sT,
-                                 uint8_t* tile, const uint32_t* s_mrow16, const int32_t* s_sub, PairRelay* rb) {
+                                 uint8_t* tile, const uint32_t* s_mrow16, const int32_t* s_sub, PairRelay* rb,
+                                 const TraceSlot& ts, WalkStage* wsm) {
   constexpr int32_t WIN = 64 * PK;   // the first tier's largest window (the executor's row width)
   const Window w = make_window(p, ext);
   ExtRec* R = wa.rec + ext;
@@ -1341,8 +1521,8 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   while (why != 2) {
     const uint32_t mask = np == PK ? (ex_mask & 63u) : ex_mask;
     const int32_t d_stop = (int32_t)(((uint32_t)c.d | mask) + 1u);
-    why = np == PK ? pair_run<PK>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31)
-                   : pair_run<NP_SMALL>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31);
+    why = np == PK ? pair_run<PK, TR>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31, ts)
+                   : pair_run<NP_SMALL, TR>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31, ts);
     if (why != 0 || ((uint32_t)c.d & ex_mask) == 0u) {
       c.cnt += live_count(c.live2);
       c.live2 = 0u;
@@ -1358,7 +1538,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       c.top = false;        // the new top lane's rows lay beyond the old window: dead
       continue;
     }
-    if (((uint32_t)c.d & ck_mask) == 0u && c.d - (c.bi + c.bj) <= wa.ckpt_recent)
+    if (!TR && ((uint32_t)c.d & ck_mask) == 0u && c.d - (c.bi + c.bj) <= wa.ckpt_recent)
       head = pair_ckpt(np, wa, L, lane, head, c, oe, sT);
     if (np == PK) {
       const int lanes = pair_live_lanes<PK>(L, oe2);   // lanes with a live cell at d or d-1
@@ -1405,6 +1585,23 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       __syncwarp();
       eager_corner(p, w, lane, sT, tile, s_sub, bi, bj, path, npath, wa.err);
     }
+  } else if (TR) {
+    const uint32_t nr = trace_walk(ts, bi, bj, (uint32_t)(bi + bj), lane, wsm);
+    if (nr == 0xffffffffu) {
+      if (lane == 0) atomicOr(wa.err, 0x20u);      // (the executor still traces it)
+    } else {
+      unsigned long long off = 0;
+      if (lane == 0) off = atomicAdd(wa.truns_used, (unsigned long long)nr);
+      off = __shfl_sync(FULL, off, 0);
+      if (off + nr <= wa.truns_cap) {
+        const bool right = (ext & 1u) == 0u;       // right side: genomic order is the walk reversed
+        for (uint32_t k = (uint32_t)lane; k < nr; k += 32) wa.truns[off + k] = __ldcg(ts.runs + (right ? nr - 1 - k : k));
+        path = off;
+        npath = nr;
+        flags |= FZ_XFLAG_TRACED;
+        width = 0;
+      }
+    }
   }
   if (lane == 0) {
     ExtRec o;
@@ -1413,27 +1610,42 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     o.m = m; o.n = n; o.width = width; o.ckpt = head;
     *R = o;
     atomicAdd(wa.live_total, (unsigned long long)tot);
+    if (TR) atomicAdd(wa.traced_live, (unsigned long long)tot);
   }
 }
 
+// The first inspector tier as the pair sweep.  TR: the traced sweep over the
+// extensions predicted long (list[0 .. *n_work_dev)); otherwise the plain
+// sweep (with list_base_dev set: over list[*list_base_dev .. n_work)).
+template <bool TR>
 __global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
   __shared__ int32_t s_T[WARPS][2 * EAGER_N + 2];
   __shared__ uint8_t s_tile[WARPS][(EAGER_N + 1) * (EAGER_N + 1)];
   __shared__ PairRelay s_relay[WARPS];
+  __shared__ WalkStage s_walk[TR ? WARPS : 1];
   __shared__ uint32_t s_mrow16[4];
   __shared__ int32_t s_sub[16];
   if (threadIdx.x < 4) s_mrow16[threadIdx.x] = p.mrow16[threadIdx.x];
   if (threadIdx.x < 16) s_sub[threadIdx.x] = p.sub[threadIdx.x];
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  TraceSlot ts{};
+  if (TR) {
+    uint8_t* base = wa.tpool + (uint64_t)(blockIdx.x * WARPS + warp) * wa.tslot_bytes;
+    ts.rows = reinterpret_cast<uint2*>(base);
+    ts.hdr = reinterpret_cast<int32_t*>(base + (uint64_t)wa.tslot_rows * 256u);
+    ts.runs = reinterpret_cast<uint32_t*>(base + (uint64_t)wa.tslot_rows * 260u);
+  }
+  const uint32_t lbase = wa.list_base_dev ? *wa.list_base_dev : 0u;
+  const uint32_t nw = wa.n_work_dev ? *wa.n_work_dev : wa.n_work - lbase;
   for (;;) {
     uint32_t idx = 0;
     if (lane == 0) idx = atomicAdd(wa.counter, 1u);
     idx = __shfl_sync(FULL, idx, 0);
-    const uint32_t nw = wa.n_work_dev ? *wa.n_work_dev : wa.n_work;
     if (idx >= nw) break;
-    const uint32_t ext = wa.list ? wa.list[idx] : idx;
-    run_inspect_pair(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow16, s_sub, &s_relay[warp]);
+    const uint32_t ext = wa.list ? wa.list[lbase + idx] : lbase + idx;
+    run_inspect_pair<TR>(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow16, s_sub, &s_relay[warp], ts,
+                         &s_walk[TR ? warp : 0]);
   }
 }
 
@@ -1479,10 +1691,21 @@ constexpr int KA = K_TIER0, KB = K_TIER1;
 int fast_window_rows(int tier) { return 32 * (tier == 0 ? KA : KB); }
 
 cudaError_t launch_inspect_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  if (tier == 0 && p.pair_ok) k_pair<<<grid, WARPS * 32, 0, st>>>(p, wa);
+  if (tier == 0 && p.pair_ok) k_pair<false><<<grid, WARPS * 32, 0, st>>>(p, wa);
   else if (tier == 0) k_extend<KA, false, 4><<<grid, WARPS * 32, 0, st>>>(p, wa);
   else k_extend<KB, false, 1><<<grid, WARPS * 32, 0, st>>>(p, wa);
   return cudaGetLastError();
+}
+
+cudaError_t launch_inspect_traced(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
+  k_pair<true><<<grid, WARPS * 32, 0, st>>>(p, wa);
+  return cudaGetLastError();
+}
+
+int traced_blocks_per_sm() {
+  int nb = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_pair<true>, WARPS * 32, 0);
+  return nb > 0 ? nb : 1;
 }
 
 cudaError_t launch_execute_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
@@ -1494,7 +1717,7 @@ cudaError_t launch_execute_fast(int tier, const Params& p, const WorkArgs& wa, i
 int extend_fast_blocks_per_sm(int tier, bool trace, bool pair) {
   int nb = 0;
   if (tier == 0 && !trace && pair) {
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_pair, WARPS * 32, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_pair<false>, WARPS * 32, 0);
   } else if (tier == 0) {
     if (trace) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KA, true, 4>, WARPS * 32, 0);
     else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_extend<KA, false, 4>, WARPS * 32, 0);

@@ -12,13 +12,17 @@ constexpr int32_t TFLOOR = -(1 << 29);    // lowest threshold: every reachable c
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int EAGER_N = 16;               // eager traceback corner: i*, j* <= 16
 constexpr int K_TIER0 = 12, K_TIER1 = 16; // rows per lane of the two register windows (384, 512 rows)
+// ExtRec flag (internal, never in an fz_result): traced by the inspector's
+// traced sweep; path = first run in the traced-run arena, npath = runs
+constexpr uint32_t FZ_XFLAG_TRACED = 1u << 16;
 
 // Per-extension record written by the inspector, read by binning, the
 // executor and the traceback.
 struct ExtRec {
   int32_t score, i_end, j_end, d_last;    // best S, its cell, last anti-diagonal with a live cell
   uint64_t live;                          // live cells of the sweep
-  uint64_t path;                          // eager traceback: ops walking back, 2 bits each
+  uint64_t path;                          // eager traceback: ops walking back, 2 bits each;
+                                          // traced: first run in the traced-run arena
   uint32_t flags;                         // FZ_FLAG_*
   uint32_t npath;                         // ops in path
   int32_t m, n;                           // window sizes
@@ -41,6 +45,7 @@ struct Params {
   uint32_t mrow16[4];     // 16-bit pair path: byte q of mrow16[t] = sub[t][q] (signed)
   int32_t pair_ok;        // 1: the inspector's first tier keeps two 16-bit rows per register
   int32_t pair_slack;     // pair sweep: threshold rise kept before the stored values move
+  int32_t trace_all;      // work order: predict every extension long (traced sweep for all)
   int32_t sub[16];
 };
 

@@ -37,6 +37,17 @@ struct WorkArgs {
   // checkpoint + 1 (0 = the origin), last anti-diagonal, first anti-diagonal};
   // list then holds the whole executor list and trace_off is indexed by position
   const uint4* seg;
+  // traced pair sweep (inspector of the extensions predicted long): one trace
+  // slot of tslot_bytes per resident warp (rows: tslot_rows x 256 B of flags,
+  // then tslot_rows int32 window headers, then tslot_rows uint32 walk runs)
+  uint8_t* tpool;
+  uint64_t tslot_bytes;
+  uint32_t tslot_rows;
+  uint32_t* truns;             // traced-run arena (runs in forward genomic order)
+  uint64_t truns_cap;
+  unsigned long long* truns_used;   // runs asked for (may pass truns_cap: those go to the executor)
+  const uint32_t* list_base_dev;    // plain pair sweep after the traced one: list offset (device)
+  unsigned long long* traced_live;  // traced sweep: its live cells
 };
 
 // register-window sweep (extend_fast.cu)
@@ -44,6 +55,9 @@ struct WorkArgs {
 int fast_window_rows(int tier);
 cudaError_t launch_inspect_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
 cudaError_t launch_execute_fast(int tier, const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+// traced pair sweep (first tier, pair_ok only): list[0 .. *n_work_dev)
+cudaError_t launch_inspect_traced(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
+int traced_blocks_per_sm();
 int extend_fast_blocks_per_sm(int tier, bool trace, bool pair);  // pair: the 16-bit first tier
 
 // general band sweep (extend_wide.cu)
@@ -87,10 +101,12 @@ struct PipeArgs {
   int32_t max_sub;             // max(0, largest substitution score)
 };
 cudaError_t launch_classify(const PipeArgs& a, cudaStream_t st);
-// inspector work order: extensions with more homologous 32-base blocks near
-// the anchor first (key: per extension; hist, cursor: [17], zeroed)
+// inspector work order: extensions predicted to align far (for the traced
+// sweep) first, then by the number of homologous 32-base blocks near the anchor
+// (key: per extension; hist, cursor: [34], zeroed; *n_long: the predicted ones,
+// list[0 .. *n_long), or 0 when fewer than min_long are predicted)
 cudaError_t launch_order(const Params& p, uint32_t n_ext, uint8_t* key, uint32_t* hist, uint32_t* cursor,
-                         uint32_t* list, cudaStream_t st);
+                         uint32_t* list, uint32_t* n_long, uint32_t min_long, cudaStream_t st);
 cudaError_t launch_scatter(const PipeArgs& a, cudaStream_t st);
 // exclusive scan of n uint64 values in place; total written to *total
 cudaError_t launch_scan_u64(uint64_t* data, uint32_t n, uint64_t* block_tmp, uint64_t* total, cudaStream_t st);
@@ -114,6 +130,7 @@ struct EmitArgs {
   int local;
   int32_t oe;
   int32_t max_sub;
+  const uint32_t* truns;       // traced-run arena (k_emit_traced)
 };
 // executor segments from the checkpoint chains, one list per executor tier
 // (0: 384-row window, 1: 512-row window, 2: wide band): nseg holds three
@@ -128,6 +145,7 @@ cudaError_t launch_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32
                             cudaStream_t st);
 
 cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st);   // eager, empty, local, not requested
+cudaError_t launch_emit_traced(const EmitArgs& a, cudaStream_t st);   // walked by the traced sweep
 // executor items [exec_begin, exec_end); items before long_end (the bins of
 // longer alignments) get a warp each, the rest a thread each
 cudaError_t launch_emit_exec(EmitArgs a, uint32_t long_end, int sms, cudaStream_t st);

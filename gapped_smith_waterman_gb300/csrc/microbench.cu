@@ -166,6 +166,40 @@ __global__ void k_cellmix16(int* out, int b) {
   out[blockIdx.x * blockDim.x + threadIdx.x] = (int)s;
 }
 
+// The cell pair of k_cellmix16 plus the four direction tests of the traced
+// sweep (g - S, I - S, h_left - I, h_up - D as packed subtractions).
+__global__ void k_cellmix16t(int* out, int b) {
+  unsigned h[CC], hp[CC], I[CC], D[CC], f[CC];
+#pragma unroll
+  for (int k = 0; k < CC; ++k) {
+    h[k] = threadIdx.x * 0x10001u + k;
+    hp[k] = h[k] ^ 0x00070007u;
+    I[k] = h[k] + 0x00030003u;
+    D[k] = h[k] + 0x00050005u;
+    f[k] = 0u;
+  }
+  const unsigned ne2 = (unsigned)b * 0x10001u, noe2 = (unsigned)(b + 1) * 0x10001u;
+  for (int i = 0; i < ITERS; ++i) {
+    const unsigned s = (unsigned)i * 0x10001u;
+#pragma unroll
+    for (int k = 0; k < CC; ++k) {
+      const unsigned ic = __viaddmax_s16x2_relu(I[k], ne2, h[k]);
+      const unsigned dc = __viaddmax_s16x2_relu(D[k], ne2, hp[k]);
+      const unsigned g = __vadd2(hp[k], s);
+      const unsigned sv = __vimax3_s16x2_relu(g, ic, dc);
+      f[k] ^= __vsub2(g, sv) ^ __vsub2(ic, sv) ^ __vsub2(h[k], ic) ^ __vsub2(hp[k], dc);
+      I[k] = ic;
+      D[k] = dc;
+      hp[k] = h[k];
+      h[k] = __vadd2(sv, noe2);
+    }
+  }
+  unsigned s = 0;
+#pragma unroll
+  for (int k = 0; k < CC; ++k) s ^= h[k] ^ I[k] ^ D[k] ^ f[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = (int)s;
+}
+
 // The same cell in 32-bit form (one cell per lane and instruction), adds as
 // multiply-adds by a runtime 1 as the 32-bit sweeps and the local fill write them.
 __global__ void k_cellmix32(int* out, int b) {
@@ -213,9 +247,9 @@ cudaError_t bench_int_rates(double rates[FZ_INT_RATES]) {
   cudaEventCreate(&e1);
   typedef void (*kfn)(int*, int);
   // operations per thread and loop iteration (cells for the two cell mixes)
-  const double per[FZ_INT_RATES] = {CH, CH, CH, CH, CH, CH, CH, CH, 2.0 * CC, CC};
+  const double per[FZ_INT_RATES] = {CH, CH, CH, CH, CH, CH, CH, CH, 2.0 * CC, CC, 2.0 * CC};
   kfn ks[FZ_INT_RATES] = {k_viaddmax, k_vimax3, k_iadd, k_imax, k_viaddmax16, k_vimax3_16, k_vadd2, k_imad,
-                          k_cellmix16, k_cellmix32};
+                          k_cellmix16, k_cellmix32, k_cellmix16t};
   for (int k = 0; k < FZ_INT_RATES; ++k) {
     ks[k]<<<blocks, threads>>>(out, 3);
     float best = 1e30f;

@@ -55,7 +55,18 @@ __device__ __forceinline__ uint64_t cigar_cap(int32_t i, int32_t j, int32_t oe, 
 // so far) matches at least 24 of the 32 bases; the key is the number of
 // homologous blocks, and the work list runs from the highest key down.  Only
 // the order of the work changes, never a result.
-constexpr int ORDER_KEYS = 17;
+//
+// The same pass predicts which extensions align far beyond the first 512
+// bases, for the traced sweep (the inspector that also stores direction codes
+// and walks its own best cell back, so that no executor replays it): one of
+// the blocks 12..15 is homologous at some diagonal offset of -24..24 (the
+// wider range follows the indels of a long alignment).  Predicted extensions
+// get key 17 + count and so come first in the work list; the first *n_long
+// entries of the list are exactly them.  A wrong prediction costs time only:
+// both sweeps and the executor compute the same records.
+constexpr int ORDER_BASE = 17;
+constexpr int ORDER_KEYS = 2 * ORDER_BASE;
+constexpr int LATE_FIRST = 12, LATE_OFF = 24;
 
 __device__ __forceinline__ uint32_t same_bases(uint32_t a, uint32_t b) {
   const uint32_t z = ~(a ^ b);
@@ -70,7 +81,7 @@ __global__ void k_order_key(Params p, uint32_t n_ext, uint8_t* key, uint32_t* hi
   const uint32_t ext = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (ext < n_ext) {                                // warp-uniform
     const Window w = make_window(p, ext);
-    uint32_t homologous = 0;
+    uint32_t homologous = 0, late = 0;
     if (lane < 16 && w.requested && 32 * lane + 32 <= w.m && 32 * lane + 32 <= w.n) {
       const int64_t b0 = 32 * lane + 1;
       const uint32_t t0 = fetch16(p.t2, p.t_len, w.tg0, w.dir, b0);
@@ -87,8 +98,26 @@ __global__ void k_order_key(Params p, uint32_t n_ext, uint8_t* key, uint32_t* hi
         best = c > best ? c : best;
       }
       homologous = best >= 24u ? 1u : 0u;
+      if (lane >= LATE_FIRST) {
+        // offsets -24..24: query bases b0 - 24 .. b0 + 55 in five 16-base words
+        uint32_t qw[6];
+#pragma unroll
+        for (int k = 0; k < 5; ++k) qw[k] = fetch16(p.q2, p.q_len, w.qg0, w.dir, b0 - LATE_OFF + 16 * k);
+        qw[5] = 0u;
+        uint32_t lb = 0;
+#pragma unroll
+        for (int o = 0; o <= 2 * LATE_OFF; ++o) {       // query offset o - 24
+          const int wi = o >> 4, sh = o & 15;
+          const uint32_t a0 = sh ? __funnelshift_r(qw[wi], qw[wi + 1], 2 * sh) : qw[wi];
+          const uint32_t a1 = sh ? __funnelshift_r(qw[wi + 1], qw[wi + 2], 2 * sh) : qw[wi + 1];
+          const uint32_t c = same_bases(t0, a0) + same_bases(t1, a1);
+          lb = c > lb ? c : lb;
+        }
+        late = lb >= 24u ? 1u : 0u;
+      }
     }
-    const uint32_t k = __popc(__ballot_sync(FULL, homologous != 0u));
+    const uint32_t k = __popc(__ballot_sync(FULL, homologous != 0u)) +
+                       ((__ballot_sync(FULL, late != 0u) || p.trace_all) ? (uint32_t)ORDER_BASE : 0u);
     if (lane == 0) {
       key[ext] = (uint8_t)k;
       atomicAdd(&h[k], 1u);
@@ -101,7 +130,7 @@ __global__ void k_order_key(Params p, uint32_t n_ext, uint8_t* key, uint32_t* hi
 // list[start(key) + rank] = ext, start(key) = extensions with a higher key;
 // ranks are taken per block in shared memory, then one range per key and block
 __global__ void k_order_scatter(uint32_t n_ext, const uint8_t* key, const uint32_t* hist, uint32_t* cursor,
-                                uint32_t* list) {
+                                uint32_t* list, uint32_t* n_long, uint32_t min_long) {
   __shared__ uint32_t start[ORDER_KEYS], count[ORDER_KEYS], base[ORDER_KEYS];
   if (threadIdx.x < ORDER_KEYS) count[threadIdx.x] = 0;
   if (threadIdx.x == 0) {
@@ -109,6 +138,10 @@ __global__ void k_order_scatter(uint32_t n_ext, const uint8_t* key, const uint32
     for (int k = ORDER_KEYS - 1; k >= 0; --k) {
       start[k] = acc;
       acc += hist[k];
+      // predicted long: keys 17..33; too few to fill the traced sweep's warps
+      // several times over leave them to the plain sweep and the executor
+      // (the traced launch would last as long as its longest extension)
+      if (k == ORDER_BASE && blockIdx.x == 0 && n_long) *n_long = acc >= min_long ? acc : 0u;
     }
   }
   __syncthreads();
@@ -140,6 +173,8 @@ __global__ void k_classify(PipeArgs a) {
         cap = cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub);
         if (r.flags & FZ_FLAG_EAGER) {
           atomicAdd(&h[0], 1u);
+        } else if (r.flags & FZ_XFLAG_TRACED) {
+          atomicAdd(&h[6], 1u);                    // traced in the inspector: no executor
         } else {
           bin = bin_of(r.i_end, r.j_end);
           atomicAdd(&h[bin], 1u);
@@ -380,7 +415,7 @@ __global__ void k_emit_direct(EmitArgs a) {
     return;
   }
   if (a.local) { write_out(a.out + x, r, 0, 0, 0); return; }
-  if (!(r.flags & FZ_FLAG_EAGER)) return;       // executor extension: k_emit_exec
+  if (!(r.flags & FZ_FLAG_EAGER)) return;       // executor extension: k_emit_exec; traced: k_emit_traced
   const uint64_t off = a.cig_off[x];
   const uint64_t cap = cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub);
   RunWriter wr;
@@ -389,6 +424,31 @@ __global__ void k_emit_direct(EmitArgs a) {
   wr.flush();
   if (wr.overflow) atomicOr(a.err, 16u);
   write_out(a.out + x, r, wr.nruns ? wr.first() : (uint32_t)off, wr.nruns, 0);
+}
+
+// Extensions the traced sweep walked: a warp per extension copies its runs
+// (already in forward genomic order) from the traced-run arena to its CIGAR
+// slot, where the run writer would have put them (right side: the slot's
+// end, left side: its start), and writes its record with its size bin.
+__global__ void k_emit_traced(EmitArgs a) {
+  const uint32_t x = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (x >= a.n_ext) return;
+  const ExtRec r = a.rec[x];
+  if (!(r.flags & FZ_FLAG_DONE) || !(r.flags & FZ_XFLAG_TRACED) || a.local) return;
+  const uint64_t off = a.cig_off[x];
+  const uint64_t cap = cigar_cap(r.i_end, r.j_end, a.oe, a.max_sub);
+  const uint32_t nr = r.npath;
+  if (nr > cap) {
+    if (lane == 0) {
+      atomicOr(a.err, 16u);
+      write_out(a.out + x, r, (uint32_t)off, 0, bin_of(r.i_end, r.j_end));
+    }
+    return;
+  }
+  const uint64_t dst = (x & 1u) == 0u ? off + cap - nr : off;
+  for (uint32_t k = lane; k < nr; k += 32) a.cigar[dst + k] = a.truns[r.path + k];
+  if (lane == 0) write_out(a.out + x, r, (uint32_t)dst, nr, bin_of(r.i_end, r.j_end));
 }
 
 // One executor extension's walk state and trace rows.
@@ -687,11 +747,11 @@ __global__ void __launch_bounds__(EMIT_T) k_emit_exec(EmitArgs a) {
 }  // namespace
 
 cudaError_t launch_order(const Params& p, uint32_t n_ext, uint8_t* key, uint32_t* hist, uint32_t* cursor,
-                         uint32_t* list, cudaStream_t st) {
+                         uint32_t* list, uint32_t* n_long, uint32_t min_long, cudaStream_t st) {
   if (n_ext == 0) return cudaSuccess;
   const uint32_t gk = (uint32_t)(((uint64_t)n_ext * 32 + TB - 1) / TB);
   k_order_key<<<gk, TB, 0, st>>>(p, n_ext, key, hist);
-  k_order_scatter<<<(n_ext + TB - 1) / TB, TB, 0, st>>>(n_ext, key, hist, cursor, list);
+  k_order_scatter<<<(n_ext + TB - 1) / TB, TB, 0, st>>>(n_ext, key, hist, cursor, list, n_long, min_long);
   return cudaGetLastError();
 }
 
@@ -739,6 +799,12 @@ cudaError_t launch_seg_fill(const ExtRec* rec, const uint32_t* exec_list, uint32
 cudaError_t launch_emit_direct(const EmitArgs& a, cudaStream_t st) {
   const uint32_t g = (a.n_ext + TB - 1) / TB;
   if (g) k_emit_direct<<<g, TB, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_emit_traced(const EmitArgs& a, cudaStream_t st) {
+  const uint64_t threads = (uint64_t)a.n_ext * 32;
+  if (a.n_ext) k_emit_traced<<<(uint32_t)((threads + TB - 1) / TB), TB, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,8 @@ class FzStats(ctypes.Structure):
                 ("bin", ctypes.c_uint32 * 5), ("extensions", ctypes.c_uint32), ("wide", ctypes.c_uint32),
                 ("trace_bytes", ctypes.c_uint64), ("cigar_runs", ctypes.c_uint64), ("launches", ctypes.c_uint32),
                 ("profiled", ctypes.c_uint32), ("phase_ms", ctypes.c_float * 6),
-                ("retried", ctypes.c_uint32), ("exec_live_cells", ctypes.c_uint64)]
+                ("retried", ctypes.c_uint32), ("exec_live_cells", ctypes.c_uint64), ("traced", ctypes.c_uint32),
+                ("traced_ms", ctypes.c_float), ("traced_live_cells", ctypes.c_uint64)]
 
 
 class FzError(RuntimeError):
@@ -167,9 +168,9 @@ def fz_combine(ctx, d_seeds: int, n_seeds: int, d_res: int, d_cigar: int, d_aln:
     return cig.value or 0
 
 
-FZ_INT_RATES = 10
+FZ_INT_RATES = 11
 INT_RATE_NAMES = ("viaddmax", "vimax3", "iadd", "imax", "viaddmax_s16x2", "vimax3_s16x2", "vadd2", "imad",
-                  "cell16_per_s", "cell32_per_s")
+                  "cell16_per_s", "cell32_per_s", "cell16_traced_per_s")
 
 
 def fz_bench_int_rates():

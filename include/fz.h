@@ -86,20 +86,27 @@ typedef struct {
     uint64_t exec_cells;    /* executor trace cells: anti-diagonals replayed x trace row width
                                (register-window path; live cells on the wide path) */
     uint32_t eager;         /* extensions traced back inside the inspector */
-    uint32_t bin[5];        /* executor bins: max(i*, j*) <= 512, 2048, 8192, 32768, 131072 */
+    uint32_t bin[5];        /* executor bins: max(i*, j*) <= 512, 2048, 8192, 32768, 131072
+                               (eager + bins + traced = extensions) */
     uint32_t extensions;    /* one-sided extensions computed */
     uint32_t wide;          /* extensions that ran on the general (wide band) path */
     uint64_t trace_bytes;   /* executor direction-bit arena used */
     uint64_t cigar_runs;    /* CIGAR arena runs used */
     uint32_t launches;      /* kernels launched by the last batch */
     uint32_t profiled;      /* 1 if phase_ms holds device times (fz_set_profiling) */
-    float phase_ms[6];      /* device time per phase: 0 inspector (register window),
+    float phase_ms[6];      /* device time per phase: 0 inspector (register window;
+                               after the traced sweep when that ran, see traced_ms),
                                1 inspector (wide band), 2 binning + scans, 3 executor,
                                4 CIGAR emission, 5 whole batch */
     uint32_t retried;       /* extensions whose live band outgrew the first register
                                window and resumed in the 512-row one */
     uint64_t exec_live_cells;   /* live cells the executor replayed (anti-diagonals
                                1 .. i* + j* of each executor extension) */
+    uint32_t traced;        /* extensions traced back by the inspector's traced sweep
+                               (predicted long; no executor replay) */
+    float traced_ms;        /* device time of the work order and the traced sweep when
+                               profiling (then phase_ms[0] excludes it) */
+    uint64_t traced_live_cells;  /* live cells of the traced sweep (part of live_cells) */
 } fz_stats;
 
 /*
@@ -259,11 +266,13 @@ fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_open, int32_t
  *      1 3-way max, 2 packed adds per two cells), independent cells
  *   9  cells/s of the costed Gotoh cell in 32-bit form (2 add-max, 1 3-way
  *      max, 2 multiply-adds per cell)
+ *  10  cells/s of the costed cell of the traced pair sweep: the cell of rate 8
+ *      plus its four direction tests (four packed subtractions per two cells)
  * Independent dependency chains per thread, every SM busy; synchronises the
- * device; allocates and frees a small output buffer.  Rates 8 and 9 are the
- * measured integer-pipe rooflines of the extension sweeps.
+ * device; allocates and frees a small output buffer.  Rates 8, 9 and 10 are
+ * the measured integer-pipe rooflines of the extension sweeps.
  */
-#define FZ_INT_RATES 10
+#define FZ_INT_RATES 11
 fz_status fz_bench_int_rates(double rates[FZ_INT_RATES]);
 
 /*

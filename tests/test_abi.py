@@ -46,8 +46,8 @@ def test_struct_layouts_match_header():
     assert W.SEED_DTYPE.itemsize == 24
     assert fz.RESULT_DTYPE.itemsize == 24
     assert fz.ALIGNMENT_DTYPE.itemsize == 48
-    # fields of fz_stats in order (4 bytes of padding before the last 8-byte field)
-    assert ctypes.sizeof(fz.FzStats) == 8 + 8 + 4 + 20 + 4 + 4 + 8 + 8 + 4 + 4 + 24 + 4 + 4 + 8
+    # fields of fz_stats in order (4 bytes of padding before exec_live_cells)
+    assert ctypes.sizeof(fz.FzStats) == 8 + 8 + 4 + 20 + 4 + 4 + 8 + 8 + 4 + 4 + 24 + 4 + 4 + 8 + 4 + 4 + 8
 
 
 def test_struct_offsets_match_a_c_compiler(tmp_path):

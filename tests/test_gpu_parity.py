@@ -93,7 +93,7 @@ def test_cfg1_full():
     gres, gcig, st, ores = _check(w, label="short-256bp")
     assert st.live_cells == int(ores["live_cells"].sum())
     assert st.extensions == len(w.seeds)
-    assert st.eager + sum(st.bin) == st.extensions
+    assert st.eager + sum(st.bin) + st.traced == st.extensions
 
 
 def test_cfg2_subset_all_fields():
@@ -353,19 +353,84 @@ def test_checkpoints_long_alignments(monkeypatch):
 
 def test_pair_sweep_equals_32bit_sweep(monkeypatch):
     """The 16-bit pair sweep (first tier when the y-drop keeps scores within 16
-    bits) and the 32-bit sweep give the same records, CIGARs and live cells;
-    both equal the oracle."""
+    bits), the same without its traced variant, and the 32-bit sweep give the
+    same records, CIGARs and live cells; all equal the oracle.  Without the
+    traced variant the executor replays the same cells as after the 32-bit
+    sweep."""
     w = G.workload(2)
     idx = np.arange(2000)
     a, acig, sa = G.gpu_run(w, w.seeds[idx])
     monkeypatch.setenv("FZ_NO_PAIR", "1")
     b, bcig, sb = G.gpu_run(w, w.seeds[idx])
     monkeypatch.delenv("FZ_NO_PAIR")
+    monkeypatch.setenv("FZ_TRACED", "0")
+    c, ccig, sc = G.gpu_run(w, w.seeds[idx])
+    monkeypatch.delenv("FZ_TRACED")
     assert np.array_equal(a, b) and np.array_equal(acig, bcig)
-    assert sa.live_cells == sb.live_cells and sa.exec_cells == sb.exec_cells
+    assert np.array_equal(a, c) and np.array_equal(acig, ccig)
+    assert sa.live_cells == sb.live_cells == sc.live_cells and sc.exec_cells == sb.exec_cells
+    assert sb.traced == 0 and sc.traced == 0
     ores, ocig, ooff = G.oracle_run(w, w.seeds[idx])
     G.compare(w, w.seeds[idx], a, acig, ores, ocig, ooff, label="pair sweep")
     assert sa.live_cells == int(ores["live_cells"].sum())
+
+
+def test_traced_sweep_on_long_alignments(monkeypatch):
+    """The traced pair sweep (direction flags stored during the inspector, the
+    warp walks its own best cell back) on chromosome-batch anchors, most of
+    them predicted long: records and CIGARs equal the oracle's and those of
+    the inspector + executor path (FZ_TRACED=0)."""
+    w = G.workload(3)
+    idx = G.sample_seeds(w, 3000, seed=31)
+    a, acig, sa, ores = _check(w, w.seeds[idx], label="traced sweep, chromosome anchors")
+    assert sa.traced > 0.4 * sa.extensions
+    assert sa.live_cells == int(ores["live_cells"].sum())
+    monkeypatch.setenv("FZ_TRACED", "0")
+    b, bcig, sb = G.gpu_run(w, w.seeds[idx])
+    assert sb.traced == 0 and np.array_equal(a, b) and np.array_equal(acig, bcig)
+    assert sa.eager + sum(sa.bin) + sa.traced == sa.extensions == sb.eager + sum(sb.bin)
+
+
+@pytest.mark.parametrize("label,env", [("every extension traced", {"FZ_TRACE_ALL": "1"}),
+                                       ("traced-run arena of 1,000 runs", {"FZ_TRACE_ALL": "1", "FZ_TRUNS_CAP": "1000"})])
+def test_traced_sweep_everywhere(label, env, monkeypatch):
+    """Every extension through the traced sweep: the edge cases (empty and
+    one-base windows, ends at the corner and the bin edges, long gaps, every
+    y-drop from 0 to none), the gap-run batch (band climbing and widening,
+    512-row overflows) and random scorings; with a tiny traced-run arena most
+    walked extensions do not fit and fall back to the executor, which then
+    replays them from the origin."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    rng = np.random.default_rng(61)
+    w, _ = _batch_from_pairs(_gap_run_pairs(rng, 30))
+    gres, gcig, st, ores = _check(w, label=f"{label}: gap runs")
+    assert st.traced + st.eager + sum(st.bin) == st.extensions
+    if "FZ_TRUNS_CAP" not in env:
+        assert st.traced > 0
+    x = rng.integers(0, 4, 300).astype(np.uint8)
+    pairs = [(np.zeros(0, np.uint8), np.zeros(0, np.uint8)), (x[:1], x[:1]), (x[:16], x[:16]), (x[:17], x[:16]),
+             (x, x), (np.concatenate([x[:80], np.zeros(60, np.uint8), x[80:]]), x),
+             (x[:100], np.concatenate([x[:50], x[60:100]])), (np.zeros(30, np.uint8), np.ones(30, np.uint8))]
+    for L in (511, 512, 513):
+        y = rng.integers(0, 4, L).astype(np.uint8)
+        pairs.append((np.concatenate([y, np.zeros(40, np.uint8)]), np.concatenate([y, np.ones(40, np.uint8)])))
+    w, _ = _batch_from_pairs(pairs)
+    for yd in (0, 1, 429, 430, 5000, 9400):
+        w2 = W.Workload(w.name, w.target, w.query, w.seeds, w.sub, w.gap_open, w.gap_extend, yd, w.max_len, w.mode)
+        _check(w2, label=f"{label}: edge cases ydrop={yd}")
+    for it in range(3):
+        sub = rng.integers(-120, 121, size=(4, 4)).astype(np.int32)
+        sub[np.arange(4), np.arange(4)] = rng.integers(20, 128, 4)
+        pairs = []
+        for _ in range(80):
+            m = int(rng.integers(0, 400))
+            t = rng.integers(0, 4, m).astype(np.uint8)
+            q = W.mutate(rng, t[:int(rng.integers(0, m + 1))], rng.uniform(0, 0.3), rng.uniform(0, 0.05), 2.0)
+            pairs.append((t, q))
+        w, _ = _batch_from_pairs(pairs, sub=sub, o=int(rng.integers(0, 600)), e=int(rng.integers(1, 60)),
+                                 ydrop=int(rng.choice([300, 2000, 9400])))
+        _check(w, label=f"{label}: random scoring {it}")
 
 
 def _gap_run_pairs(rng, n_pairs):
@@ -408,8 +473,13 @@ def test_gap_runs_move_the_band(monkeypatch):
     assert st.live_cells == int(ores["live_cells"].sum())
     monkeypatch.setenv("FZ_NO_PAIR", "1")
     b, bcig, sb = G.gpu_run(w)
+    monkeypatch.delenv("FZ_NO_PAIR")
+    monkeypatch.setenv("FZ_TRACED", "0")
+    c, ccig, sc = G.gpu_run(w)
     assert np.array_equal(a, b) and np.array_equal(acig, bcig)
-    assert st.live_cells == sb.live_cells and st.exec_cells == sb.exec_cells and st.retried == sb.retried
+    assert np.array_equal(a, c) and np.array_equal(acig, ccig)
+    assert st.live_cells == sb.live_cells == sc.live_cells and sc.exec_cells == sb.exec_cells
+    assert st.retried == sb.retried == sc.retried
 
 
 @pytest.mark.parametrize("ydrop", [20000, 20252])
