@@ -85,7 +85,8 @@ struct fz_ctx {
   DevBuf ckpt, seg_cnt, seg;         // window checkpoints, executor segments
   DevBuf comb_off, comb_cig;         // two-sided alignments (fz_combine)
   DevBuf tpool, truns;               // traced sweep: per-warp trace slots, run arena
-  bool traced_ok = false;            // the traced sweep runs (pair sweep, windows small enough)
+  bool traced_ok = false;            // the traced sweep may run (pair sweep on)
+  uint64_t tpool_cap = 0;            // largest trace pool (30% of the free memory at creation)
   int grid_traced = 0;
   uint32_t tslot_rows = 0;
   uint64_t tslot_bytes = 0;
@@ -231,8 +232,13 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   mark(ctx, 0, st);
   if (ctx->fast_ok) {
     // 384-row window for every extension; retries with 512 rows; then the wide band
-    // the traced sweep runs when at least 4 extensions per resident warp are predicted long
-    const uint32_t min_long = ctx->traced_ok ? 4u * 4u * (uint32_t)ctx->grid_traced : 0xffffffffu;
+    // the traced sweep runs when at least 4 extensions per resident warp are
+    // predicted long (testing: FZ_TRACE_MIN sets that number; FZ_TRACE_ALL
+    // makes it 0)
+    uint32_t min_long = ctx->traced_ok ? 4u * 4u * (uint32_t)ctx->grid_traced : 0xffffffffu;
+    if (ctx->traced_ok && ctx->p.trace_all) min_long = 0;
+    const char* tm = getenv("FZ_TRACE_MIN");
+    if (ctx->traced_ok && tm) min_long = (uint32_t)strtoul(tm, nullptr, 10);
     CU(launch_order(ctx->p, n_ext, ctx->order_key.as<uint8_t>(), dc->order_hist, dc->order_cursor,
                     ctx->order_list.as<uint32_t>(), &dc->n_long, min_long, st));
     ctx->launches += 2;
@@ -242,10 +248,11 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
     a.counter = &dc->work[0];
     a.ovf_list = ctx->retry_list.as<uint32_t>();
     a.ovf_count = &dc->retry_count;
-    if (ctx->traced_ok) {
+    const uint64_t tslots = std::min<uint64_t>((uint64_t)ctx->grid_traced * 4u, n_ext);
+    if (ctx->traced_ok && tslots * ctx->tslot_bytes <= ctx->tpool_cap) {
       // the extensions predicted long (the head of the work list) run the traced
       // sweep, the rest the plain one
-      CU(ctx->tpool.ensure(ctx->tslot_bytes * (uint64_t)ctx->grid_traced * 4u));
+      CU(ctx->tpool.ensure(ctx->tslot_bytes * tslots));
       uint64_t want = std::max<uint64_t>(ctx->truns_demand + ctx->truns_demand / 4, 256ull * n_ext + 4096);
       // testing: FZ_TRUNS_CAP limits the arena (extensions beyond it go to the executor)
       const char* tc = getenv("FZ_TRUNS_CAP");
@@ -257,6 +264,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
       t.tpool = ctx->tpool.as<uint8_t>();
       t.tslot_bytes = ctx->tslot_bytes;
       t.tslot_rows = ctx->tslot_rows;
+      t.tslots = (uint32_t)tslots;
       t.truns = ctx->truns.as<uint32_t>();
       t.truns_cap = tc ? want : ctx->truns.bytes / 4;
       t.truns_used = &dc->truns_used;
@@ -540,9 +548,10 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
   }
   ctx->grid_wide = ctx->sms;
   {
-    // traced sweep: one trace slot per resident warp, enough rows for the
-    // longest sweep (anti-diagonals 0 .. 2 max_len); on when the pool fits in a
-    // quarter of the free device memory (and FZ_TRACED is not "0")
+    // traced sweep: one trace slot per resident warp (at most one per
+    // extension of the batch), enough rows for the longest sweep
+    // (anti-diagonals 0 .. 2 max_len); it runs when the pool fits in 30% of
+    // the device memory free now (and FZ_TRACED is not "0")
     const char* tv = getenv("FZ_TRACED");
     const bool want = p.pair_ok && mode == FZ_EXTEND && !(tv && *tv == '0');
     ctx->grid_traced = ctx->sms * traced_blocks_per_sm();
@@ -551,8 +560,8 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     size_t fr = 0, tot = 0;
     if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) fr = 0;
     (void)cudaGetLastError();
-    const uint64_t pool = ctx->tslot_bytes * (uint64_t)ctx->grid_traced * 4u;
-    ctx->traced_ok = want && pool <= (uint64_t)(fr / 4);
+    ctx->tpool_cap = (uint64_t)(fr * 0.3);
+    ctx->traced_ok = want && ctx->tslot_bytes <= ctx->tpool_cap;
     // testing: FZ_TRACE_ALL=1 sends every extension through the traced sweep
     const char* ta = getenv("FZ_TRACE_ALL");
     p.trace_all = (ctx->traced_ok && ta && *ta && *ta != '0') ? 1 : 0;

@@ -924,16 +924,21 @@ __device__ __forceinline__ void fold2(int q, bool last, uint32_t h, uint32_t liv
 // Traced pair sweep: the four direction flags of both cells of pair p, from
 // packed differences whose sign bit (bit 15 of a half) is the flag:
 //   nd = g - S   < 0: S does not come from the diagonal
-//   ni = I - S   < 0: S does not come from I (when not from the diagonal)
+//   ni = I - S   < 0: S does not come from I (when not from the diagonal; a
+//                     tie with D goes to I)
 //   ie = hl - I  < 0: I extends (I > h of the cell to the left; a tie opens)
 //   de = hu - D  < 0: D extends (D > h of the cell above; a tie opens)
-// Every value lies in [0, 2^15) and S >= g, I, D, I >= hl, D >= hu, so each
-// difference lies in (-2^15, 2^15) and its sign is exact.  Two sign-replicating
-// byte permutes turn the four words into bytes of 0 or 0xff, and two logic ops
-// with a per-pair mask place them: acc[p / 4] byte 0 holds (nd, ie) of the
-// low-half cell (row p) at bits 7 - 2 (p % 4) and 6 - 2 (p % 4), byte 1 its
-// (ni, de), bytes 2 and 3 the same for the high-half cell (row p + NP).
-// (p is a constant once the caller's pair loop is unrolled)
+// S >= g, I, D, I >= hl and D >= hu, and every value lies in (-2^15, 2^15)
+// (g may be negative in lane 0's bottom row, which has no row above it), so
+// each difference lies in (-2^15, 0] and its sign is exact.  The packed
+// subtractions issue on the FMA pipe, which the DPX maxima, byte permutes and
+// logic ops of the cell leave less busy than the ALU pipe.  Two
+// sign-replicating byte permutes turn the four words into bytes of 0 or 0xff,
+// and two logic ops with a per-pair mask place them: acc[p / 4] byte 0 holds
+// (nd, ie) of the low-half cell (row p) at bits 7 - 2 (p % 4) and
+// 6 - 2 (p % 4), byte 1 its (ni, de), bytes 2 and 3 the same for the
+// high-half cell (row p + NP).  (p is a constant once the caller's pair loop
+// is unrolled.)
 __device__ __forceinline__ void pair_flags(uint32_t (&acc)[2], int p, uint32_t g, uint32_t sv, uint32_t ic,
                                            uint32_t hl, uint32_t dc, uint32_t hu) {
   const uint32_t w1 = prmt(__vsub2(g, sv), __vsub2(ic, sv), 0xfbd9u);
@@ -1335,19 +1340,40 @@ struct WalkRuns {
   }
 };
 
+// The four direction flags of row `row` at staged anti-diagonal d0 - t
+// (bit 0: S not from the diagonal, bit 1: not from I, bit 2: I extends, bit 3:
+// D extends), or 0x10 when the row is not in the staged flags.
+__device__ __forceinline__ uint32_t staged_flags(const WalkStage* sm, int t, int32_t row) {
+  const int32_t rpl = sm->rpl[t], np = rpl >> 1;
+  const int32_t u = row - sm->b[t];
+  if (u < 0 || u >= 32 * rpl) return 0x10u;
+  const int32_t l = rpl == 8 ? (u >> 3) : ((u * 2731) >> 15);   // u / rpl (rpl 8 or 12, u < 384)
+  const int32_t r = u - l * rpl, k = l - sm->l0[t];
+  if (k < 0 || k >= WALK_WORDS) return 0x10u;
+  const uint2 wv = sm->w[t][k];
+  const int32_t half = r >= np ? 1 : 0, pp = r - half * np;
+  const uint32_t w32 = ((pp < 4 ? wv.x : wv.y) >> (16 * half)) << (2 * (pp & 3));
+  return ((w32 >> 7) & 1u) | ((w32 >> 14) & 2u) | ((w32 >> 4) & 4u) | ((w32 >> 11) & 8u);
+}
+
 // Walks from the best cell (bi, bj) in state S back to the origin through the
 // traced flags (the traceback rules of the oracle: in S the diagonal, then I,
 // then D; in a gap state the gap opens when its flag says it does not extend;
-// on row 0 only I moves remain, on column 0 only D moves).  Writes the runs in
-// walk order to ts.runs (at most cap) and returns their number, or
-// 0xffffffff if the walk left the traced window or the run buffer.
+// on row 0 only I moves remain, on column 0 only D moves).  The warp stages 32
+// anti-diagonals of flags at a time in shared memory and then takes a whole
+// run per round: in S, lane k looks at the k-th cell down the diagonal
+// (anti-diagonal 2k further back), in I at the k-th cell to the left, in D at
+// the k-th cell above, and one ballot gives where the run ends.  Writes the
+// runs in walk order to ts.runs (at most cap) and returns their number, or
+// 0xffffffff if the walk left the staged flags or the run buffer.
 __device__ __noinline__ uint32_t trace_walk(const TraceSlot& ts, int32_t bi, int32_t bj, uint32_t cap, int lane,
                                             WalkStage* sm) {
   int32_t i = bi, j = bj, st = 0;
   WalkRuns wr;
   wr.dst = ts.runs; wr.cap = cap; wr.nr = 0; wr.op = 0xffu; wr.len = 0; wr.bad = false;
   bool bad = false;
-  while (i > 0 && j > 0) {
+  while (i > 0 && j > 0 && !bad) {
+    // stage anti-diagonals d0 - t, t = lane: the rows i - t .. i
     const int32_t d0 = i + j;
     const int32_t dt = d0 - lane;
     if (dt >= 1) {
@@ -1364,45 +1390,55 @@ __device__ __noinline__ uint32_t trace_walk(const TraceSlot& ts, int32_t bi, int
         if (l0 + k <= l1) sm->w[lane][k] = __ldcg(ts.rows + (uint32_t)dt * 32u + (uint32_t)(l0 + k));
     }
     __syncwarp();
-    if (lane == 0) {
-      while (i > 0 && j > 0) {
-        const int t = d0 - (i + j);
-        if (t > 31) break;
-        const int32_t rpl = sm->rpl[t], np = rpl >> 1;
-        const int32_t u = i - sm->b[t];
-        if (u < 0 || u >= 32 * rpl) { bad = true; break; }
-        const int32_t l = u / rpl, r = u - l * rpl, k = l - sm->l0[t];
-        if (k < 0 || k >= WALK_WORDS) { bad = true; break; }
-        const uint2 wv = sm->w[t][k];
-        const int32_t half = r >= np ? 1 : 0, pp = r - half * np;
-        const uint32_t w32 = (pp < 4 ? wv.x : wv.y) >> (16 * half);
-        const int q = 2 * (pp & 3);
-        if (st == 0) {
-          if (!((w32 >> (7 - q)) & 1u)) {                  // S from the diagonal
-            wr.push_n(0u, 1u);
-            --i;
-            --j;
-          } else {
-            st = ((w32 >> (15 - q)) & 1u) ? 2 : 1;         // S from D, else from I (same cell)
-          }
-        } else if (st == 1) {
-          wr.push_n(1u, 1u);
-          st = ((w32 >> (6 - q)) & 1u) ? 1 : 0;            // I extends, else it opens here
-          --j;
-        } else {
-          wr.push_n(2u, 1u);
-          st = ((w32 >> (14 - q)) & 1u) ? 2 : 0;           // D extends, else it opens here
-          --i;
-        }
-        if (wr.bad) { bad = true; break; }
+    // runs inside the staged window (t = d0 - (i + j) <= 31)
+    for (;;) {
+      const int t = d0 - (i + j);
+      if (i <= 0 || j <= 0 || t > 31) break;
+      const int k = lane;
+      uint32_t fl = 0;
+      bool valid;
+      if (st == 0) {
+        valid = k < 16 && t + 2 * k <= 31 && i - k >= 1 && j - k >= 1;
+        if (valid) fl = staged_flags(sm, t + 2 * k, i - k);
+      } else if (st == 1) {
+        valid = t + k <= 31 && j - k >= 1;
+        if (valid) fl = staged_flags(sm, t + k, i);
+      } else {
+        valid = t + k <= 31 && i - k >= 1;
+        if (valid) fl = staged_flags(sm, t + k, i - k);
       }
+      // (lanes past the end of the run look at cells the walk does not reach,
+      // which may lie outside the traced window: only the lane where the run
+      // stops must hold a cell of it)
+      const uint32_t eb = __ballot_sync(FULL, valid && (fl & 0x10u));
+      const uint32_t vb = __ballot_sync(FULL, valid) & ~eb;
+      if (st == 0) {
+        // diagonal moves while the cell's S comes from the diagonal
+        const uint32_t go = __ballot_sync(FULL, valid && !(fl & 0x11u));
+        const uint32_t nib = __ballot_sync(FULL, (fl & 2u) != 0u);
+        const int f = __ffs(~go) - 1;                   // 0..16
+        if ((eb >> f) & 1u) { bad = true; break; }
+        if (lane == 0 && f) wr.push_n(0u, (uint32_t)f);
+        i -= f;
+        j -= f;
+        if ((vb >> f) & 1u) st = ((nib >> f) & 1u) ? 2 : 1;   // S from D, else from I (same cell)
+      } else {
+        // gap moves while the gap extends; the cell where it opens is the run's last
+        const uint32_t go = __ballot_sync(FULL, valid && (fl & 0x10u) == 0u && (fl & (st == 1 ? 4u : 8u)));
+        const int f = go == FULL ? 32 : __ffs(~go) - 1;  // 0..32
+        if (f < 32 && ((eb >> f) & 1u)) { bad = true; break; }
+        const bool opens = f < 32 && ((vb >> f) & 1u);
+        const int n = opens ? f + 1 : f;
+        if (lane == 0 && n) wr.push_n((uint32_t)st, (uint32_t)n);
+        if (st == 1) j -= n;
+        else i -= n;
+        if (opens) st = 0;
+        else if ((st == 1 && j == 0) || (st == 2 && i == 0)) bad = true;   // a gap cannot run off the matrix
+      }
+      bad = __shfl_sync(FULL, (bad || wr.bad) ? 1 : 0, 0) != 0;
+      if (bad) break;
     }
-    i = __shfl_sync(FULL, i, 0);
-    j = __shfl_sync(FULL, j, 0);
-    st = __shfl_sync(FULL, st, 0);
-    bad = __shfl_sync(FULL, bad ? 1 : 0, 0) != 0;
     __syncwarp();
-    if (bad) break;
   }
   if (lane == 0 && !bad) {
     if (i == 0 && j > 0) {
@@ -1631,7 +1667,9 @@ __global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   TraceSlot ts{};
   if (TR) {
-    uint8_t* base = wa.tpool + (uint64_t)(blockIdx.x * WARPS + warp) * wa.tslot_bytes;
+    const uint32_t gw = blockIdx.x * WARPS + warp;
+    if (gw >= wa.tslots) return;                   // (warp-uniform; no block barrier follows)
+    uint8_t* base = wa.tpool + (uint64_t)gw * wa.tslot_bytes;
     ts.rows = reinterpret_cast<uint2*>(base);
     ts.hdr = reinterpret_cast<int32_t*>(base + (uint64_t)wa.tslot_rows * 256u);
     ts.runs = reinterpret_cast<uint32_t*>(base + (uint64_t)wa.tslot_rows * 260u);

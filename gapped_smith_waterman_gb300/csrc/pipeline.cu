@@ -59,14 +59,15 @@ __device__ __forceinline__ uint64_t cigar_cap(int32_t i, int32_t j, int32_t oe, 
 // The same pass predicts which extensions align far beyond the first 512
 // bases, for the traced sweep (the inspector that also stores direction codes
 // and walks its own best cell back, so that no executor replays it): one of
-// the blocks 12..15 is homologous at some diagonal offset of -24..24 (the
+// the blocks 8..15 is homologous at some diagonal offset of -40..40 (the
 // wider range follows the indels of a long alignment).  Predicted extensions
 // get key 17 + count and so come first in the work list; the first *n_long
 // entries of the list are exactly them.  A wrong prediction costs time only:
 // both sweeps and the executor compute the same records.
 constexpr int ORDER_BASE = 17;
 constexpr int ORDER_KEYS = 2 * ORDER_BASE;
-constexpr int LATE_FIRST = 12, LATE_OFF = 24;
+constexpr int LATE_FIRST = 8, LATE_OFF = 40;
+constexpr int LATE_WORDS = (32 + 2 * LATE_OFF + 15) / 16 + 1;   // 16-base query words around a block
 
 __device__ __forceinline__ uint32_t same_bases(uint32_t a, uint32_t b) {
   const uint32_t z = ~(a ^ b);
@@ -99,14 +100,14 @@ __global__ void k_order_key(Params p, uint32_t n_ext, uint8_t* key, uint32_t* hi
       }
       homologous = best >= 24u ? 1u : 0u;
       if (lane >= LATE_FIRST) {
-        // offsets -24..24: query bases b0 - 24 .. b0 + 55 in five 16-base words
-        uint32_t qw[6];
+        // offsets -40..40: query bases b0 - 40 .. b0 + 71 in 16-base words
+        uint32_t qw[LATE_WORDS + 1];
 #pragma unroll
-        for (int k = 0; k < 5; ++k) qw[k] = fetch16(p.q2, p.q_len, w.qg0, w.dir, b0 - LATE_OFF + 16 * k);
-        qw[5] = 0u;
+        for (int k = 0; k < LATE_WORDS; ++k) qw[k] = fetch16(p.q2, p.q_len, w.qg0, w.dir, b0 - LATE_OFF + 16 * k);
+        qw[LATE_WORDS] = 0u;
         uint32_t lb = 0;
 #pragma unroll
-        for (int o = 0; o <= 2 * LATE_OFF; ++o) {       // query offset o - 24
+        for (int o = 0; o <= 2 * LATE_OFF; ++o) {       // query offset o - LATE_OFF
           const int wi = o >> 4, sh = o & 15;
           const uint32_t a0 = sh ? __funnelshift_r(qw[wi], qw[wi + 1], 2 * sh) : qw[wi];
           const uint32_t a1 = sh ? __funnelshift_r(qw[wi + 1], qw[wi + 2], 2 * sh) : qw[wi + 1];
@@ -141,7 +142,10 @@ __global__ void k_order_scatter(uint32_t n_ext, const uint8_t* key, const uint32
       // predicted long: keys 17..33; too few to fill the traced sweep's warps
       // several times over leave them to the plain sweep and the executor
       // (the traced launch would last as long as its longest extension)
-      if (k == ORDER_BASE && blockIdx.x == 0 && n_long) *n_long = acc >= min_long ? acc : 0u;
+      // (or when they are at least half of the batch: then the plain sweep has
+      // little left to do after it either)
+      if (k == ORDER_BASE && blockIdx.x == 0 && n_long)
+        *n_long = (acc >= min_long || 2ull * acc >= (uint64_t)n_ext) ? acc : 0u;
     }
   }
   __syncthreads();

@@ -382,6 +382,7 @@ def test_traced_sweep_on_long_alignments(monkeypatch):
     the inspector + executor path (FZ_TRACED=0)."""
     w = G.workload(3)
     idx = G.sample_seeds(w, 3000, seed=31)
+    monkeypatch.setenv("FZ_TRACE_MIN", "0")        # (a sample this small would not fill the traced warps)
     a, acig, sa, ores = _check(w, w.seeds[idx], label="traced sweep, chromosome anchors")
     assert sa.traced > 0.4 * sa.extensions
     assert sa.live_cells == int(ores["live_cells"].sum())
