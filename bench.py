@@ -417,6 +417,7 @@ def main():
         "phases": ("plain inspector, wide inspector, bins+scans, executors, traceback+records, whole batch, "
                    "traced sweep (with the work order)"),
         "batch_stats": {"eager": int(st.eager), "bins": [int(b) for b in st.bin], "traced": int(st.traced),
+                        "traced_live_cells": int(st.traced_live_cells), "live_cells": int(st.live_cells),
                         "wide": int(st.wide), "retried_512": int(st.retried),
                         "executor_window_cells": int(st.exec_cells), "executor_live_cells": int(st.exec_live_cells),
                         "trace_bytes": int(st.trace_bytes),

@@ -90,6 +90,7 @@ struct fz_ctx {
   int grid_traced = 0;
   uint32_t tslot_rows = 0;
   uint64_t tslot_bytes = 0;
+  uint32_t tring = 0, tring_every = 0;   // traced sweep: ring checkpoints per slot, interval
   uint64_t truns_demand = 0;         // runs the last batch's traced sweep asked for
   DevBuf in_t, in_q, in_seeds, out_res;
   Counters* h_cnt = nullptr;         // pinned
@@ -265,6 +266,8 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
       t.tslot_bytes = ctx->tslot_bytes;
       t.tslot_rows = ctx->tslot_rows;
       t.tslots = (uint32_t)tslots;
+      t.tring = ctx->tring;
+      t.tring_every = ctx->tring_every;
       t.truns = ctx->truns.as<uint32_t>();
       t.truns_cap = tc ? want : ctx->truns.bytes / 4;
       t.truns_used = &dc->truns_used;
@@ -556,12 +559,14 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     const bool want = p.pair_ok && mode == FZ_EXTEND && !(tv && *tv == '0');
     ctx->grid_traced = ctx->sms * traced_blocks_per_sm();
     ctx->tslot_rows = (uint32_t)(2 * (int64_t)max_len + 2);
-    ctx->tslot_bytes = ((uint64_t)ctx->tslot_rows * 264u + 255u) & ~uint64_t(255);
+    ctx->tring_every = 1024;        // (set from the checkpoint interval below)
+    ctx->tring = 0;
+    ctx->tslot_bytes = 0;
     size_t fr = 0, tot = 0;
     if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) fr = 0;
     (void)cudaGetLastError();
     ctx->tpool_cap = (uint64_t)(fr * 0.3);
-    ctx->traced_ok = want && ctx->tslot_bytes <= ctx->tpool_cap;
+    ctx->traced_ok = want;
     // testing: FZ_TRACE_ALL=1 sends every extension through the traced sweep
     const char* ta = getenv("FZ_TRACE_ALL");
     p.trace_all = (ctx->traced_ok && ta && *ta && *ta != '0') ? 1 : 0;
@@ -608,6 +613,14 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     while (e < v && e < (1 << 20)) e <<= 1;   // a power of two, at least 32
     ctx->ckpt_every = e;
   }
+  // traced sweep slots: flag rows, window headers, walk runs, then the ring of
+  // checkpoints (one every 4 checkpoint intervals) that only an overflow uses
+  ctx->tring_every = (uint32_t)ctx->ckpt_every * 4u;
+  ctx->tring = (ctx->tslot_rows + ctx->tring_every - 1) / ctx->tring_every;
+  ctx->tslot_bytes = ((uint64_t)ctx->tslot_rows * 264u + (uint64_t)ctx->tring * CK_SLOT_WORDS * 4u + 255u) &
+                     ~uint64_t(255);
+  ctx->traced_ok = ctx->traced_ok && ctx->tslot_bytes <= ctx->tpool_cap;
+  if (!ctx->traced_ok) ctx->p.trace_all = 0;
   *out = ctx;
   return FZ_OK;
 }

@@ -1039,14 +1039,9 @@ __device__ __forceinline__ uint32_t pstep(PairState& L, uint32_t ne2, uint32_t n
 // Checkpoint of the pair sweep after anti-diagonal d, in the 32-bit layout
 // (rows u = K lane + r, K = 2 NP): h and I, D back in score space, dead as NEG.
 template <int NP>
-__device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const PairState& L, int lane, uint32_t head,
-                                                  const CkScalars& cs, int32_t B, int32_t oe, uint32_t cnt,
-                                                  uint32_t cnt_hi, const int32_t* sT) {
-  uint32_t slot = 0;
-  if (lane == 0) slot = atomicAdd(wa.ckpt_used, 1u);
-  slot = __shfl_sync(FULL, slot, 0);
-  if (slot >= wa.ckpt_cap) return head;
-  int32_t* c = wa.ckpt + (uint64_t)slot * CK_SLOT_WORDS;
+__device__ __forceinline__ void ck_fill_pair(int32_t* c, const PairState& L, int lane, uint32_t head,
+                                             const CkScalars& cs, int32_t B, int32_t oe, uint32_t cnt,
+                                             uint32_t cnt_hi, const int32_t* sT) {
   const int32_t c1 = oe - 128;
 #pragma unroll
   for (int r = 0; r < 2 * NP; ++r) {
@@ -1067,6 +1062,17 @@ __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const Pair
     c[CK_DLAST] = cs.d_last; c[CK_FLAGS] = 0; c[CK_PREV] = (int32_t)head;
     c[CK_CNT_HI] = (int32_t)cnt_hi;
   }
+}
+
+template <int NP>
+__device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const PairState& L, int lane, uint32_t head,
+                                                  const CkScalars& cs, int32_t B, int32_t oe, uint32_t cnt,
+                                                  uint32_t cnt_hi, const int32_t* sT) {
+  uint32_t slot = 0;
+  if (lane == 0) slot = atomicAdd(wa.ckpt_used, 1u);
+  slot = __shfl_sync(FULL, slot, 0);
+  if (slot >= wa.ckpt_cap) return head;
+  ck_fill_pair<NP>(wa.ckpt + (uint64_t)slot * CK_SLOT_WORDS, L, lane, head, cs, B, oe, cnt, cnt_hi, sT);
   return slot + 1;
 }
 
@@ -1195,6 +1201,7 @@ struct TraceSlot {
   uint2* rows;
   int32_t* hdr;
   uint32_t* runs;
+  int32_t* ring;     // wa.tring checkpoint slots (see ring_publish)
 };
 
 template <int NP>
@@ -1477,6 +1484,39 @@ __device__ __forceinline__ uint32_t pair_ckpt(int np, const WorkArgs& wa, const 
                         : ck_write_pair<PK>(wa, L, lane, head, cs, c.B, oe, c.cnt, 0u, sT);
 }
 
+// Traced sweep: checkpoints go to a ring in the warp's trace slot (one every
+// wa.tring_every anti-diagonals) instead of the shared pool, since no
+// executor replays a traced extension.  Only when the extension overflows the
+// 384-row window (it then continues untraced in the 512-row tier and the
+// executor traces it) are they copied to the pool and linked (ring_publish),
+// so that the executor splits its replay at them.
+__device__ __forceinline__ void ring_ckpt(int np, const TraceSlot& ts, uint32_t k, const PairState& L, int lane,
+                                          const PairCtl& c, int32_t oe, const int32_t* sT) {
+  const CkScalars cs{c.b, c.d, c.best, c.bi, c.bj, c.d_last};
+  int32_t* dst = ts.ring + (uint64_t)k * CK_SLOT_WORDS;
+  if (np == NP_SMALL) ck_fill_pair<NP_SMALL>(dst, L, lane, 0u, cs, c.B, oe, c.cnt, 0u, sT);
+  else ck_fill_pair<PK>(dst, L, lane, 0u, cs, c.B, oe, c.cnt, 0u, sT);
+}
+
+// Copies the n ring checkpoints (oldest first) to consecutive pool slots,
+// each linked to the one before; returns the newest's slot + 1, or 0 when the
+// pool has no room (the executor then replays from the origin).
+__device__ __noinline__ uint32_t ring_publish(const WorkArgs& wa, const TraceSlot& ts, uint32_t n, int lane) {
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(wa.ckpt_used, n);
+  base = __shfl_sync(FULL, base, 0);
+  if ((uint64_t)base + n > wa.ckpt_cap) return 0u;
+  for (uint32_t k = 0; k < n; ++k) {
+    const int32_t* src = ts.ring + (uint64_t)k * CK_SLOT_WORDS;
+    int32_t* dst = wa.ckpt + (uint64_t)(base + k) * CK_SLOT_WORDS;
+    for (int w = lane; w < CK_SLOT_WORDS; w += 32) dst[w] = __ldcg(src + w);
+    __syncwarp();
+    if (lane == 0) dst[CK_PREV] = (int32_t)(k ? base + k : 0u);   // the previous entry's slot + 1
+  }
+  __syncwarp();
+  return base + n;
+}
+
 // The pair sweep of one extension.  The window has two sizes: 256 rows (4
 // pairs per lane) to start with, and 384 rows (6 pairs): it grows when the
 // live band reaches the top lane of the small one while row b is live, and
@@ -1539,6 +1579,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     if (lane == 0) L.H[0] = (uint32_t)(-oe - c.B) & 0xffffu;      // origin: S(0,0) = 0
   }
   uint32_t head = 0u;
+  uint32_t nring = 0u;                      // traced: ring checkpoints written
   sT[lane] = NEG;
   if (lane == 0) sT[32] = NEG;
   __syncwarp();
@@ -1576,6 +1617,10 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     }
     if (!TR && ((uint32_t)c.d & ck_mask) == 0u && c.d - (c.bi + c.bj) <= wa.ckpt_recent)
       head = pair_ckpt(np, wa, L, lane, head, c, oe, sT);
+    if (TR && wa.ckpt && ((uint32_t)c.d & (wa.tring_every - 1u)) == 0u && nring < wa.tring) {
+      ring_ckpt(np, ts, nring, L, lane, c, oe, sT);
+      ++nring;
+    }
     if (np == PK) {
       const int lanes = pair_live_lanes<PK>(L, oe2);   // lanes with a live cell at d or d-1
       if (lanes * 2 * PK <= 60 * NP_SMALL) {
@@ -1585,7 +1630,10 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       }
     }
   }
-  if (overflow && wa.ckpt) head = pair_ckpt(PK, wa, L, lane, head, c, oe, sT);
+  if (overflow && wa.ckpt) {
+    if (TR && nring) head = ring_publish(wa, ts, nring, lane);
+    head = pair_ckpt(PK, wa, L, lane, head, c, oe, sT);
+  }
 
   uint64_t tot = c.cnt;
 #pragma unroll
@@ -1673,6 +1721,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
     ts.rows = reinterpret_cast<uint2*>(base);
     ts.hdr = reinterpret_cast<int32_t*>(base + (uint64_t)wa.tslot_rows * 256u);
     ts.runs = reinterpret_cast<uint32_t*>(base + (uint64_t)wa.tslot_rows * 260u);
+    ts.ring = reinterpret_cast<int32_t*>(base + (uint64_t)wa.tslot_rows * 264u);
   }
   const uint32_t lbase = wa.list_base_dev ? *wa.list_base_dev : 0u;
   const uint32_t nw = wa.n_work_dev ? *wa.n_work_dev : wa.n_work - lbase;

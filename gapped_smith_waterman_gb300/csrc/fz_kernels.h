@@ -44,6 +44,8 @@ struct WorkArgs {
   uint64_t tslot_bytes;
   uint32_t tslot_rows;
   uint32_t tslots;             // slots in the pool: warps beyond them take no work
+  uint32_t tring;              // ring checkpoints per slot (after the walk runs) ...
+  uint32_t tring_every;        // ... one every tring_every anti-diagonals (a power of two)
   uint32_t* truns;             // traced-run arena (runs in forward genomic order)
   uint64_t truns_cap;
   unsigned long long* truns_used;   // runs asked for (may pass truns_cap: those go to the executor)

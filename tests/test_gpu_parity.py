@@ -392,6 +392,24 @@ def test_traced_sweep_on_long_alignments(monkeypatch):
     assert sa.eager + sum(sa.bin) + sa.traced == sa.extensions == sb.eager + sum(sb.bin)
 
 
+def test_traced_overflow_uses_ring_checkpoints(monkeypatch):
+    """Traced extensions whose band overflows the 384-row window continue in
+    the 512-row tier and go to the executor, which splits their replay at the
+    traced sweep's ring checkpoints (published on the overflow): records and
+    CIGARs equal the oracle's, with small and default checkpoint intervals."""
+    rng = np.random.default_rng(71)
+    w, _ = _batch_from_pairs(_gap_run_pairs(rng, 40))
+    monkeypatch.setenv("FZ_TRACE_ALL", "1")
+    for every in ("32", None):
+        if every:
+            monkeypatch.setenv("FZ_CKPT_EVERY", every)
+        else:
+            monkeypatch.delenv("FZ_CKPT_EVERY", raising=False)
+        gres, gcig, st, ores = _check(w, label=f"traced overflow, checkpoint interval {every}")
+        assert st.retried > 0 and st.traced > 0
+        assert st.live_cells == int(ores["live_cells"].sum())
+
+
 @pytest.mark.parametrize("label,env", [("every extension traced", {"FZ_TRACE_ALL": "1"}),
                                        ("traced-run arena of 1,000 runs", {"FZ_TRACE_ALL": "1", "FZ_TRUNS_CAP": "1000"})])
 def test_traced_sweep_everywhere(label, env, monkeypatch):
