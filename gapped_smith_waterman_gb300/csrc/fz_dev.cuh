@@ -78,21 +78,33 @@ __device__ __forceinline__ Window make_window(const Params& p, uint32_t ext) {
 }
 
 // 16 bases of a window starting at window index w: base w+k at bits 2k.
-// Positions outside the sequence read as 0 (callers never score them).
+// Positions outside the sequence read as 0 (callers never score them).  The
+// 16 bases span 5 bytes of the packed sequence; they are taken with two
+// aligned 8-byte loads when both lie inside the sequence's bytes and the
+// sequence is 8-byte aligned (device allocations are), else byte by byte.
 __device__ __forceinline__ uint32_t fetch16(const uint8_t* __restrict__ s, uint64_t len, int64_t g0,
                                             int dir, int64_t w) {
   const int64_t lo = dir > 0 ? g0 + w : g0 - w - 15;   // lowest genomic position covered
   const int64_t b0 = lo >> 2;                           // floor division
   const int sh = (int)(lo & 3) * 2;
   const int64_t nbytes = (int64_t)((len + 3) >> 2);
-  uint64_t v = 0;
+  const int64_t a = b0 & ~int64_t(7);                   // aligned 8-byte word holding byte b0
+  uint32_t fw;                                          // genomic lo .. lo+15, forward
+  if (b0 >= 0 && a + 16 <= nbytes && ((uintptr_t)s & 7u) == 0u) {
+    const uint64_t* q = reinterpret_cast<const uint64_t*>(s + a);
+    const uint64_t w0 = __ldg(q), w1 = __ldg(q + 1);
+    const int bs = 8 * (int)(b0 - a) + sh;              // bit offset of base lo in w1:w0, 0..62
+    fw = (uint32_t)(bs ? (w0 >> bs) | (w1 << (64 - bs)) : w0);
+  } else {
+    uint64_t v = 0;
 #pragma unroll
-  for (int k = 0; k < 5; ++k) {
-    const int64_t bi = b0 + k;
-    const uint32_t byte = (bi >= 0 && bi < nbytes) ? (uint32_t)__ldg(s + bi) : 0u;
-    v |= (uint64_t)byte << (8 * k);
+    for (int k = 0; k < 5; ++k) {
+      const int64_t bi = b0 + k;
+      const uint32_t byte = (bi >= 0 && bi < nbytes) ? (uint32_t)__ldg(s + bi) : 0u;
+      v |= (uint64_t)byte << (8 * k);
+    }
+    fw = (uint32_t)(v >> sh);
   }
-  const uint32_t fw = (uint32_t)(v >> sh);              // genomic lo .. lo+15, forward
   if (dir > 0) return fw;
   const uint32_t r = __brev(fw);                        // reverse the order of the 2-bit fields
   return ((r >> 1) & 0x55555555u) | ((r & 0x55555555u) << 1);

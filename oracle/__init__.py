@@ -8,7 +8,8 @@ CUDA library and this oracle share no code.
 pthread pool only to run independent extensions side by side) into
 ``oracle/_build/liboracle.so`` and ``extend_batch()`` runs it over a batch of
 seeds, returning per extension (right, left) the score, end cell, live-cell
-count and CIGAR runs.
+count and CIGAR runs.  ``edit_distance()`` and ``dtw()`` are the article's two
+other dynamic programs (unit-cost edit distance; dynamic time warping).
 """
 from __future__ import annotations
 
@@ -72,6 +73,10 @@ def lib():
                                     ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.c_void_p, u32p, i64p]
             L.orc_batch.restype = ctypes.c_int
+            L.orc_edit_distance.argtypes = [u8p, ctypes.c_int32, u8p, ctypes.c_int32]
+            L.orc_edit_distance.restype = ctypes.c_int32
+            L.orc_dtw.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32]
+            L.orc_dtw.restype = ctypes.c_int64
             _lib = L
     return _lib
 
@@ -196,4 +201,35 @@ def combine(seeds, res, cigar, cig_off):
                     tp - (int(res["i_end"][xl]) if hl else 0), qp - (int(res["j_end"][xl]) if hl else 0),
                     tp + (int(res["i_end"][xr]) if hr else 0), qp + (int(res["j_end"][xr]) if hr else 0),
                     np.asarray(runs, np.uint32)))
+    return out
+
+
+def edit_distance(a, b) -> int:
+    """Levenshtein distance of two base-code sequences (unit costs; the DPX
+    intrinsics article, section 1.3)."""
+    a = np.ascontiguousarray(a, np.uint8)
+    b = np.ascontiguousarray(b, np.uint8)
+    r = lib().orc_edit_distance(_ptr(a, ctypes.c_uint8), a.size, _ptr(b, ctypes.c_uint8), b.size)
+    if r < 0:
+        raise RuntimeError("oracle edit distance failed")
+    return int(r)
+
+
+def dtw(x, y) -> int:
+    """Dynamic time warping cost of two int32 sequences, cell cost |x_i - y_j|
+    (the DPX intrinsics article, section 1.3); -1 when exactly one is empty."""
+    x = np.ascontiguousarray(x, np.int32)
+    y = np.ascontiguousarray(y, np.int32)
+    r = lib().orc_dtw(_ptr(x, ctypes.c_int32), x.size, _ptr(y, ctypes.c_int32), y.size)
+    if r < -1:
+        raise RuntimeError("oracle dtw failed")
+    return int(r)
+
+
+def pairs_batch(fn, a, b, pairs):
+    """fn over pairs (fields a_pos, b_pos, a_len, b_len) of the sequences a and b."""
+    out = np.zeros(len(pairs), np.int64)
+    for k, pr in enumerate(pairs):
+        ap, bp, al, bl = int(pr["a_pos"]), int(pr["b_pos"]), int(pr["a_len"]), int(pr["b_len"])
+        out[k] = fn(a[ap:ap + al], b[bp:bp + bl])
     return out

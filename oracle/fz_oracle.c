@@ -386,3 +386,68 @@ int orc_batch(const uint8_t* tseq, uint64_t t_len, const uint8_t* qseq, uint64_t
         if (out[x].status) rc = out[x].status;
     return rc;
 }
+
+/*
+ * Two more dynamic programs of the DPX intrinsics article (section 1.3: edit
+ * distance and dynamic time warping are, like alignment, a minimum over three
+ * sources plus an add).  Plain full-table definitions, one row kept at a time.
+ *
+ * Edit distance (Levenshtein: substitution, insertion and deletion cost 1):
+ *   D(i,0) = i, D(0,j) = j,
+ *   D(i,j) = min(D(i-1,j) + 1, D(i,j-1) + 1, D(i-1,j-1) + [a_i != b_j]);
+ *   result D(m,n).
+ */
+int32_t orc_edit_distance(const uint8_t* a, int32_t m, const uint8_t* b, int32_t n) {
+    int32_t* prev = (int32_t*)malloc(sizeof(int32_t) * ((size_t)n + 1));
+    int32_t* cur = (int32_t*)malloc(sizeof(int32_t) * ((size_t)n + 1));
+    if (!prev || !cur) { free(prev); free(cur); return -2; }
+    for (int32_t j = 0; j <= n; ++j) prev[j] = j;
+    for (int32_t i = 1; i <= m; ++i) {
+        cur[0] = i;
+        for (int32_t j = 1; j <= n; ++j) {
+            int32_t v = prev[j] + 1;                                   /* from above: a_i deleted */
+            if (cur[j - 1] + 1 < v) v = cur[j - 1] + 1;                /* from the left: b_j inserted */
+            const int32_t dg = prev[j - 1] + (a[i - 1] != b[j - 1]);   /* diagonal: match or substitution */
+            if (dg < v) v = dg;
+            cur[j] = v;
+        }
+        int32_t* t = prev; prev = cur; cur = t;
+    }
+    const int32_t r = prev[n];
+    free(prev);
+    free(cur);
+    return r;
+}
+
+/*
+ * Dynamic time warping of two integer sequences, cost |x_i - y_j| per cell:
+ *   D(0,0) = 0, D(i,0) = D(0,j) = infinity for i, j >= 1,
+ *   D(i,j) = |x_i - y_j| + min(D(i-1,j), D(i,j-1), D(i-1,j-1));
+ *   result D(m,n) (64-bit); -1 when exactly one sequence is empty (no warping
+ *   path exists), 0 when both are.
+ */
+int64_t orc_dtw(const int32_t* x, int32_t m, const int32_t* y, int32_t n) {
+    if (m == 0 && n == 0) return 0;
+    if (m == 0 || n == 0) return -1;
+    const int64_t INF = (int64_t)1 << 62;
+    int64_t* prev = (int64_t*)malloc(sizeof(int64_t) * ((size_t)n + 1));
+    int64_t* cur = (int64_t*)malloc(sizeof(int64_t) * ((size_t)n + 1));
+    if (!prev || !cur) { free(prev); free(cur); return -2; }
+    prev[0] = 0;
+    for (int32_t j = 1; j <= n; ++j) prev[j] = INF;
+    for (int32_t i = 1; i <= m; ++i) {
+        cur[0] = INF;
+        for (int32_t j = 1; j <= n; ++j) {
+            int64_t best = prev[j];
+            if (cur[j - 1] < best) best = cur[j - 1];
+            if (prev[j - 1] < best) best = prev[j - 1];
+            const int64_t c = (int64_t)x[i - 1] - (int64_t)y[j - 1];
+            cur[j] = best + (c < 0 ? -c : c);
+        }
+        int64_t* t = prev; prev = cur; cur = t;
+    }
+    const int64_t r = prev[n];
+    free(prev);
+    free(cur);
+    return r;
+}
