@@ -106,6 +106,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seeds", type=int, default=0, help="use only the first N seeds (profiling captures)")
+    ap.add_argument("--dp", choices=["edit", "dtw"], default=None,
+                    help="time the DPX article's other dynamic programs instead (512 edit distances of "
+                         "1024 x 1024, or 256 DTWs of 800 x 800)")
     return ap.parse_args()
 
 
@@ -269,9 +272,110 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+# Nominal integer-pipe peaks of the other two dynamic programs (cells/clk/SM,
+# one 32-bit cell per lane): edit distance = DPX add-min (64 lanes/clk) + a
+# min and an add (128 lanes/clk) = 2/64 SM-clocks per lane and cell; DTW =
+# DPX 3-way min (64) + |x - y| as a subtraction and an absolute value + the
+# add (128) = 2.5/64.
+DP_CELLS_PER_CLK_SM = {"edit": 32.0, "dtw": 25.6}
+
+
+def run_dp(args, ws, rank, lrank):
+    """The DPX article's other dynamic programs: one step = one batch through
+    fz_edit_distance_batch / fz_dtw_batch, inputs resident in HBM."""
+    import torch
+    from gapped_smith_waterman_gb300 import build as B
+    from gapped_smith_waterman_gb300 import fz
+    torch.cuda.set_device(lrank)
+    dev = torch.device("cuda", lrank)
+    B.build()
+    w = W.make_edit_batch() if args.dp == "edit" else W.make_dtw_batch()
+    if w.kind == "edit":
+        da, db = (torch.from_numpy(W.pack2(x)).to(dev) for x in (w.a, w.b))
+    else:
+        da, db = (torch.from_numpy(np.ascontiguousarray(x, np.int32)).to(dev) for x in (w.a, w.b))
+    dp = torch.from_numpy(np.ascontiguousarray(w.pairs).view(np.uint8)).to(dev)
+    out = torch.empty(len(w.pairs), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fn = fz.fz_edit_distance_batch if w.kind == "edit" else fz.fz_dtw_batch
+    call = lambda: fn(da.data_ptr(), len(w.a), db.data_ptr(), len(w.b), dp.data_ptr(), len(w.pairs),  # noqa: E731
+                      out.data_ptr(), stream.cuda_stream)
+    cells = int((w.pairs["a_len"].astype(np.int64) * w.pairs["b_len"].astype(np.int64)).sum())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(lrank)
+    sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    clocks = sampler.stop()
+    value = cells * args.steps / (tot * 1e-3) / 1e9
+    sms, ghz, clock_src = device_peaks(lrank)
+    peak = sms * ghz * DP_CELLS_PER_CLK_SM[w.kind]
+    # e2e: host inputs copied in, results copied out, inside the timed region
+    h_a = torch.from_numpy(W.pack2(w.a) if w.kind == "edit" else np.ascontiguousarray(w.a, np.int32)).pin_memory()
+    h_b = torch.from_numpy(W.pack2(w.b) if w.kind == "edit" else np.ascontiguousarray(w.b, np.int32)).pin_memory()
+    h_p = torch.from_numpy(np.ascontiguousarray(w.pairs).view(np.uint8)).pin_memory()
+    h_o = torch.empty(len(w.pairs), dtype=torch.int32).pin_memory()
+    ne, e2e_s = max(1, min(args.steps, 5)), 0.0
+    for _ in range(ne):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        da.copy_(h_a, non_blocking=True)
+        db.copy_(h_b, non_blocking=True)
+        dp.copy_(h_p, non_blocking=True)
+        call()
+        h_o.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_s += time.perf_counter() - t0
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        f = oracle.edit_distance if w.kind == "edit" else oracle.dtw
+        n = 0
+        t0 = time.perf_counter()
+        while n < len(w.pairs) and time.perf_counter() - t0 < max(1.0, args.cpu_seconds / 3):
+            oracle.pairs_batch(f, w.a, w.b, w.pairs[n:n + 1])
+            n += 1
+        dt = time.perf_counter() - t0
+        c = int((w.pairs["a_len"][:n].astype(np.int64) * w.pairs["b_len"][:n].astype(np.int64)).sum())
+        cpu = {"value": c / dt / 1e9, "unit": "GCUPS", "cores": 1, "kind": "oracle",
+               "sample": f"{n} of {len(w.pairs)} pairs, one thread, {dt:.1f} s", "cpu_model": cpu_model()}
+    line = {"metric": f"GCUPS of the batched {'edit distance' if w.kind == 'edit' else 'dynamic time warping'} "
+                      "at 1 GB300", "value": value, "unit": "GCUPS", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": w.name, "note": w.note, "cells_per_step": cells,
+                       "l2": "flushed between steps (256 MiB write)"},
+            "roofline": {"bound": "alu", "kernel": f"k_dp<{w.kind == 'dtw'}>", "achieved": value, "peak": peak,
+                         "unit": "Gcell/s", "frac": value / peak,
+                         "peak_basis": f"{sms} SM x {ghz:.3f} GHz ({clock_src}) x {DP_CELLS_PER_CLK_SM[w.kind]} "
+                                       "cells/clk/SM", "traffic": None},
+            "gpu_launches": args.steps, "clocks": clocks,
+            "e2e": {"value": cells * ne / e2e_s / 1e9, "unit": "GCUPS",
+                    "h2d_bytes_per_step": int(h_a.numel() * h_a.element_size() + h_b.numel() * h_b.element_size()
+                                              + h_p.numel()),
+                    "d2h_bytes_per_step": int(h_o.numel() * 4)},
+            "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     ws, rank, lrank = dist_env()
+    if args.dp:
+        if rank == 0:
+            run_dp(args, ws, rank, lrank)
+        return
     if args.impl == "reference":
         run_reference(args, ws, rank)
         return

@@ -22,12 +22,16 @@ FZ_FLAG_BIN_SHIFT = 4
 
 SYMBOLS = ("fz_create", "fz_extend_batch", "fz_extend_batch_host", "fz_get_stats", "fz_set_profiling",
            "fz_last_error", "fz_destroy", "fz_bench_int_rates", "fz_local_fill_noalloc", "fz_combine",
-           "fz_pair_sweep_used")
+           "fz_pair_sweep_used", "fz_edit_distance_batch", "fz_dtw_batch")
 
 RESULT_DTYPE = np.dtype([("score", "<i4"), ("t_end", "<i4"), ("q_end", "<i4"), ("cigar_off", "<u4"),
                          ("cigar_len", "<u4"), ("flags", "<u4")])
 assert RESULT_DTYPE.itemsize == 24
 
+
+PAIR_DTYPE = np.dtype([("a_pos", "<u8"), ("b_pos", "<u8"), ("a_len", "<u4"), ("b_len", "<u4")])
+assert PAIR_DTYPE.itemsize == 24
+FZ_DP_MAX_LEN = 4096
 
 ALIGNMENT_DTYPE = np.dtype([("score", "<i4"), ("cigar_len", "<u4"), ("t_start", "<u8"), ("q_start", "<u8"),
                             ("t_end", "<u8"), ("q_end", "<u8"), ("cigar_off", "<u8")])
@@ -87,6 +91,12 @@ def load(path: str | None = None, build_if_missing: bool = False):
     L.fz_local_fill_noalloc.restype = ctypes.c_int
     L.fz_combine.argtypes = [vp, vp, ctypes.c_uint32, vp, vp, vp, ctypes.POINTER(ctypes.c_void_p), vp]
     L.fz_combine.restype = ctypes.c_int
+    L.fz_edit_distance_batch.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
+                                         ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+    L.fz_edit_distance_batch.restype = ctypes.c_int
+    L.fz_dtw_batch.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_uint64,
+                               ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p]
+    L.fz_dtw_batch.restype = ctypes.c_int
     L.fz_bench_int_rates.argtypes = [ctypes.POINTER(ctypes.c_double)]
     L.fz_bench_int_rates.restype = ctypes.c_int
     L.fz_pair_sweep_used.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -166,6 +176,42 @@ def fz_combine(ctx, d_seeds: int, n_seeds: int, d_res: int, d_cigar: int, d_aln:
     cig = ctypes.c_void_p()
     _check(ctx, load().fz_combine(ctx, d_seeds, n_seeds, d_res, d_cigar or None, d_aln, ctypes.byref(cig), stream))
     return cig.value or 0
+
+
+def fz_edit_distance_batch(d_a2: int, a_bases: int, d_b2: int, b_bases: int, d_pairs: int, n_pairs: int,
+                           d_dist: int, stream: int = 0) -> None:
+    """Edit distances of n_pairs pairs (fz.h); device pointers as ints."""
+    _check(None, load().fz_edit_distance_batch(d_a2 or None, a_bases, d_b2 or None, b_bases, d_pairs or None,
+                                               n_pairs, d_dist or None, stream or None))
+
+
+def fz_dtw_batch(d_x: int, x_len: int, d_y: int, y_len: int, d_pairs: int, n_pairs: int, d_cost: int,
+                 stream: int = 0) -> None:
+    """Dynamic time warping costs of n_pairs pairs (fz.h); device pointers as ints."""
+    _check(None, load().fz_dtw_batch(d_x or None, x_len, d_y or None, y_len, d_pairs or None, n_pairs,
+                                     d_cost or None, stream or None))
+
+
+def dp_pairs_device(kind: str, a, b, pairs, device="cuda"):
+    """Runs fz_edit_distance_batch (kind "edit", a and b base codes) or
+    fz_dtw_batch (kind "dtw", a and b int32 samples) on device copies of the
+    inputs; returns the int32 results on the host."""
+    import torch
+    from .workloads import pack2
+    dev = torch.device(device)
+    if kind == "edit":
+        da = torch.from_numpy(pack2(np.asarray(a, np.uint8))).to(dev)
+        db = torch.from_numpy(pack2(np.asarray(b, np.uint8))).to(dev)
+    else:
+        da = torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+        db = torch.from_numpy(np.ascontiguousarray(b, np.int32)).to(dev)
+    dp = torch.from_numpy(np.ascontiguousarray(pairs, PAIR_DTYPE).view(np.uint8)).to(dev)
+    out = torch.full((max(1, len(pairs)),), 0x7fffffff, dtype=torch.int32, device=dev)
+    st = torch.cuda.current_stream(dev).cuda_stream
+    fn = fz_edit_distance_batch if kind == "edit" else fz_dtw_batch
+    fn(da.data_ptr(), len(a), db.data_ptr(), len(b), dp.data_ptr(), len(pairs), out.data_ptr(), st)
+    torch.cuda.synchronize(dev)
+    return out[:len(pairs)].cpu().numpy()
 
 
 FZ_INT_RATES = 11

@@ -319,3 +319,74 @@ def window_bases(seq: np.ndarray, pos: int, side: int, max_len: int) -> np.ndarr
         return seq[pos:pos + n]
     n = max(0, min(max_len, pos))
     return seq[pos - n:pos][::-1]
+
+
+# ---------------------------------------------------------------------------
+# The DPX article's other two dynamic programs (section 4.1 times a batch of
+# 512 edit distances of 1024 x 1024 and 256 DTWs of 800 x 800 on random
+# sequences): pairs laid end to end in two sequences, half of them related.
+# ---------------------------------------------------------------------------
+DP_PAIR_DTYPE = np.dtype([("a_pos", "<u8"), ("b_pos", "<u8"), ("a_len", "<u4"), ("b_len", "<u4")])
+
+
+@dataclasses.dataclass
+class DPWorkload:
+    name: str
+    kind: str                   # "edit" (base codes) or "dtw" (int32 samples)
+    a: np.ndarray
+    b: np.ndarray
+    pairs: np.ndarray           # DP_PAIR_DTYPE
+    note: str = ""
+
+
+def _dp_pairs(lens_a, lens_b):
+    pairs = np.zeros(len(lens_a), DP_PAIR_DTYPE)
+    pairs["a_len"] = lens_a
+    pairs["b_len"] = lens_b
+    pairs["a_pos"][1:] = np.cumsum(np.asarray(lens_a, np.uint64))[:-1]
+    pairs["b_pos"][1:] = np.cumsum(np.asarray(lens_b, np.uint64))[:-1]
+    return pairs
+
+
+def make_edit_batch(n_pairs: int = 512, length: int = 1024, seed: int = 6) -> DPWorkload:
+    """n_pairs DNA pairs of `length` bases; half the b sequences are the a
+    sequence with 10% substitutions and 1% indels (trimmed or padded with
+    random bases to `length`), half unrelated."""
+    rng = rng_for(seed)
+    a_parts, b_parts = [], []
+    for k in range(n_pairs):
+        a = random_bases(rng, length)
+        if k % 2 == 0:
+            b = mutate(rng, a, 0.10, 0.01, 2.0)[:length]
+            b = np.concatenate([b, random_bases(rng, length - b.size)]) if b.size < length else b
+        else:
+            b = random_bases(rng, length)
+        a_parts.append(a)
+        b_parts.append(b.astype(np.uint8))
+    return DPWorkload(f"edit-{length}", "edit", np.concatenate(a_parts), np.concatenate(b_parts),
+                      _dp_pairs([length] * n_pairs, [length] * n_pairs),
+                      f"{n_pairs} edit distances of {length} x {length} bases")
+
+
+def random_walk(rng: np.random.Generator, n: int, step: int = 8) -> np.ndarray:
+    return np.clip(np.cumsum(rng.integers(-step, step + 1, n)), -32767, 32767).astype(np.int32)
+
+
+def make_dtw_batch(n_pairs: int = 256, length: int = 800, seed: int = 7) -> DPWorkload:
+    """n_pairs pairs of `length` int32 samples (random walks); half the y
+    sequences are x resampled along a random monotone warp plus noise, half
+    independent walks."""
+    rng = rng_for(seed)
+    xs, ys = [], []
+    for k in range(n_pairs):
+        x = random_walk(rng, length)
+        if k % 2 == 0:
+            warp = np.sort(rng.integers(0, length, length))
+            y = np.clip(x[warp] + rng.integers(-3, 4, length), -32767, 32767).astype(np.int32)
+        else:
+            y = random_walk(rng, length)
+        xs.append(x)
+        ys.append(y)
+    return DPWorkload(f"dtw-{length}", "dtw", np.concatenate(xs), np.concatenate(ys),
+                      _dp_pairs([length] * n_pairs, [length] * n_pairs),
+                      f"{n_pairs} dynamic time warpings of {length} x {length} samples")

@@ -252,6 +252,48 @@ fz_status fz_local_fill_noalloc(const int32_t sub[16], int32_t gap_open, int32_t
                                 uint32_t n_seeds, fz_result* d_out, void* cuda_stream);
 
 /*
+ * Two more dynamic programs on the same instructions (the DPX intrinsics
+ * article, section 1.3: edit distance and dynamic time warping, like
+ * alignment, take a minimum over three sources plus an add; section 4.1 times
+ * a batch of 512 edit distances of 1024 x 1024 and 256 DTWs of 800 x 800).
+ * Each pair k compares a[a_pos .. a_pos + a_len) with b[b_pos .. b_pos + b_len).
+ */
+typedef struct {
+    uint64_t a_pos, b_pos;
+    uint32_t a_len, b_len;      /* at most FZ_DP_MAX_LEN each */
+} fz_pair;                      /* 24 bytes */
+#define FZ_DP_MAX_LEN 4096
+
+/*
+ * Edit distance (Levenshtein: substitution, insertion and deletion cost 1) of
+ * n_pairs pairs of 2-bit packed DNA slices (the layout of fz_extend_batch's
+ * sequences; a_bases / b_bases bases in d_a2 / d_b2):
+ *   D(i,0) = i, D(0,j) = j,
+ *   D(i,j) = min(D(i-1,j) + 1, D(i,j-1) + 1, D(i-1,j-1) + [a_i != b_j]).
+ * d_dist[k] = D(a_len, b_len), or -2 for a pair longer than FZ_DP_MAX_LEN or
+ * outside its sequence.  All pointers are caller-owned device memory (d_pairs:
+ * n_pairs records; d_dist: n_pairs int32).  Asynchronous on cuda_stream; no
+ * allocation, no host synchronisation.  FZ_ERR_ARG for null pointers with
+ * n_pairs > 0; FZ_ERR_CUDA if a CUDA error is pending when called (left
+ * pending) or the launch fails.
+ */
+fz_status fz_edit_distance_batch(const uint8_t* d_a2, uint64_t a_bases, const uint8_t* d_b2, uint64_t b_bases,
+                                 const fz_pair* d_pairs, uint32_t n_pairs, int32_t* d_dist, void* cuda_stream);
+
+/*
+ * Dynamic time warping of n_pairs pairs of int32 sample slices (d_x: x_len
+ * samples, d_y: y_len), cell cost |x_i - y_j|:
+ *   D(0,0) = 0, D(i,0) = D(0,j) = infinity for i, j >= 1,
+ *   D(i,j) = |x_i - y_j| + min(D(i-1,j), D(i,j-1), D(i-1,j-1)).
+ * d_cost[k] = D(a_len, b_len) (below 2^30); 0 when both slices are empty, -1
+ * when exactly one is (no warping path), -2 for a pair longer than
+ * FZ_DP_MAX_LEN, outside its sequence, or with a sample outside
+ * [-32767, 32767].  Memory, streams and errors as fz_edit_distance_batch.
+ */
+fz_status fz_dtw_batch(const int32_t* d_x, uint64_t x_len, const int32_t* d_y, uint64_t y_len,
+                       const fz_pair* d_pairs, uint32_t n_pairs, int32_t* d_cost, void* cuda_stream);
+
+/*
  * Integer-pipe throughput microbenchmark (whole GPU, current device), written
  * to rates[0 .. FZ_INT_RATES-1]:
  *   0  DPX add-max __viaddmax_s32            op/s (one 32-bit lane each)
