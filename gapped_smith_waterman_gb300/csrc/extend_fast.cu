@@ -148,7 +148,8 @@ struct StepIn {
 };
 
 // Direction code of a cell, added into nibble r of the lane's codes: bits 0-1
-// the source of S (0 diagonal, 1 I, 2 D, in that order of preference), bit 2
+// the source of S (0 diagonal, 1 I, 2 D, in that order of preference; from the
+// DPX predicates, cell_max), bit 2
 // set when I opens from h on the left, bit 3 when D opens from h above.  I >= h
 // and D >= h_up always, so "opens" is "h - I is not negative": the sign bit of
 // h - I, taken with a high multiply, is the complement of bit 2 (likewise for
@@ -157,14 +158,27 @@ struct StepIn {
 // starts both words at 12 in every nibble it stores, so each nibble's sum is
 // its code in 0..15 and the words hold the codes once all rows are added.
 template <int KA>
-__device__ __forceinline__ void packed_code(uint32_t (&packed)[2], int r, int32_t G, int32_t S, int32_t Ic,
-                                            int32_t Dc, int32_t hl, int32_t hu, int32_t one) {
+__device__ __forceinline__ void packed_code(uint32_t (&packed)[2], int r, uint32_t sc, int32_t Ic, int32_t Dc,
+                                            int32_t hl, int32_t hu, int32_t one) {
   // (one is a runtime 1: the products stay multiply-adds on the FMA pipe)
-  const uint32_t sc = G == S ? 0u : (Ic == S ? 1u : 2u);
   const uint32_t ie = __umulhi((uint32_t)imad(Ic, -one, hl), 2u);     // I extends
   const uint32_t de = __umulhi((uint32_t)imad(Dc, -one, hu), 2u);     // D extends
   const uint32_t nib = (uint32_t)imad((int32_t)de, -8, imad((int32_t)ie, -4, (int32_t)sc));
   packed[r >> 3] = (uint32_t)imad((int32_t)nib, (int32_t)(1u << (4 * (r & 7))), (int32_t)packed[r >> 3]);
+}
+
+// S of a cell and, for the executor, the source of S as the DPX predicates
+// give it: __vibmax_s32(a, b, &p) returns max(a, b) with p = (a >= b) (a wins
+// a tie; measured on the GB300), so the diagonal wins over I and D and I over
+// D, the traceback's order of preference.  sc: 0 diagonal, 1 I, 2 D.
+template <bool TRACE>
+__device__ __forceinline__ int32_t cell_max(int32_t G, int32_t Ic, int32_t Dc, uint32_t& sc) {
+  if (!TRACE) return __vimax3_s32(G, Ic, Dc);
+  bool i_over_d, diag;
+  const int32_t id = __vibmax_s32(Ic, Dc, &i_over_d);
+  const int32_t S = __vibmax_s32(G, id, &diag);
+  sc = diag ? 0u : (i_over_d ? 1u : 2u);
+  return S;
 }
 
 // Word w of a lane's packed codes before any row is added: 12 in each of the
@@ -202,13 +216,14 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       const int32_t hp = r ? L.HP[r - 1] : hp_top;
       const uint32_t sel = (r & 1) ? __umulhi(L.QP[r >> 1], 65536u) : L.QP[r >> 1];
       const int32_t G = imad((int32_t)prmt(L.MR[r], 0u, sel), in.one, hp);   // hp carries + o + e - 128
-      const int32_t S = __vimax3_s32(G, Ic, Dc);
+      uint32_t sc = 0;
+      const int32_t S = cell_max<TRACE>(G, Ic, Dc, sc);
       const int32_t hn = imad(S, in.one, -in.oe);
       bool alive = hn >= in.Th;
       if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
       if (TRACE) {
         const int32_t hu = r ? L.H[r - 1] : hu_top;
-        packed_code<KA>(packed, r, G, S, Ic, Dc, hl, hu, in.one);
+        packed_code<KA>(packed, r, sc, Ic, Dc, hl, hu, in.one);
       }
       L.HP[r] = imad(hl, in.one, in.c1);   // next step's diagonal source, offset by o + e - 128
       L.H[r] = alive ? hn : NEG;
@@ -235,11 +250,12 @@ __device__ __forceinline__ int32_t step(LaneState<KS>& L, const StepIn& in, int 
       const int32_t hp = L.HP[r];
       const uint32_t sel = (r & 1) ? __umulhi(L.QP[r >> 1], 65536u) : L.QP[r >> 1];
       const int32_t G = imad((int32_t)prmt(L.MR[r], 0u, sel), in.one, hp);   // hp carries + o + e - 128
-      const int32_t S = __vimax3_s32(G, Ic, Dc);
+      uint32_t sc = 0;
+      const int32_t S = cell_max<TRACE>(G, Ic, Dc, sc);
       const int32_t hn = imad(S, in.one, -in.oe);
       bool alive = hn >= in.Th;
       if (EDGE) alive = alive && r <= in.vhi && r >= in.vlo;
-      if (TRACE) packed_code<KA>(packed, r, G, S, Ic, Dc, hl, hu, in.one);
+      if (TRACE) packed_code<KA>(packed, r, sc, Ic, Dc, hl, hu, in.one);
       L.HP[r] = imad(hl, in.one, in.c1);
       L.H[r] = alive ? hn : NEG;
       L.I[r] = Ic;

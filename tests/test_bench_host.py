@@ -6,12 +6,14 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
+from gapped_smith_waterman_gb300 import workloads as W  # noqa: E402
 
 KEYS = {"impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
         "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"}
@@ -110,3 +112,14 @@ def test_every_phase_kernel_names_a_source_file():
 
 def test_cpu_model_is_a_nonempty_string():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+@pytest.mark.parametrize("ws", [1, 2, 3, 8])
+def test_rank_shards_cover_the_batch_in_order(ws):
+    seeds = np.zeros(1001, W.SEED_DTYPE)
+    seeds["t_pos"] = np.arange(1001)
+    parts = [bench.rank_seeds(seeds, r, ws) for r in range(ws)]
+    joined = np.concatenate(parts)
+    assert np.array_equal(joined["t_pos"], seeds["t_pos"])
+    sizes = [len(p) for p in parts]
+    assert max(sizes) - min(sizes) <= 1
