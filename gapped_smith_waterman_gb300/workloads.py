@@ -339,7 +339,7 @@ class DPWorkload:
     note: str = ""
 
 
-def _dp_pairs(lens_a, lens_b):
+def dp_pairs(lens_a, lens_b):
     pairs = np.zeros(len(lens_a), DP_PAIR_DTYPE)
     pairs["a_len"] = lens_a
     pairs["b_len"] = lens_b
@@ -364,7 +364,7 @@ def make_edit_batch(n_pairs: int = 512, length: int = 1024, seed: int = 6) -> DP
         a_parts.append(a)
         b_parts.append(b.astype(np.uint8))
     return DPWorkload(f"edit-{length}", "edit", np.concatenate(a_parts), np.concatenate(b_parts),
-                      _dp_pairs([length] * n_pairs, [length] * n_pairs),
+                      dp_pairs([length] * n_pairs, [length] * n_pairs),
                       f"{n_pairs} edit distances of {length} x {length} bases")
 
 
@@ -388,5 +388,5 @@ def make_dtw_batch(n_pairs: int = 256, length: int = 800, seed: int = 7) -> DPWo
         xs.append(x)
         ys.append(y)
     return DPWorkload(f"dtw-{length}", "dtw", np.concatenate(xs), np.concatenate(ys),
-                      _dp_pairs([length] * n_pairs, [length] * n_pairs),
+                      dp_pairs([length] * n_pairs, [length] * n_pairs),
                       f"{n_pairs} dynamic time warpings of {length} x {length} samples")

@@ -48,7 +48,7 @@ def _mixed_pairs(kind, rng, lens):
     dt = np.uint8 if kind == "edit" else np.int32
     a = np.concatenate(a_parts).astype(dt) if a_parts else np.zeros(0, dt)
     b = np.concatenate(b_parts).astype(dt) if b_parts else np.zeros(0, dt)
-    return a, b, W._dp_pairs(la, lb)
+    return a, b, W.dp_pairs(la, lb)
 
 
 EDGE_LENS = [(0, 0), (0, 5), (7, 0), (1, 1), (1, 1500), (1500, 1), (31, 33), (32, 32), (1023, 1024),
@@ -81,13 +81,13 @@ def test_limits_and_bad_samples():
     rng = np.random.default_rng(13)
     a = rng.integers(0, 4, 9000).astype(np.uint8)
     b = rng.integers(0, 4, 9000).astype(np.uint8)
-    pairs = W._dp_pairs([4097, 10, 10], [10, 4097, 10])
+    pairs = W.dp_pairs([4097, 10, 10], [10, 4097, 10])
     pairs["a_pos"][2] = 8995                      # runs past the end of a
     assert list(_run("edit", a, b, pairs)) == [-2, -2, -2]
     x = np.zeros(100, np.int32)
     y = np.zeros(100, np.int32)
     x[50] = 40000                                 # a sample outside [-32767, 32767]
-    p2 = W._dp_pairs([60, 40], [60, 40])
+    p2 = W.dp_pairs([60, 40], [60, 40])
     p2["a_pos"][1] = 60
     got = _run("dtw", x, y, p2)
     assert got[0] == -2 and got[1] == 0
