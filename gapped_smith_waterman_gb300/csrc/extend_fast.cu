@@ -1210,9 +1210,12 @@ __device__ __forceinline__ int pair_live_lanes(const PairState& L, uint32_t oe2)
 }
 
 // Per-warp trace of the traced pair sweep.  Anti-diagonal d's flags are row d
-// of `rows`: lane l's 8 bytes (pair_flags' acc[0], acc[1]) cover its 2 NP
-// window rows b + 2 NP l .. b + 2 NP l + 2 NP - 1; hdr[d] = b | NP << 24
-// gives the window of that step.  runs: the walk's runs, in walk order.
+// of `rows` (256 bytes): with more than 4 pairs per lane, lane l's 8 bytes
+// (pair_flags' acc[0], acc[1]) cover its 2 NP window rows b + 2 NP l ..
+// b + 2 NP l + 2 NP - 1; with at most 4 pairs acc[1] is 0 and lane l stores
+// only acc[0], as the l-th 32-bit word of the row (its first 128 bytes).
+// hdr[d] = b | NP << 24 gives the window of that step.  runs: the walk's
+// runs, in walk order.
 struct TraceSlot {
   uint2* rows;
   int32_t* hdr;
@@ -1222,7 +1225,8 @@ struct TraceSlot {
 
 template <int NP>
 __device__ __forceinline__ void trace_store(const TraceSlot& ts, const PairCtl& c, int lane, const uint32_t (&acc)[2]) {
-  ts.rows[(uint32_t)c.d * 32u + (uint32_t)lane] = make_uint2(acc[0], acc[1]);
+  if (NP <= 4) reinterpret_cast<uint32_t*>(ts.rows)[(uint32_t)c.d * 64u + (uint32_t)lane] = acc[0];
+  else ts.rows[(uint32_t)c.d * 32u + (uint32_t)lane] = make_uint2(acc[0], acc[1]);
   if (lane == 0) ts.hdr[c.d] = c.b | (NP << 24);
 }
 
@@ -1410,7 +1414,10 @@ __device__ __noinline__ uint32_t trace_walk(const TraceSlot& ts, int32_t bi, int
       sm->l0[lane] = l0;
 #pragma unroll
       for (int k = 0; k < WALK_WORDS; ++k)
-        if (l0 + k <= l1) sm->w[lane][k] = __ldcg(ts.rows + (uint32_t)dt * 32u + (uint32_t)(l0 + k));
+        if (l0 + k <= l1)
+          sm->w[lane][k] = rpl <= 8 ? make_uint2(__ldcg(reinterpret_cast<const uint32_t*>(ts.rows) +
+                                                        (uint32_t)dt * 64u + (uint32_t)(l0 + k)), 0u)
+                                    : __ldcg(ts.rows + (uint32_t)dt * 32u + (uint32_t)(l0 + k));
     }
     __syncwarp();
     // runs inside the staged window (t = d0 - (i + j) <= 31)
