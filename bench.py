@@ -413,11 +413,15 @@ def main():
     n_req = int(((side & 1) != 0).sum() + ((side & 2) != 0).sum())   # one-sided problems per step
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    rates = fz.fz_bench_int_rates() if rank == 0 else None
-
     for _ in range(args.warmup):
         ext.run(d_t, w.target.size, d_q, w.query.size, d_s, len(seeds), d_out)
         ext.stats()
+    rates = None
+    if rank == 0:
+        # integer-pipe rates on a warm GPU, the better of two runs of each (a run
+        # in a process's first moments once read 200x low)
+        r1, r2 = fz.fz_bench_int_rates(), fz.fz_bench_int_rates()
+        rates = {k: max(r1[k], r2[k]) for k in r1}
     sampler = ClockSampler(lrank)
     step_ms, cells, launches, exts = [], 0, 0, 0
     phase_tot = [0.0] * 7                      # device ms per phase over the timed steps (6: traced sweep)
