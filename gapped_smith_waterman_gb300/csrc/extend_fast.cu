@@ -1095,9 +1095,12 @@ __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const Pair
 // Warp-uniform control state of the pair sweep.  Stored values are score
 // minus B; T is the prune threshold, pend the part of its rises not yet
 // moved out of the stored values, wbest2 the stored h of a cell scoring best
-// in both halves.
+// in both halves.  The best cell is located lazily: a rise of the best score
+// records its anti-diagonal (dbest) and copies the window's h values to the
+// warp's snapshot buffer (pair_after), and pair_best_row finds the cell's row
+// when a checkpoint or the result needs it.
 struct PairCtl {
-  int32_t b, d, best, bi, bj, d_last;
+  int32_t b, d, best, dbest, d_last;
   int32_t B, T, pend;
   uint32_t wbest2;
   uint32_t lb2;              // live_mask bias: 0x8000 - the stored threshold
@@ -1107,12 +1110,19 @@ struct PairCtl {
   bool top;                  // the window's top lane holds a live cell at d
 };
 
+// Snapshot buffer of a warp (shared memory): lane l's pair q at
+// snap[32 q + l], then the stored maximum (-1 while the best cell is the
+// origin) and the window, b | NP << 24.
+constexpr int SNAP_WM = 32 * PK, SNAP_WIN = 32 * PK + 1, SNAP_WORDS = 32 * PK + 2;
+
 // After each step: the anti-diagonal's best (warp max of the stored h), a
-// rise of the best score, the last live anti-diagonal, and one ballot with
-// row b's liveness (bit 0, lane 0) and the top lane's (bit 31, lane 31).
+// rise of the best score (with a snapshot of the window), the last live
+// anti-diagonal, and one ballot with row b's liveness (bit 0, lane 0) and the
+// top lane's (bit 31, lane 31).
 template <int NP>
 __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_t lm2, const Params& p, int lane,
-                                               int32_t* sT, uint32_t m0, uint32_t m31, uint32_t& wmd_out) {
+                                               int32_t* sT, uint32_t m0, uint32_t m31, uint32_t* snap,
+                                               uint32_t& wmd_out) {
   const int32_t oe = p.oe;
   // the lane max in both halves (a 32-bit compare of such values orders them
   // like their halves)
@@ -1121,14 +1131,11 @@ __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_
   const uint32_t bits = __ballot_sync(FULL, ((L.H[0] & m0) | (lmd & m31)) != 0u);
   if (wmd > c.wbest2) {                     // implies a live cell (wbest2 > 0)
     const int32_t wm = (int32_t)lo16(wmd);
-    int rf = 2 * NP;
 #pragma unroll
-    for (int r = 2 * NP - 1; r >= 0; --r) rf = (int32_t)prow<NP>(L.H, r) == wm ? r : rf;
-    const uint32_t fm = __ballot_sync(FULL, rf < 2 * NP);
-    const int Ln = __ffs(fm) - 1;
-    const int rr = __shfl_sync(FULL, rf, Ln);
-    c.bi = c.b + Ln * 2 * NP + rr;
-    c.bj = c.d - c.bi;
+    for (int q = 0; q < NP; ++q) snap[32 * q + lane] = L.H[q];   // (each lane reads back only its own words)
+    snap[SNAP_WM] = (uint32_t)wm;                                // (the same value from every lane)
+    snap[SNAP_WIN] = (uint32_t)c.b | (NP << 24);
+    c.dbest = c.d;
     c.best = wm + oe + c.B;
     if (c.d <= 2 * EAGER_N && lane == 0) sT[c.d] = c.best;
     const int32_t Tn = threshold(c.best, p.ydrop);
@@ -1152,6 +1159,32 @@ __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_
   c.d_last = wmd != 0u ? c.d : c.d_last;
   wmd_out = wmd;
   return bits;
+}
+
+// Row of the best cell (the first cell in lane-then-row order holding the
+// stored maximum of the snapshot; the origin while no rise was seen).  Warp
+// collective.
+template <int NP>
+__device__ __forceinline__ int pair_snap_row(const uint32_t* snap, int lane, int32_t wm) {
+  uint32_t H[PK];
+#pragma unroll
+  for (int q = 0; q < NP; ++q) H[q] = snap[32 * q + lane];
+  int rf = 2 * NP;
+#pragma unroll
+  for (int r = 2 * NP - 1; r >= 0; --r) rf = (int32_t)prow<NP>(H, r) == wm ? r : rf;
+  return rf;
+}
+
+__device__ __forceinline__ int32_t pair_best_row(const uint32_t* snap, int lane) {
+  const int32_t wm = (int32_t)snap[SNAP_WM];
+  if (wm < 0) return 0;
+  const uint32_t win = snap[SNAP_WIN];
+  const int np = (int)(win >> 24);
+  const int rf = np == NP_SMALL ? pair_snap_row<NP_SMALL>(snap, lane, wm) : pair_snap_row<PK>(snap, lane, wm);
+  const uint32_t fm = __ballot_sync(FULL, rf < 2 * np);
+  const int Ln = __ffs(fm) - 1;
+  const int rr = __shfl_sync(FULL, rf, Ln);
+  return (int32_t)(win & 0xffffffu) + Ln * 2 * np + rr;
 }
 
 // Per-warp shared buffer for changing the number of pairs per lane: the
@@ -1257,7 +1290,8 @@ __device__ __forceinline__ void trace_store(const TraceSlot& ts, const PairCtl& 
 template <int NP, bool TR>
 __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& p, const Window& w, int lane,
                                      Reservoir& qr, Reservoir& tr, const uint32_t* s_mrow16, int32_t* sT,
-                                     int32_t d_stop, uint32_t m0, uint32_t m31, const TraceSlot& ts) {
+                                     int32_t d_stop, uint32_t m0, uint32_t m31, const TraceSlot& ts,
+                                     uint32_t* snap) {
   constexpr int32_t WIN = 64 * NP;
   const int32_t m = w.m, n = w.n, mn = w.m + w.n, oe = p.oe;
   const uint32_t ne2 = dup16(-p.e), noe2 = dup16(-oe), oe2 = dup16(oe);
@@ -1277,7 +1311,7 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
           const uint32_t lm2 = pstep<NP, false, false, TR>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2, acc);
           ++c.d;
           if (TR) trace_store<NP>(ts, c, lane, acc);
-          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
+          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
         }
         if ((bits & 1u) || c.d == d_fast || wmd == 0u) break;
         {
@@ -1287,7 +1321,7 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
           ++c.b;
           ++c.d;
           if (TR) trace_store<NP>(ts, c, lane, acc);
-          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
+          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
         }
         if ((int32_t)bits < 0 || c.d == d_fast || wmd == 0u) break;
       }
@@ -1318,7 +1352,7 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
       c.d = dn;
       if (TR) trace_store<NP>(ts, c, lane, acc);
       uint32_t wmd;
-      const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, wmd);
+      const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
       c.rowb_alive = bits & 1u;
       c.top = (int32_t)bits < 0;
       // (no overflow once the window reaches row m: no row lies beyond it)
@@ -1501,8 +1535,10 @@ __device__ __forceinline__ void pair_resize(PairState& L, const PairCtl& c, int 
 }
 
 __device__ __forceinline__ uint32_t pair_ckpt(int np, const WorkArgs& wa, const PairState& L, int lane,
-                                              uint32_t head, const PairCtl& c, int32_t oe, const int32_t* sT) {
-  const CkScalars cs{c.b, c.d, c.best, c.bi, c.bj, c.d_last};
+                                              uint32_t head, const PairCtl& c, int32_t oe, const int32_t* sT,
+                                              const uint32_t* snap) {
+  const int32_t bi = pair_best_row(snap, lane);
+  const CkScalars cs{c.b, c.d, c.best, bi, c.dbest - bi, c.d_last};
   return np == NP_SMALL ? ck_write_pair<NP_SMALL>(wa, L, lane, head, cs, c.B, oe, c.cnt, 0u, sT)
                         : ck_write_pair<PK>(wa, L, lane, head, cs, c.B, oe, c.cnt, 0u, sT);
 }
@@ -1514,8 +1550,9 @@ __device__ __forceinline__ uint32_t pair_ckpt(int np, const WorkArgs& wa, const 
 // executor traces it) are they copied to the pool and linked (ring_publish),
 // so that the executor splits its replay at them.
 __device__ __forceinline__ void ring_ckpt(int np, const TraceSlot& ts, uint32_t k, const PairState& L, int lane,
-                                          const PairCtl& c, int32_t oe, const int32_t* sT) {
-  const CkScalars cs{c.b, c.d, c.best, c.bi, c.bj, c.d_last};
+                                          const PairCtl& c, int32_t oe, const int32_t* sT, const uint32_t* snap) {
+  const int32_t bi = pair_best_row(snap, lane);
+  const CkScalars cs{c.b, c.d, c.best, bi, c.dbest - bi, c.d_last};
   int32_t* dst = ts.ring + (uint64_t)k * CK_SLOT_WORDS;
   if (np == NP_SMALL) ck_fill_pair<NP_SMALL>(dst, L, lane, 0u, cs, c.B, oe, c.cnt, 0u, sT);
   else ck_fill_pair<PK>(dst, L, lane, 0u, cs, c.B, oe, c.cnt, 0u, sT);
@@ -1559,7 +1596,7 @@ __device__ __noinline__ uint32_t ring_publish(const WorkArgs& wa, const TraceSlo
 template <bool TR>
 __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t ext, int lane, int32_t* sT,
                                  uint8_t* tile, const uint32_t* s_mrow16, const int32_t* s_sub, PairRelay* rb,
-                                 const TraceSlot& ts, WalkStage* wsm) {
+                                 const TraceSlot& ts, WalkStage* wsm, uint32_t* snap) {
   constexpr int32_t WIN = 64 * PK;   // the first tier's largest window (the executor's row width)
   const Window w = make_window(p, ext);
   ExtRec* R = wa.rec + ext;
@@ -1572,7 +1609,8 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   }
   const int32_t m = w.m, n = w.n, oe = p.oe, mn = w.m + w.n;
   PairCtl c;
-  c.b = 0; c.d = 0; c.best = 0; c.bi = 0; c.bj = 0; c.d_last = 0;
+  c.b = 0; c.d = 0; c.best = 0; c.dbest = 0; c.d_last = 0;
+  if (lane == 0) snap[SNAP_WM] = 0xffffffffu;   // best cell: the origin
   c.T = threshold(0, p.ydrop);
   c.B = c.T - PMG;                          // stored value = score-space value - B
   // A rise of the threshold is first only added to the stored threshold
@@ -1621,8 +1659,8 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   while (why != 2) {
     const uint32_t mask = np == PK ? (ex_mask & 63u) : ex_mask;
     const int32_t d_stop = (int32_t)(((uint32_t)c.d | mask) + 1u);
-    why = np == PK ? pair_run<PK, TR>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31, ts)
-                   : pair_run<NP_SMALL, TR>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31, ts);
+    why = np == PK ? pair_run<PK, TR>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31, ts, snap)
+                   : pair_run<NP_SMALL, TR>(L, c, p, w, lane, qr, tr, s_mrow16, sT, d_stop, m0, m31, ts, snap);
     if (why != 0 || ((uint32_t)c.d & ex_mask) == 0u) {
       c.cnt += live_count(c.live2);
       c.live2 = 0u;
@@ -1638,10 +1676,10 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       c.top = false;        // the new top lane's rows lay beyond the old window: dead
       continue;
     }
-    if (!TR && ((uint32_t)c.d & ck_mask) == 0u && c.d - (c.bi + c.bj) <= wa.ckpt_recent)
-      head = pair_ckpt(np, wa, L, lane, head, c, oe, sT);
+    if (!TR && ((uint32_t)c.d & ck_mask) == 0u && c.d - c.dbest <= wa.ckpt_recent)
+      head = pair_ckpt(np, wa, L, lane, head, c, oe, sT, snap);
     if (TR && wa.ckpt && ((uint32_t)c.d & (wa.tring_every - 1u)) == 0u && nring < wa.tring) {
-      ring_ckpt(np, ts, nring, L, lane, c, oe, sT);
+      ring_ckpt(np, ts, nring, L, lane, c, oe, sT, snap);
       ++nring;
     }
     if (np == PK) {
@@ -1655,7 +1693,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   }
   if (overflow && wa.ckpt) {
     if (TR && nring) head = ring_publish(wa, ts, nring, lane);
-    head = pair_ckpt(PK, wa, L, lane, head, c, oe, sT);
+    head = pair_ckpt(PK, wa, L, lane, head, c, oe, sT, snap);
   }
 
   uint64_t tot = c.cnt;
@@ -1674,7 +1712,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     }
     return;
   }
-  const int32_t best = c.best, bi = c.bi, bj = c.bj;
+  const int32_t best = c.best, bi = pair_best_row(snap, lane), bj = c.dbest - bi;
   uint64_t path = 0;
   uint32_t npath = 0;
   uint32_t flags = FZ_FLAG_DONE;
@@ -1730,6 +1768,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
   __shared__ uint8_t s_tile[WARPS][(EAGER_N + 1) * (EAGER_N + 1)];
   __shared__ PairRelay s_relay[WARPS];
   __shared__ WalkStage s_walk[TR ? WARPS : 1];
+  __shared__ uint32_t s_snap[WARPS][SNAP_WORDS];
   __shared__ uint32_t s_mrow16[4];
   __shared__ int32_t s_sub[16];
   if (threadIdx.x < 4) s_mrow16[threadIdx.x] = p.mrow16[threadIdx.x];
@@ -1755,7 +1794,7 @@ __global__ void __launch_bounds__(WARPS * 32, 4) k_pair(Params p, WorkArgs wa) {
     if (idx >= nw) break;
     const uint32_t ext = wa.list ? wa.list[lbase + idx] : lbase + idx;
     run_inspect_pair<TR>(p, wa, ext, lane, s_T[warp], s_tile[warp], s_mrow16, s_sub, &s_relay[warp], ts,
-                         &s_walk[TR ? warp : 0]);
+                         &s_walk[TR ? warp : 0], s_snap[warp]);
   }
 }
 
