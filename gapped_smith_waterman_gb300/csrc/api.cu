@@ -155,7 +155,7 @@ fz_status ensure_batch_buffers(fz_ctx* ctx, uint32_t n_ext) {
   CU(ctx->counters.ensure(sizeof(Counters)));
   if (ctx->mode == FZ_EXTEND) {
     const uint64_t per = wide_scratch_elems(ctx->p.max_len) * 4;
-    CU(ctx->scratch.ensure((size_t)ctx->grid_wide * wide_warps_per_block() * per));
+    CU(ctx->scratch.ensure((size_t)ctx->grid_wide * per));
   } else if (!ctx->local_use_smem) {
     const uint64_t per = 2ull * (ctx->p.max_len + 1) * 4;
     CU(ctx->spill.ensure((size_t)ctx->grid_local * local_warps_per_block() * per));
@@ -549,7 +549,9 @@ fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32
     ctx->grid_fast[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, false, p.pair_ok != 0);
     ctx->grid_fast_trace[tier] = ctx->sms * extend_fast_blocks_per_sm(tier, true, false);
   }
-  ctx->grid_wide = ctx->sms;
+  // wide path: one block per extension, as many as fit with the ring
+  // (a failure shows as the pending error checked below)
+  ctx->grid_wide = ctx->sms * std::max(1, wide_blocks_per_sm(max_len));
   {
     // traced sweep: one trace slot per resident warp (at most one per
     // extension of the batch), enough rows for the longest sweep

@@ -1,12 +1,19 @@
 // General-band anti-diagonal sweep (sm_103a): the path for extensions whose
-// live band outgrows the register window (very large ydrop, long gapped
-// regions).  One warp per extension; the last three anti-diagonals live in a
-// per-warp global scratch indexed by target row (L1/L2 resident), each lane
-// computes one cell of a 32-cell chunk, chunks cover the candidate band
-// [lo, hi] of the anti-diagonal: rows that have a live predecessor on one of
-// the two previous anti-diagonals (FastZ section 3.2 strips, spilled to memory
-// instead of kept in registers).  Liveness is tracked exactly as written in
-// the y-drop rule: dead cells hold NEG in S, I and D.
+// live band outgrows the register windows (very large ydrop, long gapped
+// regions), and for every extension when the scores do not fit the byte forms.
+//
+// One block (CTA) per extension.  Each anti-diagonal's candidate band [lo, hi]
+// (rows with a live predecessor on one of the two previous anti-diagonals) is
+// cut into 32-row strips, dealt round-robin to the block's warps (FastZ
+// section 3.2: strips of an anti-diagonal computed side by side, the strip
+// boundaries exchanged through memory).  A cell reads its three predecessors
+// from the last two anti-diagonals, which the block keeps in a shared-memory
+// ring indexed by target row modulo the ring size; the anti-diagonal's
+// maximum (earliest row on ties) and live range are combined across the warps
+// once per anti-diagonal, in the same barrier that publishes its cells.  When
+// a band is wider than the ring, the three anti-diagonals move to a per-block
+// global scratch indexed by row and the sweep continues there.  Liveness
+// follows the y-drop rule as written: dead cells hold NEG in S, I and D.
 #include <cuda_runtime.h>
 
 #include "fz_dev.cuh"
@@ -16,7 +23,17 @@ namespace fz {
 
 namespace {
 
-constexpr int WW = 4;   // warps per block
+constexpr int CW = 4;               // warps per block
+constexpr int CT = CW * 32;         // threads per block
+constexpr int RING_MAX = 2048;      // rows of the shared-memory ring at most
+
+// Ring rows for windows of up to max_len rows: a power of two holding a whole
+// window when it fits RING_MAX.
+__host__ __device__ inline int32_t ring_rows(int32_t max_len) {
+  int32_t c = 64;
+  while (c < max_len + 1 && c < RING_MAX) c <<= 1;
+  return c;
+}
 
 __device__ __forceinline__ uint32_t base_at(const uint8_t* __restrict__ s, uint64_t len, int64_t g0, int dir,
                                             int64_t w) {
@@ -25,71 +42,65 @@ __device__ __forceinline__ uint32_t base_at(const uint8_t* __restrict__ s, uint6
   return ((uint32_t)__ldg(s + (g >> 2)) >> ((g & 3) * 2)) & 3u;
 }
 
-__device__ __forceinline__ int mod3(int32_t d) { return ((d % 3) + 3) % 3; }
+// Candidate band of an anti-diagonal already computed: the rows written
+// [blo, bhi] (dead ones hold NEG), the live rows [llo, lhi], and which of the
+// three buffers holds it.
+struct Band {
+  int32_t blo, bhi, llo, lhi;
+  int k;
+};
 
-template <bool TRACE>
-__device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint32_t idx, int lane,
-                         int32_t* buf, int32_t cap, const int32_t* s_sub) {
-  const Window w = make_window(p, ext);
-  ExtRec* R = wa.rec + ext;
-  if (!w.requested) {
-    if (!TRACE && lane == 0) {
-      ExtRec z = {};
-      *R = z;
-    }
-    return;
+// Sweep state shared by every thread of the block (each keeps its own copy;
+// all copies follow the same block-wide values).
+struct WideState {
+  Band b1, b2;                      // anti-diagonals dn - 1 and dn - 2
+  int32_t dn;                       // next anti-diagonal
+  int32_t best, bi, bj, d_last, wrun, wbest;
+};
+
+// Buffer k's component c (0 S, 1 I, 2 D) at row i: buf[(3 k + c) stride + (i & mask)].
+template <bool SMEM>
+struct Bufs {
+  int32_t* buf;
+  int32_t stride, mask;
+  __device__ __forceinline__ int32_t* at(int k, int c, int32_t i) const {
+    return buf + (3 * k + c) * stride + (i & mask);
   }
+};
+
+// Anti-diagonals from s.dn on, until the sweep ends (true) or, in the ring, a
+// band wider than the ring (false: s.dn is the anti-diagonal still to do).
+template <bool TRACE, bool SMEM>
+__device__ bool wide_run(const Params& p, const Window& w, WideState& s, const Bufs<SMEM>& B, int32_t ring,
+                         int32_t d_stop, uint32_t W, uint8_t* tbase, int32_t* lo_arr, const int32_t* s_sub,
+                         int4 (*red)[CW], uint32_t& cnt, int tid, int warp, int lane) {
   const int32_t m = w.m, n = w.n, oe = p.oe, e = p.e;
-  int32_t* Sb[3];
-  int32_t* Ib[3];
-  int32_t* Db[3];
-#pragma unroll
-  for (int k = 0; k < 3; ++k) {
-    Sb[k] = buf + (3 * k + 0) * (int64_t)cap;
-    Ib[k] = buf + (3 * k + 1) * (int64_t)cap;
-    Db[k] = buf + (3 * k + 2) * (int64_t)cap;
-  }
-  int32_t blo[3], bhi[3], llo[3], lhi[3];
-#pragma unroll
-  for (int k = 0; k < 3; ++k) { blo[k] = 1; bhi[k] = 0; llo[k] = 1; lhi[k] = 0; }
-  if (lane == 0) { Sb[0][0] = 0; Ib[0][0] = NEG; Db[0][0] = NEG; }
-  blo[0] = 0; bhi[0] = 0; llo[0] = 0; lhi[0] = 0;
-
-  int32_t d_stop = 0x7fffffff;
-  uint32_t W = 0;
-  uint8_t* tbase = nullptr;
-  int32_t* lo_arr = nullptr;
-  if (TRACE) {
-    d_stop = R->i_end + R->j_end;
-    W = R->width;
-    tbase = wa.trace + (wa.trace_off[idx] - wa.trace_sub);
-    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(W, d_stop));
-    if (lane == 0) lo_arr[0] = 0;
-  }
-  int32_t best = 0, bi = 0, bj = 0, d_last = 0, wrun = 1, wbest = 1;
-  uint32_t cnt = lane == 0 ? 1u : 0u;
-  __syncwarp();
-
-  for (int32_t dn = 1; dn <= m + n; ++dn) {
-    if (dn > d_stop) break;
-    const int k1 = mod3(dn - 1), k2 = mod3(dn - 2), kc = mod3(dn);
+  for (; s.dn <= m + n; ++s.dn) {
+    const int32_t dn = s.dn;
+    if (dn > d_stop) return true;
+    const Band& b1 = s.b1;
+    const Band& b2 = s.b2;
     int32_t lo = 0x7fffffff, hi = -0x7fffffff;
-    if (lhi[k1] >= llo[k1]) { lo = llo[k1]; hi = lhi[k1] + 1; }
-    if (lhi[k2] >= llo[k2]) { lo = imin(lo, llo[k2] + 1); hi = imax(hi, lhi[k2] + 1); }
+    if (b1.lhi >= b1.llo) { lo = b1.llo; hi = b1.lhi + 1; }
+    if (b2.lhi >= b2.llo) { lo = imin(lo, b2.llo + 1); hi = imax(hi, b2.lhi + 1); }
     lo = imax(lo, imax(0, dn - n));
     hi = imin(hi, imin(m, dn));
-    if (lo > hi) break;
-    const int32_t T = threshold(best, p.ydrop);
+    if (lo > hi) return true;
+    if (SMEM && hi - lo + 1 > ring) return false;
+    const int kc = 3 - b1.k - b2.k;
+    const int32_t T = threshold(s.best, p.ydrop);
     int32_t mx = NEG, mi = 0x7fffffff, a_lo = 0x7fffffff, a_hi = -1;
-    for (int32_t c = lo; c <= hi; c += 32) {
+    // (the strip loop's bound is uniform within a warp, so every lane takes
+    // part in the shuffle that pairs trace codes)
+    for (int32_t c = lo + 32 * warp; c <= hi; c += CT) {
       const int32_t i = c + lane;
       const bool act = i <= hi;
       const int32_t j = dn - i;
       int32_t sl = NEG, il = NEG, su = NEG, du = NEG, sd = NEG;
       if (act) {
-        if (j >= 1 && i >= blo[k1] && i <= bhi[k1]) { sl = Sb[k1][i]; il = Ib[k1][i]; }
-        if (i >= 1 && i - 1 >= blo[k1] && i - 1 <= bhi[k1]) { su = Sb[k1][i - 1]; du = Db[k1][i - 1]; }
-        if (i >= 1 && j >= 1 && i - 1 >= blo[k2] && i - 1 <= bhi[k2]) sd = Sb[k2][i - 1];
+        if (j >= 1 && i >= b1.blo && i <= b1.bhi) { sl = *B.at(b1.k, 0, i); il = *B.at(b1.k, 1, i); }
+        if (i >= 1 && i - 1 >= b1.blo && i - 1 <= b1.bhi) { su = *B.at(b1.k, 0, i - 1); du = *B.at(b1.k, 2, i - 1); }
+        if (i >= 1 && j >= 1 && i - 1 >= b2.blo && i - 1 <= b2.bhi) sd = *B.at(b2.k, 0, i - 1);
       }
       const int32_t Iv = j >= 1 ? imax(il - e, sl - oe) : NEG;
       const int32_t Dv = i >= 1 ? imax(du - e, su - oe) : NEG;
@@ -102,9 +113,9 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
       const int32_t S = imax(G, imax(Iv, Dv));
       const bool alive = act && S >= T;
       if (act) {
-        Sb[kc][i] = alive ? S : NEG;
-        Ib[kc][i] = alive ? Iv : NEG;
-        Db[kc][i] = alive ? Dv : NEG;
+        *B.at(kc, 0, i) = alive ? S : NEG;
+        *B.at(kc, 1, i) = alive ? Iv : NEG;
+        *B.at(kc, 2, i) = alive ? Dv : NEG;
       }
       if (alive) {
         ++cnt;
@@ -113,6 +124,8 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
         a_hi = imax(a_hi, i);
       }
       if (TRACE) {
+        // rows lo + 2u and lo + 2u + 1 sit in lanes of the same warp (strips
+        // start at lo + 32 k)
         const uint32_t code = (G == S ? 0u : (Iv == S ? 1u : 2u)) | (j >= 1 && Iv == sl - oe ? 4u : 0u) |
                               (i >= 1 && Dv == su - oe ? 8u : 0u);
         const uint32_t hi4 = __shfl_down_sync(FULL, code, 1);
@@ -120,53 +133,126 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
         if (act && !(lane & 1) && u < W) tbase[(uint64_t)dn * (W / 2) + (u >> 1)] = (uint8_t)(code | (hi4 << 4));
       }
     }
-    const int32_t wm = __reduce_max_sync(FULL, mx);
-    const uint32_t wi = __reduce_min_sync(FULL, (mx == wm && mx != NEG) ? (uint32_t)mi : 0xffffffffu);
-    const int32_t nlo = (int32_t)__reduce_min_sync(FULL, (uint32_t)a_lo);
-    const int32_t nhi = (int32_t)__reduce_max_sync(FULL, (uint32_t)(a_hi + 1)) - 1;
-    blo[kc] = lo; bhi[kc] = hi;
-    llo[kc] = nlo; lhi[kc] = nhi;
-    wrun = imax(wrun, hi - lo + 1);
-    if (wm != NEG) {
-      d_last = dn;
-      if (wm > best) { best = wm; bi = (int32_t)wi; bj = dn - bi; wbest = wrun; }
+    {
+      const int32_t wm = __reduce_max_sync(FULL, mx);
+      const uint32_t wi = __reduce_min_sync(FULL, (mx == wm && mx != NEG) ? (uint32_t)mi : 0xffffffffu);
+      const uint32_t wlo = __reduce_min_sync(FULL, (uint32_t)a_lo);
+      const int32_t whi = (int32_t)__reduce_max_sync(FULL, (uint32_t)(a_hi + 1)) - 1;
+      if (lane == 0) red[dn & 1][warp] = make_int4(wm, (int32_t)wi, (int32_t)wlo, whi);
     }
-    if (TRACE && lane == 0) lo_arr[dn] = lo;
-    __syncwarp();
-  }
-  uint64_t tot = cnt;
+    // publishes this anti-diagonal's cells and the warps' partial results
+    // (red alternates by parity: a warp writing anti-diagonal dn + 1's entry
+    // cannot overwrite one that a slower warp is still reading)
+    __syncthreads();
+    int32_t wm = NEG, nlo = 0x7fffffff, nhi = -1;
+    uint32_t wi = 0xffffffffu;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
-  if (TRACE) {
-    if (lane == 0) {
-      atomicAdd(wa.exec_total, (unsigned long long)tot);
-      atomicAdd(wa.exec_live, (unsigned long long)tot);
+    for (int k = 0; k < CW; ++k) {
+      const int4 r = red[dn & 1][k];
+      if (r.x > wm) { wm = r.x; wi = (uint32_t)r.y; }
+      else if (r.x == wm && (uint32_t)r.y < wi) wi = (uint32_t)r.y;
+      nlo = imin(nlo, r.z);
+      nhi = imax(nhi, r.w);
     }
-    return;
+    s.b2 = s.b1;
+    s.b1 = Band{lo, hi, nlo, nhi, kc};
+    s.wrun = imax(s.wrun, hi - lo + 1);
+    if (wm != NEG) {
+      s.d_last = dn;
+      if (wm > s.best) { s.best = wm; s.bi = (int32_t)wi; s.bj = dn - s.bi; s.wbest = s.wrun; }
+    }
+    if (TRACE && tid == 0) lo_arr[dn] = lo;
   }
-  if (lane == 0) {
-    ExtRec o;
-    o.score = best; o.i_end = bi; o.j_end = bj; o.d_last = d_last;
-    o.live = tot; o.path = 0; o.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE; o.npath = 0;
-    o.m = m; o.n = n; o.width = (uint32_t)((wbest + 31) & ~31); o.ckpt = 0;
-    *R = o;
-    atomicAdd(wa.live_total, (unsigned long long)tot);
-  }
+  return true;
 }
 
 template <bool TRACE>
-__global__ void __launch_bounds__(WW * 32) k_wide(Params p, WorkArgs wa) {
-  __shared__ int32_t s_sub[16];
-  if (threadIdx.x < 16) s_sub[threadIdx.x] = p.sub[threadIdx.x];
+__device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint32_t idx, int tid, int32_t* ring_buf,
+                         int32_t ring, int32_t* gbuf, int32_t cap, const int32_t* s_sub, int4 (*red)[CW],
+                         unsigned long long* s_sum) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const Window w = make_window(p, ext);
+  ExtRec* R = wa.rec + ext;
+  if (!w.requested) {
+    if (!TRACE && tid == 0) {
+      ExtRec z = {};
+      *R = z;
+    }
+    return;
+  }
+  int32_t d_stop = 0x7fffffff;
+  uint32_t W = 0;
+  uint8_t* tbase = nullptr;
+  int32_t* lo_arr = nullptr;
+  if (TRACE) {
+    d_stop = R->i_end + R->j_end;
+    W = R->width;
+    tbase = wa.trace + (wa.trace_off[idx] - wa.trace_sub);
+    lo_arr = reinterpret_cast<int32_t*>(tbase + trace_lo_offset(W, d_stop));
+    if (tid == 0) lo_arr[0] = 0;
+  }
+  // anti-diagonal 0: the origin alone, S = 0
+  WideState s;
+  s.b1 = Band{0, 0, 0, 0, 0};
+  s.b2 = Band{1, 0, 1, 0, 2};
+  s.dn = 1;
+  s.best = 0; s.bi = 0; s.bj = 0; s.d_last = 0; s.wrun = 1; s.wbest = 1;
+  uint32_t cnt = tid == 0 ? 1u : 0u;
+  const Bufs<true> RB{ring_buf, ring, ring - 1};
+  if (tid == 0) { *RB.at(0, 0, 0) = 0; *RB.at(0, 1, 0) = NEG; *RB.at(0, 2, 0) = NEG; }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint64_t gw = (uint64_t)blockIdx.x * WW + warp;
-  int32_t* buf = wa.scratch + gw * wa.scratch_stride;
+  if (!wide_run<TRACE, true>(p, w, s, RB, ring, d_stop, W, tbase, lo_arr, s_sub, red, cnt, tid, warp, lane)) {
+    // the band outgrew the ring: move the two previous anti-diagonals (the
+    // only ones still read) to the global scratch, rows at their own index
+    const Bufs<false> GB{gbuf, cap, 0x7fffffff};
+    const Band bs[2] = {s.b1, s.b2};
+    for (int q = 0; q < 2; ++q)
+      for (int32_t i = bs[q].blo + tid; i <= bs[q].bhi; i += CT)
+#pragma unroll
+        for (int c = 0; c < 3; ++c) *GB.at(bs[q].k, c, i) = *RB.at(bs[q].k, c, i);
+    __syncthreads();
+    wide_run<TRACE, false>(p, w, s, GB, cap, d_stop, W, tbase, lo_arr, s_sub, red, cnt, tid, warp, lane);
+  }
+  // live cells: warp sums, then thread 0 adds the warps' (the barrier also
+  // ends every read of the ring before the next extension writes it)
+  const unsigned long long ws = __reduce_add_sync(FULL, cnt);
+  if (lane == 0) s_sum[warp] = ws;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long tot = 0;
+    for (int k = 0; k < CW; ++k) tot += s_sum[k];
+    if (TRACE) {
+      atomicAdd(wa.exec_total, tot);
+      atomicAdd(wa.exec_live, tot);
+    } else {
+      ExtRec o;
+      o.score = s.best; o.i_end = s.bi; o.j_end = s.bj; o.d_last = s.d_last;
+      o.live = tot; o.path = 0; o.flags = FZ_FLAG_DONE | FZ_FLAG_WIDE; o.npath = 0;
+      o.m = w.m; o.n = w.n; o.width = (uint32_t)((s.wbest + 31) & ~31); o.ckpt = 0;
+      *R = o;
+      atomicAdd(wa.live_total, tot);
+    }
+  }
+  __syncthreads();   // (s_sum is rewritten by the next extension)
+}
+
+template <bool TRACE>
+__global__ void __launch_bounds__(CT) k_wide(Params p, WorkArgs wa) {
+  extern __shared__ int32_t s_ring[];             // 9 x ring rows: S, I, D of three anti-diagonals
+  __shared__ int32_t s_sub[16];
+  __shared__ int4 s_red[2][CW];
+  __shared__ unsigned long long s_sum[CW];
+  __shared__ uint32_t s_idx;
+  const int tid = threadIdx.x;
+  if (tid < 16) s_sub[tid] = p.sub[tid];
+  const int32_t ring = ring_rows(p.max_len);
+  int32_t* gbuf = wa.scratch + (uint64_t)blockIdx.x * wa.scratch_stride;
   const int32_t cap = (int32_t)(wa.scratch_stride / 9);
   for (;;) {
-    uint32_t idx = 0;
-    if (lane == 0) idx = atomicAdd(wa.counter, 1u);
-    idx = __shfl_sync(FULL, idx, 0);
+    if (tid == 0) s_idx = atomicAdd(wa.counter, 1u);
+    __syncthreads();
+    const uint32_t idx = s_idx;
+    __syncthreads();                               // (s_idx is rewritten next round)
     const uint32_t nw = TRACE ? wa.n_work : *wa.wide_count;
     if (idx >= nw) break;
     if (TRACE) {
@@ -174,25 +260,41 @@ __global__ void __launch_bounds__(WW * 32) k_wide(Params p, WorkArgs wa) {
       const uint4 sg = wa.seg[idx];
       const uint32_t ext = wa.list[sg.x];
       if (!(wa.rec[ext].flags & FZ_FLAG_WIDE)) continue;
-      wide_ext<TRACE>(p, wa, ext, sg.x, lane, buf, cap, s_sub);
+      wide_ext<TRACE>(p, wa, ext, sg.x, tid, s_ring, ring, gbuf, cap, s_sub, s_red, s_sum);
     } else {
-      wide_ext<TRACE>(p, wa, wa.list[idx], idx, lane, buf, cap, s_sub);
+      wide_ext<TRACE>(p, wa, wa.list[idx], idx, tid, s_ring, ring, gbuf, cap, s_sub, s_red, s_sum);
     }
   }
 }
 
+size_t ring_bytes(int32_t max_len) { return (size_t)9 * ring_rows(max_len) * sizeof(int32_t); }
+
 }  // namespace
 
 uint64_t wide_scratch_elems(int32_t max_len) { return 9ull * (uint64_t)(max_len + 1); }
-int wide_warps_per_block() { return WW; }
+
+int wide_blocks_per_sm(int32_t max_len) {
+  const size_t rb = ring_bytes(max_len);
+  int best = 0;
+  for (int t = 0; t < 2; ++t) {
+    const void* f = t ? reinterpret_cast<const void*>(k_wide<true>) : reinterpret_cast<const void*>(k_wide<false>);
+    // the limit of the largest ring, so that contexts with other window caps can launch too
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes(RING_MAX)) != cudaSuccess)
+      return 0;
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, CT, rb) != cudaSuccess) return 0;
+    best = t ? (nb < best ? nb : best) : nb;
+  }
+  return best;
+}
 
 cudaError_t launch_inspect_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  k_wide<false><<<grid, WW * 32, 0, st>>>(p, wa);
+  k_wide<false><<<grid, CT, ring_bytes(p.max_len), st>>>(p, wa);
   return cudaGetLastError();
 }
 
 cudaError_t launch_execute_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  k_wide<true><<<grid, WW * 32, 0, st>>>(p, wa);
+  k_wide<true><<<grid, CT, ring_bytes(p.max_len), st>>>(p, wa);
   return cudaGetLastError();
 }
 

@@ -24,8 +24,8 @@ struct WorkArgs {
   unsigned long long* exec_total;
   unsigned long long* exec_live;   // executor: live cells replayed
   uint32_t* err;               // device error word (0 = fine)
-  int32_t* scratch;            // wide path: per-warp anti-diagonal buffers
-  uint64_t scratch_stride;     // int32 elements per warp
+  int32_t* scratch;            // wide path: per-block anti-diagonal buffers (bands wider than the ring)
+  uint64_t scratch_stride;     // int32 elements per block
   // window checkpoints (register-window sweeps)
   int32_t* ckpt;               // pool of CK_SLOT_WORDS-word slots, or nullptr (none written)
   uint32_t ckpt_cap;           // slots in the pool
@@ -64,8 +64,8 @@ int traced_blocks_per_sm();
 int extend_fast_blocks_per_sm(int tier, bool trace, bool pair);  // pair: the 16-bit first tier
 
 // general band sweep (extend_wide.cu)
-uint64_t wide_scratch_elems(int32_t max_len);   // per warp
-int wide_warps_per_block();
+uint64_t wide_scratch_elems(int32_t max_len);   // per block
+int wide_blocks_per_sm(int32_t max_len);         // 0 on failure (sets the kernels' shared-memory limit)
 cudaError_t launch_inspect_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
 cudaError_t launch_execute_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st);
 

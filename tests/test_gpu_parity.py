@@ -306,6 +306,22 @@ def test_wide_band_path():
     assert st.wide > 0
 
 
+def test_wide_band_beyond_the_ring():
+    """Bands wider than the wide path's 2,048-row shared-memory ring (no
+    y-drop, windows of 2,300 to 2,700 bases, homologous and unrelated pairs):
+    the block moves its anti-diagonals to the global scratch mid-sweep, in the
+    inspector and in the executor; records and CIGARs equal the oracle's."""
+    rng = np.random.default_rng(12)
+    pairs = []
+    for L in (2300, 2500, 2700):
+        t = rng.integers(0, 4, L).astype(np.uint8)
+        pairs.append((t, W.mutate(rng, t, 0.1, 0.02, 3.0)))
+        pairs.append((t, rng.integers(0, 4, L).astype(np.uint8)))
+    w, _ = _batch_from_pairs(pairs, ydrop=W.YDROP_INF)
+    gres, gcig, st, ores = _check(w, label="wide band beyond the ring")
+    assert st.wide == len(pairs)
+
+
 def test_matrix_outside_byte_range_uses_general_path():
     rng = np.random.default_rng(9)
     sub = (W.HOXD70 * 3).astype(np.int32)          # entries beyond [-128, 127]
