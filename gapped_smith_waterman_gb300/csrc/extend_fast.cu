@@ -1456,15 +1456,14 @@ __device__ __noinline__ uint32_t trace_walk(const TraceSlot& ts, int32_t bi, int
     __syncwarp();
     // The next two stages start near d0 - 32 and d0 - 64 (the walk leaves a
     // stage 32 or 33 anti-diagonals down): bring their headers and flag rows
-    // (both 128-byte lines of a row) to L2 while this stage's runs resolve,
-    // so that their staging loads do not each wait for DRAM.
+    // to L2 while this stage's runs resolve, so that their staging loads do
+    // not each wait for DRAM.  Only a row's first 128-byte line: with at most
+    // 4 pairs per lane (nearly every traced step) the second holds no flags.
 #pragma unroll
     for (int s = 1; s <= 2; ++s) {
       const int32_t dn = d0 - 32 * s - lane;
       if (dn >= 1) {
-        const uint2* row = ts.rows + (uint32_t)dn * 32u;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 16));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(ts.rows + (uint32_t)dn * 32u));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(ts.hdr + dn));
       }
     }
