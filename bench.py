@@ -468,7 +468,7 @@ def main():
     if not args.no_e2e:
         pin = lambda a: torch.from_numpy(a).pin_memory().numpy()  # noqa: E731
         h_t, h_q, h_s = pin(t2), pin(q2), pin(seeds.view(np.uint8)).view(W.SEED_DTYPE)
-        h_out = np.zeros(2 * len(seeds), fz.RESULT_DTYPE)
+        h_out = pin(np.zeros(2 * len(seeds), fz.RESULT_DTYPE).view(np.uint8)).view(fz.RESULT_DTYPE)
         res_dev = np.frombuffer(d_out[:2 * len(seeds) * fz.RESULT_DTYPE.itemsize].cpu().numpy().tobytes(),
                                 dtype=fz.RESULT_DTYPE)
         h_cig = pin(np.zeros(int(res_dev["cigar_len"].astype(np.int64).sum()) + 16, np.uint32))   # runs written
