@@ -10,13 +10,16 @@ Default workload: the chromosome-scale batch, the largest configuration on one
 GPU -- 1,000,000 seed anchors on a synthetic 50 Mbp target and a query derived
 from it (15% substitutions, 3% indels, 10 kbp block inversions and moves),
 extended on both sides in 6,000 bp windows (2,000,000 one-sided extensions),
-HOXD70, gap open 400, extend 30, ydrop 9400.  --config 1|2|4|5 runs the others.
+HOXD70, gap open 400, extend 30, ydrop 9400.  --config 1|2|4|5 runs the others;
+--wide runs a batch for the general-band path (512 extensions of 3 kbp windows
+at a y-drop of 40,000, bands of about a thousand rows: workloads.make_wide), and
+--dp edit|dtw the DPX article's other two dynamic programs.
 Metric: GCUPS = live DP cells of the inspector sweeps per second of the whole
 step; extensions/s is reported beside it.  The roofline line names the kernel
 that took the most time in the timed steps (CUDA events on the library's stream
 around its phases) and divides its own cells by its own time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fz|reference] [--config C]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fz|reference] [--config C | --wide | --dp P]
 
 Multi-GPU (torchrun): the batch's seeds are split into contiguous shards, one
 per rank (gapped_smith_waterman_gb300.multi.shard_bounds); every rank extends
@@ -70,7 +73,7 @@ PHASES = {
     0: ("inspector (register-window sweep; first tier two 16-bit rows per register)", "extend_fast.cu",
         "plain_live_cells", "pair", "inspector_traffic.json"),
     1: ("inspector, wide band (k_wide<0>)", "extend_wide.cu", "live_cells", "32", None),
-    3: ("executor (k_extend<K,1,*> replay with 4-bit direction codes)", "extend_fast.cu",
+    3: ("executor (k_extend<K,1,*> / k_wide<1> replay with 4-bit direction codes)", "extend_fast.cu",
         "exec_live_cells", "32", "executor_traffic.json"),
     4: ("traceback walk and records (k_emit_*)", "pipeline.cu", None, "32", None),
 }
@@ -109,6 +112,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seeds", type=int, default=0, help="use only the first N seeds (profiling captures)")
+    ap.add_argument("--wide", action="store_true",
+                    help="time the general-band path instead: 512 extensions of 3 kbp windows at y-drop 40,000")
     ap.add_argument("--dp", choices=["edit", "dtw"], default=None,
                     help="time the DPX article's other dynamic programs instead (512 edit distances of "
                          "1024 x 1024, or 256 DTWs of 800 x 800)")
@@ -253,7 +258,7 @@ def run_reference(args, ws, rank):
     that one step takes about --ref-step-seconds."""
     if rank != 0:
         return
-    w = W.make(args.config)
+    w = W.make_wide() if args.wide else W.make(args.config)
     import oracle
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(321)
@@ -402,7 +407,7 @@ def main():
         B.build()
     if ws > 1:
         dist.barrier()
-    w = W.make(args.config)
+    w = W.make_wide() if args.wide else W.make(args.config)
     t2, q2 = W.pack2(w.target), W.pack2(w.query)
     seeds = rank_seeds(w.seeds[:args.seeds] if args.seeds else w.seeds, rank, ws)
     ext = fz.Extender.for_workload(w, device=dev)
@@ -540,7 +545,7 @@ def main():
                      "frac_of_measured": (achieved / measured_peak) if (achieved and measured_peak) else None,
                      "measured_basis": f"fz_bench_int_rates {MEASURED_RATE[kind]} (the costed cell loop)",
                      "int_rates_gops": {k: v / 1e9 for k, v in (rates or {}).items()},
-                     "traffic": traffic_for_kernel(kernel, args.config),
+                     "traffic": traffic_for_kernel(kernel, "wide" if args.wide else args.config),
                      "traffic_unit": "DRAM bytes per step of this kernel (ncu, scaled to the full batch)",
                      "kernel_ms_per_step": k_ms / args.steps},
         "phase_ms_per_step": [round(x / args.steps, 4) for x in phase_tot],

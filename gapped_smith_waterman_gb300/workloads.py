@@ -299,6 +299,19 @@ def make_cfg3(n_anchors: int = 1_000_000, t_len: int = 50_000_000, window: int =
                     f"{n_anchors} two-sided anchors on a {t_len} bp target")
 
 
+def make_wide(n_pairs: int = 512, win: int = 3000) -> Workload:
+    """A batch for the general-band path (not one of the five configurations):
+    n_pairs right extensions over win x win windows, the query a mutated copy of
+    the whole target window (10% substitutions, 2% indels of mean length 3), and
+    a y-drop of 40,000, so that the live bands hold about a thousand rows, more
+    than the register windows' 512."""
+    rng = rng_for(6)
+    hom = np.full(n_pairs, win)
+    w = _pairs_workload("wide-band-3kbp", rng, n_pairs, win, hom, 0.10, 0.02, 3.0,
+                        f"{n_pairs} right extensions, {win} bp windows, homologous throughout, y-drop 40000")
+    return dataclasses.replace(w, ydrop=40000)
+
+
 MAKERS = {1: make_cfg1, 2: make_cfg2, 3: make_cfg3, 4: make_cfg4, 5: make_cfg5}
 
 

@@ -39,6 +39,23 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"] == "short-256bp"
 
 
+def test_wide_band_workload_and_its_reference_line():
+    """The general-band batch: 512 right extensions of 3 kbp windows at y-drop
+    40,000, each query a mutated copy of its whole target window; the
+    reference arm times the oracle on it."""
+    w = W.make_wide()
+    assert w.ydrop == 40000 and w.max_len == 3000 and len(w.seeds) == 512
+    assert np.all(w.seeds["side"] == W.SIDE_RIGHT)
+    import oracle
+    t0, q0 = w.target[:300], w.query[:300]
+    d = oracle.edit_distance(t0, q0)                              # homologous, not identical
+    assert 0 < d < 0.35 * 300 < oracle.edit_distance(t0, w.query[3000:3300])
+    p = _run(["--impl", "reference", "--wide", "--steps", "1", "--warmup", "0", "--ref-step-seconds", "1"])
+    assert p.returncode == 0, p.stderr
+    d = json.loads([l for l in p.stdout.splitlines() if l.strip()][0])
+    assert d["config"]["workload"] == "wide-band-3kbp" and d["value"] > 0
+
+
 def test_reference_arm_other_ranks_print_nothing():
     p = _run(["--impl", "reference", "--config", "1", "--steps", "1", "--warmup", "0"],
              {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
