@@ -1095,12 +1095,15 @@ __device__ __forceinline__ uint32_t ck_write_pair(const WorkArgs& wa, const Pair
 // Warp-uniform control state of the pair sweep.  Stored values are score
 // minus B; T is the prune threshold, pend the part of its rises not yet
 // moved out of the stored values, wbest2 the stored h of a cell scoring best
-// in both halves.  The best cell is located lazily: a rise of the best score
-// records its anti-diagonal (dbest) and copies the window's h values to the
-// warp's snapshot buffer (pair_after), and pair_best_row finds the cell's row
-// when a checkpoint or the result needs it.
+// in both halves.  A rise of the best score records its anti-diagonal
+// (dbest).  The traced sweep locates the best cell lazily: the rise copies the
+// window's h values to the warp's snapshot buffer (pair_after), and
+// pair_best_row finds the cell's row when a checkpoint or the result needs
+// it.  The plain sweep, whose rises are rare on short alignments, finds the
+// row at once (bi).
 struct PairCtl {
   int32_t b, d, best, dbest, d_last;
+  int32_t bi;                // plain sweep: row of the best cell
   int32_t B, T, pend;
   uint32_t wbest2;
   uint32_t lb2;              // live_mask bias: 0x8000 - the stored threshold
@@ -1116,10 +1119,10 @@ struct PairCtl {
 constexpr int SNAP_WM = 32 * PK, SNAP_WIN = 32 * PK + 1, SNAP_WORDS = 32 * PK + 2;
 
 // After each step: the anti-diagonal's best (warp max of the stored h), a
-// rise of the best score (with a snapshot of the window), the last live
-// anti-diagonal, and one ballot with row b's liveness (bit 0, lane 0) and the
-// top lane's (bit 31, lane 31).
-template <int NP>
+// rise of the best score (traced: with a snapshot of the window; plain: with
+// the best cell's row), the last live anti-diagonal, and one ballot with row
+// b's liveness (bit 0, lane 0) and the top lane's (bit 31, lane 31).
+template <int NP, bool TR>
 __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_t lm2, const Params& p, int lane,
                                                int32_t* sT, uint32_t m0, uint32_t m31, uint32_t* snap,
                                                uint32_t& wmd_out) {
@@ -1131,10 +1134,20 @@ __device__ __forceinline__ uint32_t pair_after(PairState& L, PairCtl& c, uint32_
   const uint32_t bits = __ballot_sync(FULL, ((L.H[0] & m0) | (lmd & m31)) != 0u);
   if (wmd > c.wbest2) {                     // implies a live cell (wbest2 > 0)
     const int32_t wm = (int32_t)lo16(wmd);
+    if (TR) {
 #pragma unroll
-    for (int q = 0; q < NP; ++q) snap[32 * q + lane] = L.H[q];   // (each lane reads back only its own words)
-    snap[SNAP_WM] = (uint32_t)wm;                                // (the same value from every lane)
-    snap[SNAP_WIN] = (uint32_t)c.b | (NP << 24);
+      for (int q = 0; q < NP; ++q) snap[32 * q + lane] = L.H[q];   // (each lane reads back only its own words)
+      snap[SNAP_WM] = (uint32_t)wm;                                // (the same value from every lane)
+      snap[SNAP_WIN] = (uint32_t)c.b | (NP << 24);
+    } else {
+      int rf = 2 * NP;
+#pragma unroll
+      for (int r = 2 * NP - 1; r >= 0; --r) rf = (int32_t)prow<NP>(L.H, r) == wm ? r : rf;
+      const uint32_t fm = __ballot_sync(FULL, rf < 2 * NP);
+      const int Ln = __ffs(fm) - 1;
+      const int rr = __shfl_sync(FULL, rf, Ln);
+      c.bi = c.b + Ln * 2 * NP + rr;
+    }
     c.dbest = c.d;
     c.best = wm + oe + c.B;
     if (c.d <= 2 * EAGER_N && lane == 0) sT[c.d] = c.best;
@@ -1175,7 +1188,9 @@ __device__ __forceinline__ int pair_snap_row(const uint32_t* snap, int lane, int
   return rf;
 }
 
-__device__ __forceinline__ int32_t pair_best_row(const uint32_t* snap, int lane) {
+template <bool TR>
+__device__ __forceinline__ int32_t pair_best_row(const PairCtl& c, const uint32_t* snap, int lane) {
+  if (!TR) return c.bi;
   const int32_t wm = (int32_t)snap[SNAP_WM];
   if (wm < 0) return 0;
   const uint32_t win = snap[SNAP_WIN];
@@ -1311,7 +1326,7 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
           const uint32_t lm2 = pstep<NP, false, false, TR>(L, ne2, noe2, oe2, c.lb2, lane, qb, 0u, 0, 0, c.live2, acc);
           ++c.d;
           if (TR) trace_store<NP>(ts, c, lane, acc);
-          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
+          bits = pair_after<NP, TR>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
         }
         if ((bits & 1u) || c.d == d_fast || wmd == 0u) break;
         {
@@ -1321,7 +1336,7 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
           ++c.b;
           ++c.d;
           if (TR) trace_store<NP>(ts, c, lane, acc);
-          bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
+          bits = pair_after<NP, TR>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
         }
         if ((int32_t)bits < 0 || c.d == d_fast || wmd == 0u) break;
       }
@@ -1352,7 +1367,7 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
       c.d = dn;
       if (TR) trace_store<NP>(ts, c, lane, acc);
       uint32_t wmd;
-      const uint32_t bits = pair_after<NP>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
+      const uint32_t bits = pair_after<NP, TR>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
       c.rowb_alive = bits & 1u;
       c.top = (int32_t)bits < 0;
       // (no overflow once the window reaches row m: no row lies beyond it)
@@ -1547,10 +1562,11 @@ __device__ __forceinline__ void pair_resize(PairState& L, const PairCtl& c, int 
   res_init(tr, p.t2, p.t_len, w.tg0, w.dir, (int64_t)c.b + 64 * NPN);   // target rows entering at the new top
 }
 
+template <bool TR>
 __device__ __forceinline__ uint32_t pair_ckpt(int np, const WorkArgs& wa, const PairState& L, int lane,
                                               uint32_t head, const PairCtl& c, int32_t oe, const int32_t* sT,
                                               const uint32_t* snap) {
-  const int32_t bi = pair_best_row(snap, lane);
+  const int32_t bi = pair_best_row<TR>(c, snap, lane);
   const CkScalars cs{c.b, c.d, c.best, bi, c.dbest - bi, c.d_last};
   return np == NP_SMALL ? ck_write_pair<NP_SMALL>(wa, L, lane, head, cs, c.B, oe, c.cnt, 0u, sT)
                         : ck_write_pair<PK>(wa, L, lane, head, cs, c.B, oe, c.cnt, 0u, sT);
@@ -1564,7 +1580,7 @@ __device__ __forceinline__ uint32_t pair_ckpt(int np, const WorkArgs& wa, const 
 // so that the executor splits its replay at them.
 __device__ __forceinline__ void ring_ckpt(int np, const TraceSlot& ts, uint32_t k, const PairState& L, int lane,
                                           const PairCtl& c, int32_t oe, const int32_t* sT, const uint32_t* snap) {
-  const int32_t bi = pair_best_row(snap, lane);
+  const int32_t bi = pair_best_row<true>(c, snap, lane);
   const CkScalars cs{c.b, c.d, c.best, bi, c.dbest - bi, c.d_last};
   int32_t* dst = ts.ring + (uint64_t)k * CK_SLOT_WORDS;
   if (np == NP_SMALL) ck_fill_pair<NP_SMALL>(dst, L, lane, 0u, cs, c.B, oe, c.cnt, 0u, sT);
@@ -1622,7 +1638,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   }
   const int32_t m = w.m, n = w.n, oe = p.oe, mn = w.m + w.n;
   PairCtl c;
-  c.b = 0; c.d = 0; c.best = 0; c.dbest = 0; c.d_last = 0;
+  c.b = 0; c.d = 0; c.best = 0; c.dbest = 0; c.d_last = 0; c.bi = 0;
   if (lane == 0) snap[SNAP_WM] = 0xffffffffu;   // best cell: the origin
   c.T = threshold(0, p.ydrop);
   c.B = c.T - PMG;                          // stored value = score-space value - B
@@ -1690,7 +1706,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
       continue;
     }
     if (!TR && ((uint32_t)c.d & ck_mask) == 0u && c.d - c.dbest <= wa.ckpt_recent)
-      head = pair_ckpt(np, wa, L, lane, head, c, oe, sT, snap);
+      head = pair_ckpt<TR>(np, wa, L, lane, head, c, oe, sT, snap);
     if (TR && wa.ckpt && ((uint32_t)c.d & (wa.tring_every - 1u)) == 0u && nring < wa.tring) {
       ring_ckpt(np, ts, nring, L, lane, c, oe, sT, snap);
       ++nring;
@@ -1706,7 +1722,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
   }
   if (overflow && wa.ckpt) {
     if (TR && nring) head = ring_publish(wa, ts, nring, lane);
-    head = pair_ckpt(PK, wa, L, lane, head, c, oe, sT, snap);
+    head = pair_ckpt<TR>(PK, wa, L, lane, head, c, oe, sT, snap);
   }
 
   uint64_t tot = c.cnt;
@@ -1725,7 +1741,7 @@ __device__ void run_inspect_pair(const Params& p, const WorkArgs& wa, uint32_t e
     }
     return;
   }
-  const int32_t best = c.best, bi = pair_best_row(snap, lane), bj = c.dbest - bi;
+  const int32_t best = c.best, bi = pair_best_row<TR>(c, snap, lane), bj = c.dbest - bi;
   uint64_t path = 0;
   uint32_t npath = 0;
   uint32_t flags = FZ_FLAG_DONE;
