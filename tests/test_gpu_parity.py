@@ -322,6 +322,34 @@ def test_wide_band_beyond_the_ring():
     assert st.wide == len(pairs)
 
 
+def test_wide_band_fuzz():
+    """The wide-band sweep on random non-symmetric scorings (a transposed
+    substitution lookup fails here) with no y-drop: every band outgrows the
+    512-row tier, some also the 2,048-row ring; then a matrix outside the
+    byte range, which sends every extension to the wide path from the start."""
+    rng = np.random.default_rng(78)
+    for it in range(3):
+        sub = rng.integers(-120, 121, size=(4, 4)).astype(np.int32)
+        sub[np.arange(4), np.arange(4)] = rng.integers(40, 128, 4)
+        pairs = []
+        for _ in range(10):
+            L = int(rng.integers(600, 2300))
+            t = rng.integers(0, 4, L).astype(np.uint8)
+            q = W.mutate(rng, t, 0.15, 0.03, 3.0) if rng.random() < 0.7 else rng.integers(0, 4, L).astype(np.uint8)
+            pairs.append((t, q))
+        w, _ = _batch_from_pairs(pairs, sub=sub, o=int(rng.integers(50, 500)), e=int(rng.integers(5, 60)),
+                                 ydrop=W.YDROP_INF)
+        gres, gcig, st, ores = _check(w, label=f"wide fuzz {it}")
+        assert st.wide == len(pairs)
+    sub = rng.integers(-300, 301, size=(4, 4)).astype(np.int32)
+    sub[np.arange(4), np.arange(4)] = rng.integers(150, 300, 4)
+    pairs = [(rng.integers(0, 4, int(rng.integers(1, 400))).astype(np.uint8),) * 2 for _ in range(12)]
+    pairs = [(t, W.mutate(rng, t, 0.1, 0.02, 2.0)) for (t, _) in pairs]
+    w, _ = _batch_from_pairs(pairs, sub=sub, o=900, e=70, ydrop=20000)
+    gres, gcig, st, ores = _check(w, label="wide fuzz, matrix outside the byte range")
+    assert st.wide == 2 * len(pairs)     # every extension slot, both sides of each seed
+
+
 def test_matrix_outside_byte_range_uses_general_path():
     rng = np.random.default_rng(9)
     sub = (W.HOXD70 * 3).astype(np.int32)          # entries beyond [-128, 127]
