@@ -226,7 +226,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
     wa.ckpt_cap = (uint32_t)std::min<uint64_t>(ctx->ckpt.bytes / (CK_SLOT_WORDS * sizeof(int32_t)), 0xffffff00ull);
     wa.ckpt_used = &dc->ckpt_used;
     wa.ckpt_every = ctx->ckpt_every;
-    wa.ckpt_recent = ctx->ckpt_every;
+    wa.ckpt_recent = ctx->ckpt_every / 4;
   }
 
   // 1. inspector
