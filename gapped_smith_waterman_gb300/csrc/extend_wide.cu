@@ -23,7 +23,7 @@ namespace fz {
 
 namespace {
 
-constexpr int CW = 4;               // warps per block
+constexpr int CW = 8;               // warps per block
 constexpr int CT = CW * 32;         // threads per block
 constexpr int RING_MAX = 2048;      // rows of the shared-memory ring at most
 
