@@ -11,8 +11,9 @@
 // ring indexed by target row modulo the ring size; the anti-diagonal's
 // maximum (earliest row on ties) and live range are combined across the warps
 // once per anti-diagonal, in the same barrier that publishes its cells.  When
-// a band is wider than the ring, the three anti-diagonals move to a per-block
-// global scratch indexed by row and the sweep continues there.  Liveness
+// a band is wider than the ring, the two anti-diagonals still read move to a
+// per-block global scratch indexed by row and the sweep continues there, with
+// all three buffers in it.  Liveness
 // follows the y-drop rule as written: dead cells hold NEG in S, I and D.
 #include <cuda_runtime.h>
 
