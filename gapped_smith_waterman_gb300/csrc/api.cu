@@ -334,7 +334,7 @@ fz_status run_extend(fz_ctx* ctx, uint32_t n_seeds, fz_result* d_out, cudaStream
   for (int t = 0; t < 3; ++t)
     CU(launch_scan_u64(ctx->seg_cnt.as<uint64_t>() + (size_t)t * n_ext, n_ext, ctx->scan_tmp.as<uint64_t>(),
                        &dc->seg_total[t], st));
-  ctx->launches += 3 + 6 + 1 + 9;
+  ctx->launches += 3 + 1 + 5 * scan_launch_count(n_ext);
   mark(ctx, 3, st);
   CU(cudaMemcpyAsync(ctx->h_cnt, dc, sizeof(Counters), cudaMemcpyDeviceToHost, st));
   CU(cudaStreamSynchronize(st));
@@ -704,7 +704,7 @@ fz_status fz_extend_batch_host(fz_ctx* ctx, const uint8_t* h_target2, uint64_t t
     used = ctx->h_cnt->cig_packed;
     CU(ctx->cigar_packed.ensure(std::max<uint64_t>(used, 1) * 4));
     CU(launch_cig_pack(d_out, n_ext, ctx->cig_cap.as<uint64_t>(), dc, ctx->cigar_packed.as<uint32_t>(), st));
-    ctx->launches += 5;
+    ctx->launches += 2 + scan_launch_count(n_ext);
     dc = ctx->cigar_packed.as<uint32_t>();
   }
   if (n_seeds) CU(cudaMemcpyAsync(h_out, ctx->out_res.p, (size_t)n_seeds * 2 * sizeof(fz_result), cudaMemcpyDeviceToHost, st));

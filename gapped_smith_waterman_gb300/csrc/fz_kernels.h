@@ -112,6 +112,7 @@ cudaError_t launch_order(const Params& p, uint32_t n_ext, uint8_t* key, uint32_t
                          uint32_t* list, uint32_t* n_long, uint32_t min_long, cudaStream_t st);
 cudaError_t launch_scatter(const PipeArgs& a, cudaStream_t st);
 // exclusive scan of n uint64 values in place; total written to *total
+uint32_t scan_launch_count(uint32_t n);   // kernels one launch_scan_u64 of n elements launches
 cudaError_t launch_scan_u64(uint64_t* data, uint32_t n, uint64_t* block_tmp, uint64_t* total, cudaStream_t st);
 uint32_t scan_tmp_elems(uint32_t n);
 

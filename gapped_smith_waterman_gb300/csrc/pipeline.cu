@@ -355,6 +355,24 @@ __global__ void __launch_bounds__(SCAN_T) k_scan2(uint64_t* bsum, uint32_t nb, u
   if (threadIdx.x == 0) *total_out = carry;
 }
 
+// A whole scan in one block (small arrays): chunks of SCAN_E elements in
+// order, each scanned in the block and offset by the total of those before.
+__global__ void __launch_bounds__(SCAN_T) k_scan_small(uint64_t* d, uint32_t n, uint64_t* total_out) {
+  __shared__ uint64_t wt[32];
+  uint64_t carry = 0;
+  for (uint32_t c = 0; c < n; c += SCAN_E) {
+    const uint32_t i0 = c + 2 * threadIdx.x;
+    const uint64_t a = i0 < n ? d[i0] : 0, b = i0 + 1 < n ? d[i0 + 1] : 0;
+    uint64_t total;
+    const uint64_t ex = block_excl_scan(a + b, wt, total);
+    if (i0 < n) d[i0] = carry + ex;
+    if (i0 + 1 < n) d[i0 + 1] = carry + ex + a;
+    carry += total;
+    __syncthreads();                               // (wt is reused by the next chunk)
+  }
+  if (threadIdx.x == 0) *total_out = carry;
+}
+
 __global__ void k_scan3(uint64_t* d, uint32_t n, const uint64_t* bsum) {
   const uint64_t i = (uint64_t)blockIdx.x * SCAN_E + threadIdx.x;
   const uint64_t add = bsum[blockIdx.x];
@@ -774,10 +792,19 @@ cudaError_t launch_scatter(const PipeArgs& a, cudaStream_t st) {
 
 uint32_t scan_tmp_elems(uint32_t n) { return (n + SCAN_E - 1) / SCAN_E + 1; }
 
+uint32_t scan_launch_count(uint32_t n) {
+  const uint32_t nb = (n + SCAN_E - 1) / SCAN_E;
+  return nb == 0 ? 0u : (nb <= 16 ? 1u : 3u);
+}
+
 cudaError_t launch_scan_u64(uint64_t* data, uint32_t n, uint64_t* block_tmp, uint64_t* total, cudaStream_t st) {
   const uint32_t nb = (n + SCAN_E - 1) / SCAN_E;
   if (nb == 0) {
     cudaMemsetAsync(total, 0, sizeof(uint64_t), st);
+    return cudaGetLastError();
+  }
+  if (nb <= 16) {                                  // up to 32,768 elements: one launch
+    k_scan_small<<<1, SCAN_T, 0, st>>>(data, n, total);
     return cudaGetLastError();
   }
   k_scan1<<<nb, SCAN_T, 0, st>>>(data, n, block_tmp);
