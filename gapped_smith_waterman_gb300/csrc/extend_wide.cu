@@ -15,6 +15,10 @@
 // per-block global scratch indexed by row and the sweep continues there, with
 // all three buffers in it.  Liveness
 // follows the y-drop rule as written: dead cells hold NEG in S, I and D.
+// With windows of up to SB_MAX_LEN bases the block also stages both windows'
+// bases in shared memory (2 bits each, 16 to a word, loaded once per
+// extension), so a cell reads its two bases there instead of from global
+// memory.
 #include <cuda_runtime.h>
 
 #include "fz_dev.cuh"
@@ -27,6 +31,10 @@ namespace {
 constexpr int CW = 8;               // warps per block
 constexpr int CT = CW * 32;         // threads per block
 constexpr int RING_MAX = 2048;      // rows of the shared-memory ring at most
+constexpr int32_t SB_MAX_LEN = 4080;  // windows staged in shared memory up to this length (3 blocks per SM)
+
+// Words of staged bases per window (window positions 0 .. max_len, 16 to a word).
+__host__ __device__ inline int32_t sb_words(int32_t max_len) { return max_len / 16 + 1; }
 
 // Ring rows for windows of up to max_len rows: a power of two holding a whole
 // window when it fits RING_MAX.
@@ -71,10 +79,11 @@ struct Bufs {
 
 // Anti-diagonals from s.dn on, until the sweep ends (true) or, in the ring, a
 // band wider than the ring (false: s.dn is the anti-diagonal still to do).
-template <bool TRACE, bool SMEM>
+template <bool TRACE, bool SMEM, bool SB>
 __device__ bool wide_run(const Params& p, const Window& w, WideState& s, const Bufs<SMEM>& B, int32_t ring,
                          int32_t d_stop, uint32_t W, uint8_t* tbase, int32_t* lo_arr, const int32_t* s_sub,
-                         int4 (*red)[CW], uint32_t& cnt, int tid, int warp, int lane) {
+                         const uint32_t* sb_t, const uint32_t* sb_q, int4 (*red)[CW], uint32_t& cnt, int tid,
+                         int warp, int lane) {
   const int32_t m = w.m, n = w.n, oe = p.oe, e = p.e;
   for (; s.dn <= m + n; ++s.dn) {
     const int32_t dn = s.dn;
@@ -107,8 +116,8 @@ __device__ bool wide_run(const Params& p, const Window& w, WideState& s, const B
       const int32_t Dv = i >= 1 ? imax(du - e, su - oe) : NEG;
       int32_t G = NEG;
       if (act && i >= 1 && j >= 1) {
-        const uint32_t tb = base_at(p.t2, p.t_len, w.tg0, w.dir, i);
-        const uint32_t qb = base_at(p.q2, p.q_len, w.qg0, w.dir, j);
+        const uint32_t tb = SB ? (sb_t[i >> 4] >> (2 * (i & 15))) & 3u : base_at(p.t2, p.t_len, w.tg0, w.dir, i);
+        const uint32_t qb = SB ? (sb_q[j >> 4] >> (2 * (j & 15))) & 3u : base_at(p.q2, p.q_len, w.qg0, w.dir, j);
         G = sd + s_sub[tb * 4 + qb];
       }
       const int32_t S = imax(G, imax(Iv, Dv));
@@ -167,10 +176,10 @@ __device__ bool wide_run(const Params& p, const Window& w, WideState& s, const B
   return true;
 }
 
-template <bool TRACE>
+template <bool TRACE, bool SB>
 __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint32_t idx, int tid, int32_t* ring_buf,
-                         int32_t ring, int32_t* gbuf, int32_t cap, const int32_t* s_sub, int4 (*red)[CW],
-                         unsigned long long* s_sum) {
+                         int32_t ring, int32_t* gbuf, int32_t cap, const int32_t* s_sub, uint32_t* sb_t, uint32_t* sb_q,
+                         int4 (*red)[CW], unsigned long long* s_sum) {
   const int warp = tid >> 5, lane = tid & 31;
   const Window w = make_window(p, ext);
   ExtRec* R = wa.rec + ext;
@@ -201,8 +210,14 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
   uint32_t cnt = tid == 0 ? 1u : 0u;
   const Bufs<true> RB{ring_buf, ring, ring - 1};
   if (tid == 0) { *RB.at(0, 0, 0) = 0; *RB.at(0, 1, 0) = NEG; *RB.at(0, 2, 0) = NEG; }
+  if (SB) {
+    // word k: window positions 16 k .. 16 k + 15 (row or column i at bits 2 (i % 16))
+    for (int32_t k = tid; k <= w.m / 16; k += CT) sb_t[k] = fetch16(p.t2, p.t_len, w.tg0, w.dir, 16 * (int64_t)k);
+    for (int32_t k = tid; k <= w.n / 16; k += CT) sb_q[k] = fetch16(p.q2, p.q_len, w.qg0, w.dir, 16 * (int64_t)k);
+  }
   __syncthreads();
-  if (!wide_run<TRACE, true>(p, w, s, RB, ring, d_stop, W, tbase, lo_arr, s_sub, red, cnt, tid, warp, lane)) {
+  if (!wide_run<TRACE, true, SB>(p, w, s, RB, ring, d_stop, W, tbase, lo_arr, s_sub, sb_t, sb_q, red, cnt, tid,
+                                 warp, lane)) {
     // the band outgrew the ring: move the two previous anti-diagonals (the
     // only ones still read) to the global scratch, rows at their own index
     const Bufs<false> GB{gbuf, cap, 0x7fffffff};
@@ -212,7 +227,8 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
 #pragma unroll
         for (int c = 0; c < 3; ++c) *GB.at(bs[q].k, c, i) = *RB.at(bs[q].k, c, i);
     __syncthreads();
-    wide_run<TRACE, false>(p, w, s, GB, cap, d_stop, W, tbase, lo_arr, s_sub, red, cnt, tid, warp, lane);
+    wide_run<TRACE, false, SB>(p, w, s, GB, cap, d_stop, W, tbase, lo_arr, s_sub, sb_t, sb_q, red, cnt, tid, warp,
+                               lane);
   }
   // live cells: warp sums, then thread 0 adds the warps' (the barrier also
   // ends every read of the ring before the next extension writes it)
@@ -237,9 +253,11 @@ __device__ void wide_ext(const Params& p, const WorkArgs& wa, uint32_t ext, uint
   __syncthreads();   // (s_sum is rewritten by the next extension)
 }
 
-template <bool TRACE>
+template <bool TRACE, bool SB>
 __global__ void __launch_bounds__(CT) k_wide(Params p, WorkArgs wa) {
-  extern __shared__ int32_t s_ring[];             // 9 x ring rows: S, I, D of three anti-diagonals
+  // dynamic shared memory: 9 x ring rows (S, I, D of three anti-diagonals),
+  // then (SB) the target window's and the query window's staged bases
+  extern __shared__ int32_t s_ring[];
   __shared__ int32_t s_sub[16];
   __shared__ int4 s_red[2][CW];
   __shared__ unsigned long long s_sum[CW];
@@ -247,6 +265,8 @@ __global__ void __launch_bounds__(CT) k_wide(Params p, WorkArgs wa) {
   const int tid = threadIdx.x;
   if (tid < 16) s_sub[tid] = p.sub[tid];
   const int32_t ring = ring_rows(p.max_len);
+  uint32_t* sb_t = reinterpret_cast<uint32_t*>(s_ring + 9 * ring);
+  uint32_t* sb_q = sb_t + sb_words(p.max_len);
   int32_t* gbuf = wa.scratch + (uint64_t)blockIdx.x * wa.scratch_stride;
   const int32_t cap = (int32_t)(wa.scratch_stride / 9);
   for (;;) {
@@ -261,41 +281,60 @@ __global__ void __launch_bounds__(CT) k_wide(Params p, WorkArgs wa) {
       const uint4 sg = wa.seg[idx];
       const uint32_t ext = wa.list[sg.x];
       if (!(wa.rec[ext].flags & FZ_FLAG_WIDE)) continue;
-      wide_ext<TRACE>(p, wa, ext, sg.x, tid, s_ring, ring, gbuf, cap, s_sub, s_red, s_sum);
+      wide_ext<TRACE, SB>(p, wa, ext, sg.x, tid, s_ring, ring, gbuf, cap, s_sub, sb_t, sb_q, s_red, s_sum);
     } else {
-      wide_ext<TRACE>(p, wa, wa.list[idx], idx, tid, s_ring, ring, gbuf, cap, s_sub, s_red, s_sum);
+      wide_ext<TRACE, SB>(p, wa, wa.list[idx], idx, tid, s_ring, ring, gbuf, cap, s_sub, sb_t, sb_q, s_red, s_sum);
     }
   }
 }
 
 size_t ring_bytes(int32_t max_len) { return (size_t)9 * ring_rows(max_len) * sizeof(int32_t); }
 
+bool staged(int32_t max_len) { return max_len <= SB_MAX_LEN; }
+
+// Dynamic shared memory of a launch: the ring, and the staged bases when the
+// windows are short enough.
+size_t wide_smem(int32_t max_len) {
+  return ring_bytes(max_len) + (staged(max_len) ? 2 * (size_t)sb_words(max_len) * sizeof(uint32_t) : 0);
+}
+
+const void* kernel_of(bool trace, bool sb) {
+  if (trace) return sb ? reinterpret_cast<const void*>(k_wide<true, true>) : reinterpret_cast<const void*>(k_wide<true, false>);
+  return sb ? reinterpret_cast<const void*>(k_wide<false, true>) : reinterpret_cast<const void*>(k_wide<false, false>);
+}
+
 }  // namespace
 
 uint64_t wide_scratch_elems(int32_t max_len) { return 9ull * (uint64_t)(max_len + 1); }
 
 int wide_blocks_per_sm(int32_t max_len) {
-  const size_t rb = ring_bytes(max_len);
+  // every variant may take the largest dynamic shared memory, so that
+  // contexts with other window caps can launch too
+  const int limit = (int)(ring_bytes(RING_MAX) + 2 * (size_t)sb_words(SB_MAX_LEN) * sizeof(uint32_t));
+  for (int t = 0; t < 2; ++t)
+    for (int b = 0; b < 2; ++b)
+      if (cudaFuncSetAttribute(kernel_of(t, b), cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess)
+        return 0;
   int best = 0;
   for (int t = 0; t < 2; ++t) {
-    const void* f = t ? reinterpret_cast<const void*>(k_wide<true>) : reinterpret_cast<const void*>(k_wide<false>);
-    // the limit of the largest ring, so that contexts with other window caps can launch too
-    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring_bytes(RING_MAX)) != cudaSuccess)
-      return 0;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, CT, rb) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel_of(t, staged(max_len)), CT, wide_smem(max_len)) !=
+        cudaSuccess)
+      return 0;
     best = t ? (nb < best ? nb : best) : nb;
   }
   return best;
 }
 
 cudaError_t launch_inspect_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  k_wide<false><<<grid, CT, ring_bytes(p.max_len), st>>>(p, wa);
+  if (staged(p.max_len)) k_wide<false, true><<<grid, CT, wide_smem(p.max_len), st>>>(p, wa);
+  else k_wide<false, false><<<grid, CT, wide_smem(p.max_len), st>>>(p, wa);
   return cudaGetLastError();
 }
 
 cudaError_t launch_execute_wide(const Params& p, const WorkArgs& wa, int grid, cudaStream_t st) {
-  k_wide<true><<<grid, CT, ring_bytes(p.max_len), st>>>(p, wa);
+  if (staged(p.max_len)) k_wide<true, true><<<grid, CT, wide_smem(p.max_len), st>>>(p, wa);
+  else k_wide<true, false><<<grid, CT, wide_smem(p.max_len), st>>>(p, wa);
   return cudaGetLastError();
 }
 

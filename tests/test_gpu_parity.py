@@ -322,6 +322,21 @@ def test_wide_band_beyond_the_ring():
     assert st.wide == len(pairs)
 
 
+def test_wide_band_long_windows():
+    """Windows longer than the wide path stages in shared memory (4,080
+    bases): it reads the bases from global memory instead; records and
+    CIGARs equal the oracle's."""
+    rng = np.random.default_rng(13)
+    pairs = []
+    for L in (4200, 4400):
+        t = rng.integers(0, 4, L).astype(np.uint8)
+        pairs.append((t, W.mutate(rng, t, 0.1, 0.02, 3.0)))
+    w, _ = _batch_from_pairs(pairs, ydrop=40000)
+    assert w.max_len > 4080
+    gres, gcig, st, ores = _check(w, label="wide band, long windows")
+    assert st.wide == len(pairs)
+
+
 def test_wide_band_fuzz():
     """The wide-band sweep on random non-symmetric scorings (a transposed
     substitution lookup fails here) with no y-drop: every band outgrows the
