@@ -322,6 +322,29 @@ def test_wide_band_beyond_the_ring():
     assert st.wide == len(pairs)
 
 
+def test_wide_band_both_sides():
+    """Two-sided anchors in the middle of long homologous pairs at y-drop
+    40,000: both extensions of every seed take the wide path, the left one
+    reading its windows backwards (the staged bases in reverse order), with
+    windows short enough to be staged and, in a second batch, too long."""
+    rng = np.random.default_rng(14)
+    for L, mid in ((3000, 1400), (9000, 4300)):
+        T, Q, seeds = [], [], np.zeros(3, W.SEED_DTYPE)
+        for k in range(3):
+            t = rng.integers(0, 4, L).astype(np.uint8)
+            q = W.mutate(rng, t, 0.1, 0.02, 3.0)[:L]
+            q = np.concatenate([q, rng.integers(0, 4, L - q.size).astype(np.uint8)])
+            seeds[k]["t_pos"] = k * L + mid
+            seeds[k]["q_pos"] = k * L + mid + int(rng.integers(-3, 4))
+            T.append(t)
+            Q.append(q)
+        seeds["side"] = W.SIDE_BOTH
+        w = W.Workload("both", np.concatenate(T), np.concatenate(Q), seeds, W.HOXD70.copy(), 400, 30, 40000,
+                       L // 2 - 100 if L < 5000 else L // 2, W.MODE_EXTEND)
+        gres, gcig, st, ores = _check(w, label=f"wide band, both sides, {L} bp pairs")
+        assert st.wide >= 4
+
+
 def test_wide_band_long_windows():
     """Windows longer than the wide path stages in shared memory (4,080
     bases): it reads the bases from global memory instead; records and
