@@ -116,10 +116,10 @@ typedef struct {
  * (window cap per side).  |score| bounds: max(|sub|, gap_open + gap_extend) *
  * (2 * max_len + 1) must stay below 2^28 (int32 DP without wrap-around).
  * The context owns its device scratch and arenas; the calling thread's current
- * device is used.  It also sets, once per process and device, the largest
- * dynamic shared memory of the library's general-band kernels (a function
- * attribute, the same value whatever max_len, so contexts with different
- * window caps coexist).  Returns FZ_ERR_ARG on a bad parameter, FZ_ERR_OOM or
+ * device is used.  Each call also sets the library's general-band kernels'
+ * dynamic shared-memory limit (a process-wide function attribute), always to
+ * the same value whatever max_len, so contexts with different window caps
+ * coexist.  Returns FZ_ERR_ARG on a bad parameter, FZ_ERR_OOM or
  * FZ_ERR_CUDA when the device refuses an allocation or a call (*out = NULL).
  */
 fz_status fz_create(fz_ctx** out, const int32_t sub[16], int32_t gap_open, int32_t gap_extend,
