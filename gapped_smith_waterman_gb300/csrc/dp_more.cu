@@ -7,10 +7,11 @@
 // Edit distance (unit costs, 2-bit DNA):
 //   D(i,0) = i, D(0,j) = j,
 //   D(i,j) = min(min(D(i-1,j), D(i,j-1)) + 1, D(i-1,j-1) + [a_i != b_j])
-//          = viaddmin(min(up, left), 1, diag + mismatch)
-// DTW (int32 samples, cell cost |x_i - y_j|):
+//          = viaddmin(left, 1, viaddmin(up, 1, diag + mismatch))
+// DTW (int32 samples, cell cost c = |x_i - y_j|):
 //   D(0,0) = 0, D(i,0) = D(0,j) = infinity,
-//   D(i,j) = |x_i - y_j| + vimin3(D(i-1,j), D(i,j-1), D(i-1,j-1))
+//   D(i,j) = c + min(D(i-1,j), D(i,j-1), D(i-1,j-1))
+//          = viaddmin(left, c, min(up, diag) + c)
 //
 // One warp per pair, the local fill's wavefront: the b (column) sequence is
 // cut into strips of 32 * KC columns; in a strip lane l owns KC consecutive
@@ -114,12 +115,17 @@ __global__ void __launch_bounds__(DW * 32) k_dp(Seqs<DTW> sq, const fz_pair* pai
         for (int q = 0; q < KC; ++q) {
           const int32_t up = dc[q];
           int32_t v;
+          // Only the cell to the left is on the lane's dependent chain: the
+          // minimum over the other two sources is formed off it, and one
+          // add-min joins the left one (the same values: min is associative,
+          // and no sum nears 2^31)
           if (DTW) {
             const int32_t d = ab - col[q];
-            v = __vimin3_s32(up, left, diag) + (d < 0 ? -d : d);
+            const int32_t c = d < 0 ? -d : d;
+            v = __viaddmin_s32(left, c, min(up, diag) + c);
           } else {
             const int32_t x = (int32_t)prmt(prof[q], 0u, 0x4440u | (uint32_t)ab);
-            v = __viaddmin_s32(min(up, left), 1, diag + x);
+            v = __viaddmin_s32(left, 1, __viaddmin_s32(up, 1, diag + x));
           }
           diag = up;
           dc[q] = v;
