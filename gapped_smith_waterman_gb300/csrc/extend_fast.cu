@@ -1287,13 +1287,15 @@ __device__ __forceinline__ void trace_store(const TraceSlot& ts, const PairCtl& 
 // keeps the base, then one that moves it up a row.  A loop with one kind of
 // step after the other needs no register moves between them, where a loop
 // choosing the kind per step pays for both register layouts every step.  The
-// pair leaves after its first step when row b is live (the base cannot move:
-// the next pair starts right away) and after its second when the top lane is
-// live (the next step is then taken alone).  Keeping the base while row b is
-// dead only leaves a dead row at the bottom, so every live cell stays inside
-// the window; the base never passes the base of the shift-by-one rule, and
-// the two agree whenever row b is live, which is when the window has to grow
-// or the extension overflows — the same decisions as the shift-by-one rule.
+// pair ends after its first step when row b is live (the base cannot move:
+// the next pair starts right away, inside the loop, since leaving and
+// re-entering it costs more than a step), and the loop is left after the
+// second step when the top lane is live (the next step is then taken alone).
+// Keeping the base while row b is dead only leaves a dead row at the bottom,
+// so every live cell stays inside the window; the base never passes the base
+// of the shift-by-one rule, and the two agree whenever row b is live, which is
+// when the window has to grow or the extension overflows — the same decisions
+// as the shift-by-one rule.
 //
 // Steps that cannot touch the window's edges run without edge masks: the base
 // grows by at most one row per step, so b + 64 NP <= m and b >= d - n hold
@@ -1328,7 +1330,12 @@ __device__ __forceinline__ int pair_run(PairState& L, PairCtl& c, const Params& 
           if (TR) trace_store<NP>(ts, c, lane, acc);
           bits = pair_after<NP, TR>(L, c, lm2, p, lane, sT, m0, m31, snap, wmd);
         }
-        if ((bits & 1u) || c.d == d_fast || wmd == 0u) break;
+        if ((bits & 1u) || c.d == d_fast || wmd == 0u) {
+          // row b live: the base stays and the next pair starts here, unless
+          // the window must grow or overflows (the top lane is live too)
+          if (bits != 1u || c.d == d_fast || wmd == 0u) break;
+          continue;
+        }
         {
           const uint32_t mr_new = s_mrow16[res_take(tr, p.t2, p.t_len, w.tg0, w.dir)];
           uint32_t acc[2] = {0u, 0u};
